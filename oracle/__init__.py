@@ -1,0 +1,153 @@
+"""CPU oracle for dense C = A·B -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never loads it, and the
+two share no code. The arithmetic lives in ``oracle.c`` (plain C, FP64
+accumulation, ascending k); this module only builds and loads it and marshals
+numpy arrays.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against brute
+force on small integer inputs (exact rational arithmetic), closed forms
+(ones·ones = K, I·B = B), the row-major/column-major transpose identity,
+bit-exhaustive checks of the half and bf16 decoders, and a float64 library
+matmul on the decoded values.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+LAYOUTS = {"rm": 0, "cm": 1}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so beside it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c99",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+            lib.oracle_gemm.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64, dp, dp]
+            lib.oracle_gemm_rows.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64,
+                                             vp, i64, dp, dp]
+            lib.oracle_gemm_entries.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64,
+                                                vp, vp, i64, dp, dp]
+            lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
+            lib.oracle_decode_f16.restype = ctypes.c_double
+            lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+            lib.oracle_decode_bf16.restype = ctypes.c_double
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _buf(x: np.ndarray, dtype: str, n: int) -> np.ndarray:
+    want = np.float32 if dtype == "f32" else np.uint16
+    x = np.ascontiguousarray(x).reshape(-1)
+    if x.dtype != want:
+        raise TypeError(f"{dtype} buffer must be {np.dtype(want).name}, got {x.dtype}")
+    if x.size != n:
+        raise ValueError(f"buffer holds {x.size} elements, expected {n}")
+    return x
+
+
+def _ptr(x: np.ndarray):
+    return x.ctypes.data_as(ctypes.c_void_p)
+
+
+def _variant(variant: str):
+    dtype, layout = variant.split("_")
+    return dtype, layout
+
+
+def gemm(variant: str, A: np.ndarray, B: np.ndarray, M: int, N: int, K: int):
+    """Full product of a problem, e.g. variant 'f32_rm', 'f16_cm', 'bf16_rm' (any
+    dtype/layout pair is accepted). A and B are flat storage buffers.
+
+    Returns (C, S): float64 arrays of logical shape [M, N] holding the exact-order
+    FP64 sums and sum_k |a_ik b_kj|.
+    """
+    dtype, layout = _variant(variant)
+    lib = _load()
+    a = _buf(A, dtype, M * K)
+    b = _buf(B, dtype, K * N)
+    C = np.empty(M * N, dtype=np.float64)
+    S = np.empty(M * N, dtype=np.float64)
+    rc = lib.oracle_gemm(DTYPES[dtype], LAYOUTS[layout], _ptr(a), _ptr(b), M, N, K, _ptr(C), _ptr(S))
+    if rc:
+        raise RuntimeError(f"oracle_gemm failed ({rc})")
+    if layout == "rm":
+        return C.reshape(M, N), S.reshape(M, N)
+    return C.reshape(N, M).T, S.reshape(N, M).T
+
+
+def gemm_rows(variant: str, A, B, M: int, N: int, K: int, rows):
+    """Output rows ``rows`` only: returns (C, S) of shape [len(rows), N]."""
+    dtype, layout = _variant(variant)
+    lib = _load()
+    a = _buf(A, dtype, M * K)
+    b = _buf(B, dtype, K * N)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    C = np.empty(r.size * N, dtype=np.float64)
+    S = np.empty(r.size * N, dtype=np.float64)
+    rc = lib.oracle_gemm_rows(DTYPES[dtype], LAYOUTS[layout], _ptr(a), _ptr(b), M, N, K,
+                              _ptr(r), r.size, _ptr(C), _ptr(S))
+    if rc:
+        raise RuntimeError(f"oracle_gemm_rows failed ({rc})")
+    return C.reshape(r.size, N), S.reshape(r.size, N)
+
+
+def gemm_entries(variant: str, A, B, M: int, N: int, K: int, ii, jj):
+    """Single entries C[ii[t], jj[t]]: returns (C, S) of shape [len(ii)]."""
+    dtype, layout = _variant(variant)
+    lib = _load()
+    a = _buf(A, dtype, M * K)
+    b = _buf(B, dtype, K * N)
+    i = np.ascontiguousarray(ii, dtype=np.int64)
+    j = np.ascontiguousarray(jj, dtype=np.int64)
+    if i.shape != j.shape:
+        raise ValueError("ii and jj differ in length")
+    C = np.empty(i.size, dtype=np.float64)
+    S = np.empty(i.size, dtype=np.float64)
+    rc = lib.oracle_gemm_entries(DTYPES[dtype], LAYOUTS[layout], _ptr(a), _ptr(b), M, N, K,
+                                 _ptr(i), _ptr(j), i.size, _ptr(C), _ptr(S))
+    if rc:
+        raise RuntimeError(f"oracle_gemm_entries failed ({rc})")
+    return C, S
+
+
+def decode(dtype: str, bits) -> np.ndarray:
+    """The oracle's own decoder of half/bf16 bit patterns, as float64."""
+    lib = _load()
+    fn = lib.oracle_decode_f16 if dtype == "f16" else lib.oracle_decode_bf16
+    b = np.asarray(bits, dtype=np.uint16).reshape(-1)
+    return np.array([fn(int(v)) for v in b], dtype=np.float64)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())

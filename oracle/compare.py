@@ -1,0 +1,68 @@
+"""Acceptance tolerances for a GEMM result against the oracle -- TEST INFRASTRUCTURE ONLY.
+
+FP32 output: |C - C_ref| <= 1e-5 * sum_k |a_ik * b_kj|, per element.
+Half / bf16 output: |C - C_ref| <= 1e-2 * sqrt(K/512) * max(1, |C_ref|), per element.
+
+The half form is the contest's correctness rule ("MTT S4000 FP16 GEMM",
+section 1: tolerance 0.01*sqrt(K/512), 0.057 at K = 16384), widened by the
+relative factor max(1, |C_ref|) so that outputs much larger than one are judged
+against their own half/bf16 spacing. The FP32 form scales with the sum of
+absolute products, the natural bound for any summation order.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def tol_f32(S: np.ndarray) -> np.ndarray:
+    return 1e-5 * np.asarray(S, dtype=np.float64)
+
+
+def tol_half(C_ref: np.ndarray, K: int) -> np.ndarray:
+    return 1e-2 * math.sqrt(K / 512.0) * np.maximum(1.0, np.abs(np.asarray(C_ref, dtype=np.float64)))
+
+
+def tolerance(variant: str, C_ref: np.ndarray, S: np.ndarray, K: int) -> np.ndarray:
+    if variant.startswith("f32"):
+        return tol_f32(S)
+    return tol_half(C_ref, K)
+
+
+def check(variant: str, C: np.ndarray, C_ref: np.ndarray, S: np.ndarray, K: int) -> dict:
+    """Element-wise comparison; C is the result widened to float64, same shape as C_ref."""
+    C = np.asarray(C, dtype=np.float64)
+    C_ref = np.asarray(C_ref, dtype=np.float64)
+    if C.shape != C_ref.shape:
+        raise ValueError(f"shape {C.shape} != reference shape {C_ref.shape}")
+    tol = tolerance(variant, C_ref, S, K)
+    err = np.abs(C - C_ref)
+    bad = ~(err <= tol)  # NaN in C counts as a violation
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(tol > 0, err / np.where(tol > 0, tol, 1.0), np.where(err > 0, np.inf, 0.0))
+    return {
+        "n": int(C.size),
+        "n_bad": int(bad.sum()),
+        "max_abs_err": float(np.nanmax(err)) if C.size else 0.0,
+        "max_err_over_tol": float(np.nanmax(ratio)) if C.size else 0.0,
+        "ok": bool(not bad.any()),
+    }
+
+
+def round_to(variant: str, x: np.ndarray) -> np.ndarray:
+    """Round exact float64 values once to the output type (nearest, ties to even) and
+    return them as float64 again. Used only for closed forms whose exact value is
+    known, e.g. ones*ones = K or I*B = B."""
+    x = np.asarray(x, dtype=np.float64)
+    if variant.startswith("f32"):
+        return x.astype(np.float32).astype(np.float64)
+    if variant.startswith("f16"):
+        return x.astype(np.float16).astype(np.float64)
+    # bf16: the values used here are exact in float32, so round float32 -> bf16.
+    f = x.astype(np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    lsb = (b >> np.uint64(16)) & np.uint64(1)
+    r = (((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)).astype(np.uint32)
+    return r.view(np.float32).astype(np.float64)

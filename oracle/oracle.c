@@ -1,0 +1,220 @@
+/*
+ * CPU oracle for dense C = A·B.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+ * load this library.  The product (the CUDA library) never links, loads or calls
+ * it, and the two share no source, header, table or helper.
+ *
+ * What it computes is the plain definition the pages give:
+ *
+ *     C[i,j] = sum_{k=0}^{K-1} A[i,k] * B[k,j]
+ *
+ * ("Chapter 5 Operators and Runtime", section 5.2.1, the element loop and the
+ * 2MKN FLOP count; "SGEMM measured and the three ledgers", section 2, the
+ * FLOP convention; "MTT S4000 FP16 GEMM", section 1, FP32-or-better
+ * accumulation.)  Here every product and every partial sum is kept in IEEE
+ * double, in ascending k, on the already-rounded input values.  A product of two
+ * float/half/bf16 values is exact in double (at most 48 significant bits), so the
+ * only rounding is in the running sum.  The result is returned in double, not in
+ * the output type; alongside it, S[i,j] = sum_k |A[i,k]*B[k,j]|, the scale the
+ * FP32 tolerance is measured against.
+ *
+ * Layouts ("SGEMM measured and the three ledgers", section 2: the same bytes read
+ * row-major or column-major are transposes of each other; "MTT S4000 FP16 GEMM",
+ * section 1: the column-major contest signature):
+ *   row-major:    A[i*K + k], B[k*N + j], C[i*N + j]
+ *   column-major: A[i + k*M], B[k + j*K], C[i + j*M]
+ *
+ * Element types: float32 (read as is), IEEE half and bf16 (uint16 bit patterns,
+ * decoded bit by bit below; no compiler half type and no CUDA header is used).
+ *
+ * Loop order: rows i in parallel (OpenMP), then k, then j, with one double
+ * accumulator per output of the row.  Each C[i,j] still sums its K products in
+ * ascending k, so the result does not depend on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+enum { ORACLE_ROW_MAJOR = 0, ORACLE_COL_MAJOR = 1 };
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_decode_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);            /* subnormal: f * 2^-10 * 2^-14 */
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE binary32 (1 sign, 8 exponent bits with
+ * bias 127, 7 fraction bits). */
+double oracle_decode_bf16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xFF;
+    int f = h & 0x7F;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133);           /* subnormal: f * 2^-7 * 2^-126 */
+    } else if (e == 255) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(128 + f), e - 134); /* (1 + f/128) * 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+static double elem(const void *p, int dtype, int64_t idx)
+{
+    switch (dtype) {
+    case ORACLE_F32: return (double)((const float *)p)[idx];
+    case ORACLE_F16: return oracle_decode_f16(((const uint16_t *)p)[idx]);
+    default:         return oracle_decode_bf16(((const uint16_t *)p)[idx]);
+    }
+}
+
+/* Storage offsets of A(i,k), B(k,j) and C(i,j) for the chosen layout. */
+static int64_t off_a(int layout, int64_t M, int64_t K, int64_t i, int64_t k)
+{
+    return layout == ORACLE_ROW_MAJOR ? i * K + k : i + k * M;
+}
+static int64_t off_b(int layout, int64_t K, int64_t N, int64_t k, int64_t j)
+{
+    return layout == ORACLE_ROW_MAJOR ? k * N + j : k + j * K;
+}
+static int64_t off_c(int layout, int64_t M, int64_t N, int64_t i, int64_t j)
+{
+    return layout == ORACLE_ROW_MAJOR ? i * N + j : i + j * M;
+}
+
+static int bad_args(int dtype, int layout, int64_t M, int64_t N, int64_t K)
+{
+    if (dtype < ORACLE_F32 || dtype > ORACLE_BF16) return 1;
+    if (layout != ORACLE_ROW_MAJOR && layout != ORACLE_COL_MAJOR) return 1;
+    if (M < 0 || N < 0 || K < 0) return 1;
+    return 0;
+}
+
+/* One output row i of the product, written to acc[0..N) and sabs[0..N). */
+static void one_row(int dtype, int layout, const void *A, const void *B,
+                    int64_t M, int64_t N, int64_t K, int64_t i,
+                    double *acc, double *sabs)
+{
+    for (int64_t j = 0; j < N; ++j) { acc[j] = 0.0; sabs[j] = 0.0; }
+    for (int64_t k = 0; k < K; ++k) {
+        double a = elem(A, dtype, off_a(layout, M, K, i, k));
+        for (int64_t j = 0; j < N; ++j) {
+            double p = a * elem(B, dtype, off_b(layout, K, N, k, j));
+            acc[j] += p;
+            sabs[j] += fabs(p);
+        }
+    }
+}
+
+/* Full product.  C and S (S may be NULL) are written in the problem's own layout. */
+int oracle_gemm(int dtype, int layout, const void *A, const void *B,
+                int64_t M, int64_t N, int64_t K, double *C, double *S)
+{
+    if (bad_args(dtype, layout, M, N, K)) return 1;
+    if (M == 0 || N == 0) return 0;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+        double *sab = (double *)malloc(sizeof(double) * (size_t)N);
+        if (!acc || !sab) {
+#pragma omp atomic write
+            err = 2;
+        }
+#pragma omp for schedule(static)
+        for (int64_t i = 0; i < M; ++i) {
+            if (!acc || !sab) continue;
+            one_row(dtype, layout, A, B, M, N, K, i, acc, sab);
+            for (int64_t j = 0; j < N; ++j) {
+                C[off_c(layout, M, N, i, j)] = acc[j];
+                if (S) S[off_c(layout, M, N, i, j)] = sab[j];
+            }
+        }
+        free(acc);
+        free(sab);
+    }
+    return err;
+}
+
+/* Selected rows only: C and S (S may be NULL) are nrows x N, row-major, row r
+ * holding output row rows[r]. */
+int oracle_gemm_rows(int dtype, int layout, const void *A, const void *B,
+                     int64_t M, int64_t N, int64_t K,
+                     const int64_t *rows, int64_t nrows, double *C, double *S)
+{
+    if (bad_args(dtype, layout, M, N, K)) return 1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return 1;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double *sab = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        if (!acc || !sab) {
+#pragma omp atomic write
+            err = 2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            if (!acc || !sab) continue;
+            one_row(dtype, layout, A, B, M, N, K, rows[r], acc, sab);
+            memcpy(C + r * N, acc, sizeof(double) * (size_t)N);
+            if (S) memcpy(S + r * N, sab, sizeof(double) * (size_t)N);
+        }
+        free(acc);
+        free(sab);
+    }
+    return err;
+}
+
+/* Selected entries (ii[t], jj[t]), one dot product each. */
+int oracle_gemm_entries(int dtype, int layout, const void *A, const void *B,
+                        int64_t M, int64_t N, int64_t K,
+                        const int64_t *ii, const int64_t *jj, int64_t n,
+                        double *C, double *S)
+{
+    if (bad_args(dtype, layout, M, N, K)) return 1;
+    for (int64_t t = 0; t < n; ++t)
+        if (ii[t] < 0 || ii[t] >= M || jj[t] < 0 || jj[t] >= N) return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = elem(A, dtype, off_a(layout, M, K, ii[t], k)) *
+                       elem(B, dtype, off_b(layout, K, N, k, jj[t]));
+            acc += p;
+            sab += fabs(p);
+        }
+        C[t] = acc;
+        if (S) S[t] = sab;
+    }
+    return 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
