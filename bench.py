@@ -1,0 +1,476 @@
+"""Benchmark of the GB300 dense GEMM library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-paths] [--no-cpu-baseline] [--no-e2e]
+
+A step is one C = A·B call on one batch of seeded synthetic input.  The
+default workload is the pages' main SGEMM: FP32 row-major M = N = K = 4096 (A,
+B uniform[-1, 1]), pure FP32 FFMA.  The line printed by rank 0 carries the
+throughput in TFLOP/s (2*M*N*K per step, device time by CUDA events on the
+launching stream), the roofline of the kernel, the oracle's CPU throughput
+on a bounded sample, an end-to-end number through host buffers, the clocks seen
+during the timed region and -- under "paths" -- the same measurements for the
+tensor-core workloads (FP16 column-major 8192^3 and 3072x5120x6144, BF16 FFN
+projection) and the M = 1 decode shapes.
+
+--impl reference times the CPU oracle (the reference arm of this build) on
+the same workload and prints its line with "impl": "reference".
+
+Under torchrun every rank runs the same workload on its own GPU (replicas, no
+collective on the data path): value = FLOPs of all ranks / slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from datetime import datetime
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+from dense_matrix_multiply_gb300 import metrics  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (2·M·N·K/t) and % of FP32-SIMT or BF16/FP16 tensor peak"
+DEFAULT_WORKLOAD = "sgemm_f32_rm_4096"
+SMS_NOMINAL = 152
+FP32_LANES_PER_SM = 128
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+L2_BYTES = 129e6
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture, keyed by workload; valid only while the kernel's source is the one
+# captured (sha256 prefix of the .cu file), else reported as null.
+TRAFFIC = {}
+
+KERNEL_SOURCE = {
+    "simt": "simt_gemm.cu",
+    "umma": "umma_gemm.cu",
+    "gemv": "gemv.cu",
+}
+
+
+def all_workloads():
+    out = {}
+    for name, (cfg, probs) in synthetic.WORKLOADS.items():
+        out[name] = (cfg, probs[0])
+    for (M, N, K) in synthetic.EDGE_SHAPES:
+        for v in ("f32_rm", "bf16_rm"):
+            out[f"edge_{v}_{M}x{N}x{K}"] = (synthetic.EDGE_CONFIG_ID, (v, M, N, K, "uniform", 1.0, "uniform", 1.0))
+    return out
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(kind: str) -> str:
+    path = os.path.join(ROOT, "dense_matrix_multiply_gb300", "csrc", KERNEL_SOURCE[kind])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    FIELDS = ["timestamp", "uuid", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid: str | None, period_ms: int = 50):
+        self.uuid = uuid
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms)], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self, t0: float, t1: float):
+        """Median SM MHz and the throttle reasons seen between host times t0 and t1."""
+        self.file.seek(0)
+        rows = list(csv.reader(io.StringIO(self.file.read())))
+        try:
+            os.unlink(self.file.name)
+        except OSError:
+            pass
+        mhz, maxmhz, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < len(self.FIELDS):
+                continue
+            r = [x.strip() for x in r]
+            try:
+                ts = datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if self.uuid and r[1] != self.uuid:
+                continue
+            if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            try:
+                mhz.append(float(r[2]))
+                maxmhz.append(float(r[3]))
+                power.append(float(r[4]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxmhz), "reasons": sorted(reasons),
+                "samples": len(mhz), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ helpers
+def device_inputs(variant, A, B, M, N):
+    import torch
+    if variant.startswith("f32"):
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        dC = torch.empty(M * N, dtype=torch.float32, device="cuda")
+    else:
+        dA = torch.from_numpy(A.view(np.int16)).cuda()
+        dB = torch.from_numpy(B.view(np.int16)).cuda()
+        dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    return dA, dB, dC
+
+
+ENTRY = {"f32_rm": "gemm_f32_rm", "f16_cm": "gemm_f16_cm", "bf16_rm": "gemm_bf16_rm"}
+
+
+def kernel_kind(name: str) -> str:
+    return name.split("_")[0]
+
+
+def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, peaks: dict, peaks_src: str,
+                 sm_mhz: float | None, sms: int, workload: str):
+    es = 4 if variant.startswith("f32") else 2
+    flops = metrics.gemm_flops(M, N, K)
+    algo_bytes = metrics.min_bytes(M, N, K, es)
+    tr = TRAFFIC.get(workload)
+    traffic = None
+    if tr and tr.get("source") == source_hash(kind if kind in KERNEL_SOURCE else "simt"):
+        traffic = tr["bytes"]
+    if kind == "gemv":
+        achieved = algo_bytes / seconds_per_launch / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "algorithmic_bytes": algo_bytes, "peak_source": peaks_src}
+    achieved = flops / seconds_per_launch / 1e12
+    if kind == "umma":
+        peak = float(peaks["bf16_tflops"])
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "algorithmic_flops": flops,
+                "algorithmic_bytes": algo_bytes, "peak_source": f"{peaks_src} cuBLAS bf16 burst"
+                + (" (f16 dense rate equals bf16)" if variant.startswith("f16") else "")}
+    # SIMT FP32: SMs x 128 lanes x 2 FLOP x clock
+    max_mhz = float(peaks.get("sm_max_mhz", FALLBACK_PEAKS["sm_max_mhz"]))
+    peak = metrics.simt_fp32_peak(sms, max_mhz * 1e6, FP32_LANES_PER_SM) / 1e12
+    out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+           "traffic": traffic, "algorithmic_flops": flops, "algorithmic_bytes": algo_bytes,
+           "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {max_mhz:.0f} MHz (max SM clock)"}
+    if sm_mhz:
+        p2 = metrics.simt_fp32_peak(sms, sm_mhz * 1e6, FP32_LANES_PER_SM) / 1e12
+        out["peak_at_measured_clock"] = p2
+        out["frac_at_measured_clock"] = achieved / p2
+        out["measured_clock_mhz"] = sm_mhz
+    return out
+
+
+def time_device(fn, steps: int, warmup: int, stream):
+    """CUDA-event time of `steps` calls on `stream` after `warmup` calls: ms total."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def cpu_sample(variant, A, B, M, N, K, budget_s: float):
+    """Times the oracle on a bounded sample of output rows of the same problem.
+    Returns (flop/s, rows, seconds, threads)."""
+    import oracle
+    threads = oracle.num_threads()
+    # calibrate on one row per thread
+    rows = np.arange(min(threads, M), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(variant, A, B, M, N, K, rows)
+    dt = time.perf_counter() - t0
+    per_round = max(dt, 1e-6)
+    rounds = max(1, int(budget_s / per_round))
+    nrows = int(min(M, rows.size * rounds))
+    sel = np.arange(nrows, dtype=np.int64) % M
+    t0 = time.perf_counter()
+    oracle.gemm_rows(variant, A, B, M, N, K, sel)
+    dt = time.perf_counter() - t0
+    return 2.0 * nrows * N * K / dt, nrows, dt, threads
+
+
+# ------------------------------------------------------------------ our arm
+def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler_uuid=None, e2e=True,
+                     cpu_budget=0.0, clocks=True):
+    import torch
+    import dense_matrix_multiply_gb300 as g
+
+    cfg, (variant, M, N, K, da, sa, db, sb) = all_workloads()[name]
+    A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
+    dA, dB, dC = device_inputs(variant, A, B, M, N)
+    entry = getattr(g.load(), ENTRY[variant])
+    g.gemm_set_stream(stream)
+    pa, pb, pc = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
+
+    def step():
+        st = entry(pa, pb, pc, M, N, K)
+        if st != 0:
+            raise RuntimeError(f"{ENTRY[variant]} failed: {g.gemm_status_string(st)} {g.gemm_last_error()}")
+
+    step()
+    g.gemm_synchronize()
+    kernel = g.gemm_last_kernel()
+    kind = kernel_kind(kernel)
+
+    sampler = ClockSampler(sampler_uuid) if clocks else None
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    time.sleep(0.2 if clocks else 0)
+    t_host0 = time.time()
+    ms = time_device(step, steps, 0, stream)
+    t_host1 = time.time()
+    g.gemm_synchronize()
+    clk = None
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+        clk = sampler.summary(t_host0, t_host1)
+
+    flops = metrics.gemm_flops(M, N, K)
+    s_per = ms / 1e3 / steps
+    res = {
+        "workload": name, "variant": variant, "M": M, "N": N, "K": K, "kernel": kernel,
+        "ms_per_step": ms / steps, "tflops": flops / s_per / 1e12, "steps": steps, "ms_total": ms,
+        "roofline": roofline_for(kind, variant, M, N, K, s_per, peaks, peaks_src,
+                                 clk["sm_mhz"] if clk else None, sms, name),
+        "clocks": clk, "footprint_bytes": int(dA.numel() * dA.element_size() + dB.numel() * dB.element_size()
+                                              + dC.numel() * dC.element_size()),
+    }
+
+    if e2e:
+        hA = torch.from_numpy(A.view(np.int16) if A.dtype != np.float32 else A).pin_memory()
+        hB = torch.from_numpy(B.view(np.int16) if B.dtype != np.float32 else B).pin_memory()
+        hC = torch.empty_like(dC, device="cpu").pin_memory()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                step()
+                hC.copy_(dC, non_blocking=True)
+
+        n_e2e = max(3, min(steps, 20))
+        ms_e2e = time_device(e2e_step, n_e2e, 2, stream)
+        res["e2e"] = {"value": flops * n_e2e / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": int(hA.numel() * hA.element_size() + hB.numel() * hB.element_size()),
+                      "d2h_bytes_per_step": int(hC.numel() * hC.element_size()),
+                      "ms_per_step": ms_e2e / n_e2e, "steps": n_e2e}
+
+    if cpu_budget > 0:
+        fps, nrows, dt, threads = cpu_sample(variant, A, B, M, N, K, cpu_budget)
+        res["cpu_baseline"] = {"value": fps / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                               "sample": f"{nrows} of {M} output rows ({nrows}x{N}x{K} FMAs, FP64 oracle) "
+                                         f"in {dt:.1f} s"}
+    del dA, dB, dC
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import dense_matrix_multiply_gb300 as g
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    if world == 1:
+        g.ensure_built()
+    g.load()
+    peaks, peaks_src = read_peaks()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        uuid = None
+    stream = torch.cuda.Stream()
+
+    # CPU baseline first (before heavy GPU use), rank 0 at N=1 only.
+    res = measure_workload(args.workload, args.steps, args.warmup, peaks, peaks_src, sms, stream,
+                           sampler_uuid=uuid, e2e=not args.no_e2e,
+                           cpu_budget=(args.cpu_seconds if (rank == 0 and world == 1
+                                                            and not args.no_cpu_baseline) else 0.0),
+                           clocks=(rank == 0))
+    ms_total = res["ms_total"]
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    paths = []
+    if not args.no_paths and rank == 0:
+        for wl in args.paths:
+            if wl == args.workload:
+                continue
+            r = measure_workload(wl, max(5, args.path_steps), 3, peaks, peaks_src, sms, stream,
+                                 sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True)
+            paths.append({k: r[k] for k in ("workload", "kernel", "M", "N", "K", "ms_per_step", "tflops",
+                                            "roofline", "clocks")})
+
+    if rank == 0:
+        M, N, K = res["M"], res["N"], res["K"]
+        flops_all = metrics.gemm_flops(M, N, K) * args.steps * world
+        value = flops_all / (ms_total / 1e3) / 1e12
+        clk = res["clocks"] or {}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if res["variant"].startswith("f32") else res["variant"].split("_")[0],
+            "data": "synthetic",
+            "config": {"workload": args.workload, "M": M, "N": N, "K": K,
+                       "layout": "column-major" if res["variant"].endswith("_cm") else "row-major",
+                       "inputs": "uniform[-1,1] seeded SplitMix64" if "ffn" not in args.workload
+                       else "X~N(0,1), W~N(0,1/4096) seeded SplitMix64",
+                       "l2": f"no flush: A+B+C = {res['footprint_bytes'] / 2**20:.0f} MiB "
+                             f"{'>' if res['footprint_bytes'] > L2_BYTES else '<='} 129 MB L2",
+                       "parallelism": f"replicas x{world}"},
+            "kernel": res["kernel"],
+            "roofline": res["roofline"],
+            "gpu_launches": args.steps,
+            "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
+                       "reasons": clk.get("reasons", []), "samples": clk.get("samples", 0)},
+        }
+        if "e2e" in res:
+            line["e2e"] = res["e2e"]
+        if "cpu_baseline" in res:
+            line["cpu_baseline"] = res["cpu_baseline"]
+        if paths:
+            line["paths"] = paths
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cfg, (variant, M, N, K, da, sa, db, sb) = all_workloads()[args.workload]
+    A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
+    threads = oracle.num_threads()
+    # size each step so that warmup + steps take about args.ref_seconds in total
+    rows = np.arange(min(threads, M), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(variant, A, B, M, N, K, rows)
+    per_round = max(time.perf_counter() - t0, 1e-6)
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
+    nrows = int(min(M, max(1, round(per_step / per_round)) * rows.size))
+    sel = np.arange(nrows, dtype=np.int64) % M
+    for _ in range(args.warmup):
+        oracle.gemm_rows(variant, A, B, M, N, K, sel)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_rows(variant, A, B, M, N, K, sel)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * nrows * N * K * args.steps
+    value = flops / dt / 1e12
+    sample = f"{nrows} of {M} output rows per step ({nrows}x{N}x{K} FMAs, FP64 oracle)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K,
+                   "layout": "column-major" if variant.endswith("_cm") else "row-major",
+                   "parallelism": "host cores (CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
+    p.add_argument("--paths", nargs="*", default=["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144",
+                                                   "ffn_bf16_rm_1024x12288x4096", "edge_bf16_rm_1x12288x4096",
+                                                   "edge_f32_rm_1x12288x4096"])
+    p.add_argument("--path-steps", type=int, default=50)
+    p.add_argument("--no-paths", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--ref-seconds", type=float, default=60.0)
+    args = p.parse_args(argv)
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,242 @@
+// C ABI of the library: argument checks, per-thread stream, device check,
+// dispatch to the kernels.  See include/gemm.h for the contract.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "gemm.h"
+#include "internal.h"
+
+using namespace gemm_gb300;
+
+namespace {
+
+enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma };
+
+thread_local cudaStream_t t_stream = nullptr;
+thread_local const char *t_last_kernel = "none";
+thread_local char t_last_error[256] = "";
+thread_local Family t_force = Family::Auto;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::once_flag once;
+    bool supported = false;
+    int num_sms = 0;
+    int *status = nullptr;  // device word the tensor-core kernel reports timeouts in
+    cudaError_t init_error = cudaSuccess;
+};
+DeviceInfo g_devices[kMaxDevices];
+
+__global__ void zero_fill_kernel(uint4 *p, size_t n16, uint8_t *tail, size_t ntail) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        p[i] = make_uint4(0, 0, 0, 0);
+    if (blockIdx.x == 0 && threadIdx.x < ntail) tail[threadIdx.x] = 0;
+}
+
+__global__ void zero_fill_bytes_kernel(uint8_t *p, size_t n) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0;
+}
+
+void record_cuda_error(cudaError_t e) {
+    strncpy(t_last_error, cudaGetErrorString(e), sizeof(t_last_error) - 1);
+    t_last_error[sizeof(t_last_error) - 1] = '\0';
+}
+
+// Per-device set-up on first use: capability check, SM count, status word.
+gemm_status_t device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    DeviceInfo &d = g_devices[dev];
+    std::call_once(d.once, [&] {
+        int major = 0, minor = 0;
+        cudaError_t err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) { d.init_error = err; return; }
+        d.supported = (major == 10 && minor == 3);
+        if (!d.supported) return;
+        err = cudaMalloc(&d.status, sizeof(int));
+        if (err == cudaSuccess) err = cudaMemset(d.status, 0, sizeof(int));
+        if (err != cudaSuccess) d.init_error = err;
+    });
+    if (d.init_error != cudaSuccess) { record_cuda_error(d.init_error); return GEMM_ERR_CUDA; }
+    if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return GEMM_OK;
+}
+
+bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return an && bn && a0 < b0 + bn && b0 < a0 + an;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+gemm_status_t finish(cudaError_t e, const char *name) {
+    t_last_kernel = name;
+    if (e == cudaSuccess) return GEMM_OK;
+    record_cuda_error(e);
+    return GEMM_ERR_CUDA;
+}
+
+const char *kernel_name(const char *fam, Elt elt) {
+    // Static names: family x element type.
+    static const char *names[5][3] = {
+        {"simt_f32_vec4", "simt_f16_scalar", "simt_bf16_scalar"},
+        {"simt_f32_scalar", "simt_f16_scalar", "simt_bf16_scalar"},
+        {"gemv_f32_vec", "gemv_f16_vec", "gemv_bf16_vec"},
+        {"gemv_f32_scalar", "gemv_f16_scalar", "gemv_bf16_scalar"},
+        {"umma_f32", "umma_f16", "umma_bf16"},
+    };
+    int f = 0;
+    if (!strcmp(fam, "simt")) f = 0;
+    else if (!strcmp(fam, "simt_scalar")) f = 1;
+    else if (!strcmp(fam, "gemv")) f = 2;
+    else if (!strcmp(fam, "gemv_scalar")) f = 3;
+    else f = 4;
+    return names[f][(int)elt];
+}
+
+// Row-major problem C[M,N] = A[M,K] B[K,N] with tight strides.
+gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, Elt elt) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    const size_t es = elt == Elt::F32 ? 4 : 2;
+    if (M == 0 || N == 0) { t_last_kernel = "noop"; return GEMM_OK; }
+    if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_VALUE;
+    const size_t c_bytes = (size_t)M * N * es;
+    if (overlaps(C, c_bytes, A, (size_t)M * K * es) || overlaps(C, c_bytes, B, (size_t)K * N * es))
+        return GEMM_ERR_ALIAS;
+
+    DeviceInfo *dev = nullptr;
+    gemm_status_t st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = t_stream;
+
+    if (K == 0) {
+        if (t_force != Family::Auto) return GEMM_ERR_INVALID_VALUE;
+        const unsigned grid = (unsigned)(dev->num_sms * 4);
+        if (aligned16(C)) {
+            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)C, c_bytes / 16, (uint8_t *)C + (c_bytes & ~(size_t)15),
+                                                  c_bytes & 15);
+        } else {
+            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)C, c_bytes);
+        }
+        return finish(cudaGetLastError(), "zero_fill");
+    }
+
+    Problem p{A, B, C, M, N, K, elt};
+    const int vw = elt == Elt::F32 ? 4 : 8;
+    const bool gemv_vec_ok = (N % vw) == 0 && aligned16(B);
+    const bool simt_vec_ok = elt == Elt::F32 && (K % 4) == 0 && (N % 4) == 0 && aligned16(A) &&
+                             aligned16(B) && aligned16(C);
+
+    switch (t_force) {
+    case Family::Simt:
+        if (elt == Elt::F32 && !simt_vec_ok) return GEMM_ERR_INVALID_VALUE;
+        return finish(launch_simt(p, elt == Elt::F32, s), kernel_name("simt", elt));
+    case Family::SimtScalar:
+        return finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
+    case Family::Gemv:
+        if (M > kGemvMaxM || !gemv_vec_ok) return GEMM_ERR_INVALID_VALUE;
+        return finish(launch_gemv(p, true, s), kernel_name("gemv", elt));
+    case Family::GemvScalar:
+        if (M > kGemvMaxM) return GEMM_ERR_INVALID_VALUE;
+        return finish(launch_gemv(p, false, s), kernel_name("gemv_scalar", elt));
+    case Family::Umma:
+        if (!umma_supported(p)) return GEMM_ERR_INVALID_VALUE;
+        return finish(launch_umma(p, dev->num_sms, dev->status, s), kernel_name("umma", elt));
+    case Family::Auto:
+        break;
+    }
+
+    if (M <= kGemvMaxM)
+        return gemv_vec_ok ? finish(launch_gemv(p, true, s), kernel_name("gemv", elt))
+                           : finish(launch_gemv(p, false, s), kernel_name("gemv_scalar", elt));
+    if (elt == Elt::F32)
+        return simt_vec_ok ? finish(launch_simt(p, true, s), kernel_name("simt", elt))
+                           : finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
+    if (umma_supported(p)) return finish(launch_umma(p, dev->num_sms, dev->status, s), kernel_name("umma", elt));
+    return finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
+}
+
+}  // namespace
+
+extern "C" {
+
+GEMM_API gemm_status_t gemm_f32_rm(const float *A, const float *B, float *C, int M, int N, int K) {
+    return run(A, B, C, M, N, K, Elt::F32);
+}
+
+// Column-major C = A·B is row-major C^T = B^T·A^T on the same buffers: the
+// column-major B buffer read row-major is B^T [N,K], the column-major A buffer
+// read row-major is A^T [K,M], and the row-major [N,M] result is the
+// column-major [M,N] C ("SGEMM measured and the three ledgers", section 2).
+GEMM_API gemm_status_t gemm_f16_cm(const uint16_t *A, const uint16_t *B, uint16_t *C, int M, int N, int K) {
+    return run(B, A, C, N, M, K, Elt::F16);
+}
+
+GEMM_API gemm_status_t gemm_bf16_rm(const uint16_t *A, const uint16_t *B, uint16_t *C, int M, int N, int K) {
+    return run(A, B, C, M, N, K, Elt::BF16);
+}
+
+GEMM_API gemm_status_t gemm_set_stream(void *cuda_stream) {
+    t_stream = static_cast<cudaStream_t>(cuda_stream);
+    return GEMM_OK;
+}
+
+GEMM_API void *gemm_get_stream(void) { return t_stream; }
+
+GEMM_API gemm_status_t gemm_synchronize(void) {
+    cudaError_t e = cudaStreamSynchronize(t_stream);
+    if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
+    DeviceInfo *dev = nullptr;
+    gemm_status_t st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    int code = 0;
+    e = cudaMemcpy(&code, dev->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
+    if (code != 0) {
+        e = cudaMemset(dev->status, 0, sizeof(int));
+        if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+GEMM_API const char *gemm_status_string(gemm_status_t s) {
+    switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE";
+    case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+GEMM_API const char *gemm_last_kernel(void) { return t_last_kernel; }
+
+GEMM_API const char *gemm_last_error(void) { return t_last_error; }
+
+GEMM_API gemm_status_t gemm_force_kernel(const char *family) {
+    if (!family || !*family) { t_force = Family::Auto; return GEMM_OK; }
+    if (!strcmp(family, "simt")) t_force = Family::Simt;
+    else if (!strcmp(family, "simt_scalar")) t_force = Family::SimtScalar;
+    else if (!strcmp(family, "gemv")) t_force = Family::Gemv;
+    else if (!strcmp(family, "gemv_scalar")) t_force = Family::GemvScalar;
+    else if (!strcmp(family, "umma")) t_force = Family::Umma;
+    else return GEMM_ERR_INVALID_VALUE;
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+// Skinny-M GEMM (M <= 8), e.g. the decode case M = 1: c[m,j] = sum_k x[m,k]*W[k,j].
+//
+// With one or a few rows of A the product is bound by reading B (W) once from
+// HBM ("SGEMM measured and the three ledgers", the shape table: decode with
+// batch 1 gains only 3.4x from the SGEMM tricks; "Chapter 5", section 5.1:
+// decode processes M = 1).  So the kernel is a streaming reduction, not a
+// tiled contraction:
+//   * a CTA owns a strip of CW consecutive columns of W and all of K; its 256
+//     threads form TC column-lanes x TK k-groups; a column-lane reads VW
+//     consecutive elements (16 bytes) of one row of W per step, so TC lanes read
+//     one contiguous 128-byte row segment;
+//   * k-group g handles rows k = g, g + TK, ...; loads are issued UNROLL rows
+//     at a time to keep enough bytes in flight;
+//   * FP32 accumulators per (m, column); the TK partial sums of a column are
+//     added in shared memory in the fixed order g = 0, 1, ..., TK-1, so the
+//     result is deterministic (no atomics, no second launch, no global scratch).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace gemm_gb300 {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int UNROLL = 8;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// VW elements of W as one 16-byte load (VW = 16 / sizeof(T)) or VW = 1 scalar.
+template <typename T, int VW>
+struct Vec { T v[VW]; };
+
+template <typename T, int VW>
+__device__ __forceinline__ Vec<T, VW> load_w(const T *p) {
+    Vec<T, VW> r;
+    if constexpr (VW * sizeof(T) == 16) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+        memcpy(&r, &u, 16);
+    } else {
+#pragma unroll
+        for (int i = 0; i < VW; ++i) r.v[i] = p[i];
+    }
+    return r;
+}
+
+template <typename T, int VW, int TC, int MM>
+__global__ void __launch_bounds__(THREADS)
+gemv_kernel(const T *__restrict__ X, const T *__restrict__ W, T *__restrict__ C, int M, int N, int K)
+{
+    constexpr int TK = THREADS / TC;
+    constexpr int CW = TC * VW;
+    extern __shared__ float red[];  // [TK][MM][CW]
+
+    const int tc = threadIdx.x % TC;
+    const int kg = threadIdx.x / TC;
+    const int n = blockIdx.x * CW + tc * VW;
+    // Vector loads need the whole vector in range (N % VW == 0 when VW > 1).
+    const bool active = n < N;
+
+    float acc[MM][VW];
+#pragma unroll
+    for (int m = 0; m < MM; ++m)
+#pragma unroll
+        for (int v = 0; v < VW; ++v) acc[m][v] = 0.f;
+
+    if (active) {
+        const T *wp = W + n;
+        int k = kg;
+        for (; k + (UNROLL - 1) * TK < K; k += UNROLL * TK) {
+            Vec<T, VW> w[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) w[u] = load_w<T, VW>(wp + (size_t)(k + u * TK) * N);
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+#pragma unroll
+                for (int m = 0; m < MM; ++m) {
+                    if (m < M) {
+                        const float x = to_f32(X[(size_t)m * K + k + u * TK]);
+#pragma unroll
+                        for (int v = 0; v < VW; ++v) acc[m][v] = fmaf(x, to_f32(w[u].v[v]), acc[m][v]);
+                    }
+                }
+            }
+        }
+        for (; k < K; k += TK) {
+            const Vec<T, VW> w = load_w<T, VW>(wp + (size_t)k * N);
+#pragma unroll
+            for (int m = 0; m < MM; ++m) {
+                if (m < M) {
+                    const float x = to_f32(X[(size_t)m * K + k]);
+#pragma unroll
+                    for (int v = 0; v < VW; ++v) acc[m][v] = fmaf(x, to_f32(w.v[v]), acc[m][v]);
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int m = 0; m < MM; ++m)
+#pragma unroll
+        for (int v = 0; v < VW; ++v) red[((size_t)kg * MM + m) * CW + tc * VW + v] = acc[m][v];
+    __syncthreads();
+
+    for (int o = threadIdx.x; o < MM * CW; o += THREADS) {
+        const int m = o / CW, c = o % CW;
+        const int gn = blockIdx.x * CW + c;
+        if (m >= M || gn >= N) continue;
+        float s = 0.f;
+        for (int g = 0; g < TK; ++g) s += red[((size_t)g * MM + m) * CW + c];
+        C[(size_t)m * N + gn] = from_f32<T>(s);
+    }
+}
+
+template <typename T, int VW, int TC, int MM>
+cudaError_t launch_cfg(const Problem &p, cudaStream_t s) {
+    constexpr int TK = THREADS / TC;
+    constexpr int CW = TC * VW;
+    const size_t smem = sizeof(float) * TK * MM * CW;
+    auto kern = gemv_kernel<T, VW, TC, MM>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const unsigned grid = (unsigned)((p.N + CW - 1) / CW);
+    kern<<<grid, THREADS, smem, s>>>(static_cast<const T *>(p.A), static_cast<const T *>(p.B),
+                                     static_cast<T *>(p.C), p.M, p.N, p.K);
+    return cudaGetLastError();
+}
+
+template <typename T, int VW, int TC>
+cudaError_t launch_m(const Problem &p, cudaStream_t s) {
+    if (p.M == 1) return launch_cfg<T, VW, TC, 1>(p, s);
+    if (p.M <= 2) return launch_cfg<T, VW, TC, 2>(p, s);
+    if (p.M <= 4) return launch_cfg<T, VW, TC, 4>(p, s);
+    return launch_cfg<T, VW, TC, 8>(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const Problem &p, bool vec, cudaStream_t s) {
+    if (p.M < 1 || p.M > kGemvMaxM) return cudaErrorInvalidValue;
+    switch (p.elt) {
+    case Elt::F32:
+        return vec ? launch_m<float, 4, 8>(p, s) : launch_m<float, 1, 32>(p, s);
+    case Elt::F16:
+        return vec ? launch_m<__half, 8, 8>(p, s) : launch_m<__half, 1, 32>(p, s);
+    case Elt::BF16:
+        return vec ? launch_m<__nv_bfloat16, 8, 8>(p, s) : launch_m<__nv_bfloat16, 1, 32>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,39 @@
+// Internal launcher interface shared by the C-ABI layer and the kernels.
+// Every problem reaching a launcher is row-major with tight leading
+// dimensions: C[M,N] = A[M,K] · B[K,N], M, N, K >= 1.  The column-major half
+// entry point is mapped onto this form before dispatch (C^T = B^T · A^T).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gemm_gb300 {
+
+enum class Elt { F32, F16, BF16 };
+
+struct Problem {
+    const void *A;
+    const void *B;
+    void *C;
+    int M, N, K;
+    Elt elt;
+};
+
+// FP32 (or 16-bit fallback) SIMT kernel on the CUDA cores.  vec4: float4
+// global loads/stores (needs K % 4 == 0, N % 4 == 0 and 16-byte aligned bases;
+// f32 only).  Returns the launch status.
+cudaError_t launch_simt(const Problem &p, bool vec4, cudaStream_t s);
+
+// Skinny-M kernel (M <= kGemvMaxM): streams B once, FP32 accumulation, fixed
+// order reduction in shared memory.  vec: 16-byte loads of B (needs N a
+// multiple of the vector width and a 16-byte aligned B).
+constexpr int kGemvMaxM = 8;
+cudaError_t launch_gemv(const Problem &p, bool vec, cudaStream_t s);
+
+// tcgen05 tensor-core kernel for 16-bit inputs.  Needs 16-byte aligned A, B, C
+// and K*2, N*2 multiples of 16 bytes (TMA strides).  num_sms: persistent grid
+// size.  status: device word the kernel ORs a timeout code into.
+cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s);
+bool umma_supported(const Problem &p);
+
+}  // namespace gemm_gb300

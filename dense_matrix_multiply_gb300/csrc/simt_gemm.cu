@@ -1,0 +1,213 @@
+// SIMT GEMM on the CUDA cores: FP32 FFMA only, no tensor cores, no TF32.
+//
+// Design (prior art: "SGEMM measured and the three ledgers", K5/K6 -- register
+// blocking and 128-bit shared loads; the 800 -> 10600 GFLOPS SGEMM blog,
+// versions 2-4 -- shared tiles, register micro-tiles, double buffering; chapter
+// 5 of the AI-infra book, section 5.2.3 -- bank-conflict-free layouts):
+//   * CTA tile 128 x 128, K step 16, 256 threads, 8 x 8 outputs per thread held
+//     in 64 FP32 registers.
+//   * A is stored k-major in shared memory (transposed on the way in), so one
+//     128-bit shared load gives four consecutive rows; B is stored as it lies
+//     (n contiguous).  Per k: two LDS.128 of A, two of B, 64 FFMA.
+//   * Each warp covers a 32 x 64 sub-tile as 4 x 8 lanes; a lane owns rows
+//     {4t..4t+3, 16+4t..16+4t+3} and columns {4u..4u+3, 32+4u..32+4u+3}, so the
+//     A and B fragment loads of a warp touch 64 and 128 contiguous bytes: one
+//     shared-memory wavefront each, no bank conflict.
+//   * Two shared buffers; the next K tile is fetched into registers (LDG.128)
+//     while the current one is computed, then stored into the other buffer: one
+//     barrier per K tile.
+//   * Grouped rasterisation: runs of 8 row-tiles sweep the column tiles so that
+//     concurrently resident CTAs share A rows and B columns in L2.
+//   * Ragged M, N, K: loads are predicated with zero fill, stores are predicated.
+// The same template with 16-bit inputs (converted to FP32 when staged) and
+// 16-bit outputs (rounded to nearest even once) serves as the tensor path's
+// fallback for strides TMA cannot describe.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace gemm_gb300 {
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 16, THREADS = 256;
+constexpr int A_LD = BM + 4;  // padded row of the k-major A tile (floats)
+constexpr int B_LD = BN;      // row of the B tile (floats)
+constexpr int GROUP_M = 8;
+#ifndef SIMT_MIN_BLOCKS
+#define SIMT_MIN_BLOCKS 1
+#endif
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Linear CTA index -> (row tile, column tile), grouped along M.
+__device__ __forceinline__ void raster(int pid, int tiles_m, int tiles_n, int &tm, int &tn) {
+    const int per_group = GROUP_M * tiles_n;
+    const int group = pid / per_group;
+    const int first_m = group * GROUP_M;
+    const int gsize = min(tiles_m - first_m, GROUP_M);
+    const int r = pid - group * per_group;
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+}
+
+template <typename TIn, typename TOut, bool VEC>
+__global__ void __launch_bounds__(THREADS, SIMT_MIN_BLOCKS)
+simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__restrict__ C,
+                 int M, int N, int K)
+{
+    __shared__ __align__(16) float As[2][BK][A_LD];
+    __shared__ __align__(16) float Bs[2][BK][B_LD];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wm = warp >> 1, wn = warp & 1;     // 4 x 2 warps
+    const int lm = lane >> 3, ln = lane & 7;     // 4 x 8 lanes
+
+    int tm, tn;
+    raster(blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+
+    // Global -> register staging.  A: 128 rows x 4 quads of k; B: 16 k-rows x
+    // 32 quads of n; each thread moves two quads of each.
+    float ra[2][4], rb[2][4];
+    auto load_tile = [&](int k0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + i * THREADS;
+            const int row = idx >> 2, kq = (idx & 3) * 4;
+            const int gm = m0 + row, gk = k0 + kq;
+            if (VEC) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gm < M && gk < K)
+                    v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gm * K + gk));
+                ra[i][0] = v.x; ra[i][1] = v.y; ra[i][2] = v.z; ra[i][3] = v.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    ra[i][j] = (gm < M && gk + j < K) ? to_f32(A[(size_t)gm * K + gk + j]) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + i * THREADS;
+            const int kr = idx >> 5, nq = (idx & 31) * 4;
+            const int gk = k0 + kr, gn = n0 + nq;
+            if (VEC) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gk < K && gn < N)
+                    v = __ldg(reinterpret_cast<const float4 *>(B + (size_t)gk * N + gn));
+                rb[i][0] = v.x; rb[i][1] = v.y; rb[i][2] = v.z; rb[i][3] = v.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    rb[i][j] = (gk < K && gn + j < N) ? to_f32(B[(size_t)gk * N + gn + j]) : 0.f;
+            }
+        }
+    };
+    auto store_tile = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + i * THREADS;
+            const int row = idx >> 2, kq = (idx & 3) * 4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) As[buf][kq + j][row] = ra[i][j];
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + i * THREADS;
+            const int kr = idx >> 5, nq = (idx & 31) * 4;
+            *reinterpret_cast<float4 *>(&Bs[buf][kr][nq]) =
+                make_float4(rb[i][0], rb[i][1], rb[i][2], rb[i][3]);
+        }
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    const int a_off = wm * 32 + lm * 4;  // + {0, 16}
+    const int b_off = wn * 64 + ln * 4;  // + {0, 32}
+    const int ktiles = (K + BK - 1) / BK;
+
+    load_tile(0);
+    store_tile(0);
+    __syncthreads();
+
+    for (int t = 0; t < ktiles; ++t) {
+        const int buf = t & 1;
+        if (t + 1 < ktiles) load_tile((t + 1) * BK);
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][kk][a_off]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][kk][a_off + 16]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][b_off]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][b_off + 32]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        if (t + 1 < ktiles) store_tile(buf ^ 1);
+        __syncthreads();
+    }
+
+    // Epilogue: each thread writes its 8 rows x (2 x 4) columns.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int gm = m0 + a_off + (i < 4 ? i : 12 + i);
+        if (gm >= M) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int gn = n0 + b_off + h * 32;
+            TOut *dst = C + (size_t)gm * N + gn;
+            if (VEC && gn + 3 < N) {
+                *reinterpret_cast<float4 *>(dst) =
+                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gn + j < N) dst[j] = from_f32<TOut>(acc[i][4 * h + j]);
+            }
+        }
+    }
+}
+
+template <typename TIn, typename TOut, bool VEC>
+cudaError_t launch_typed(const Problem &p, cudaStream_t s) {
+    const long long tiles = (long long)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    simt_gemm_kernel<TIn, TOut, VEC><<<(unsigned)tiles, THREADS, 0, s>>>(
+        static_cast<const TIn *>(p.A), static_cast<const TIn *>(p.B), static_cast<TOut *>(p.C),
+        p.M, p.N, p.K);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_simt(const Problem &p, bool vec4, cudaStream_t s) {
+    switch (p.elt) {
+    case Elt::F32:
+        return vec4 ? launch_typed<float, float, true>(p, s) : launch_typed<float, float, false>(p, s);
+    case Elt::F16:
+        return launch_typed<__half, __half, false>(p, s);
+    case Elt::BF16:
+        return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,485 @@
+// Tensor-core GEMM for 16-bit inputs on sm_103a: tcgen05 MMA, TMEM
+// accumulators, TMA loads, warp specialisation, persistent tile loop.
+//
+// Problem (row-major, tight): C[M,N] = A[M,K] · B[K,N], A and B both f16 or
+// both bf16, FP32 accumulation in tensor memory, one rounding to the output
+// type.  A is K-major (k contiguous); B is MN-major (n contiguous).  The
+// column-major half entry point reaches this kernel through C^T = B^T · A^T.
+//
+// Prior art and what is kept ("Chapter 5 Operators and Runtime", section 5.1.5
+// on asynchronous matrix instructions fed from shared memory, producer and
+// consumer handoff through barriers, descriptors and swizzle; section 5.2.2 on
+// output tiles and their byte counts; "MTT S4000 FP16 GEMM" on epilogue bank
+// conflicts and CTA order):
+//   * CTA tile 128 x 256, K step 64.  One tcgen05.mma.cta_group::1.kind::f16
+//     instruction is M=128, N=256, K=16; four per K step.
+//   * Shared-memory ring of STAGES stages, each holding the A tile (128 rows x
+//     128 bytes) and the B tile (64 k-rows x 256 columns, as four 64-column
+//     boxes), all in the 128-byte swizzled layout TMA writes and the MMA
+//     descriptors describe.  full[s] completes when TMA has landed both tiles
+//     (transaction count); empty[s] completes when the MMAs that read stage s
+//     are done (tcgen05.commit).
+//   * Warp 0: TMA producer.  Warp 1: TMEM allocation and the single MMA-issuing
+//     thread.  Warps 2-5: epilogue (TMEM -> registers -> bf16/half -> global).
+//   * Two accumulators of 256 FP32 columns each in TMEM (512 columns, the whole
+//     tensor memory of the SM), so the epilogue of one tile overlaps the MMAs of
+//     the next: acc_full[b] is committed by the MMA thread, acc_empty[b] is
+//     arrived on by the 128 epilogue threads.
+//   * Persistent grid of one CTA per SM; CTA c takes tiles c, c + grid, ...
+//     in an M-grouped order so that concurrently running tiles share operands
+//     in L2.
+//   * Ragged edges: TMA zero-fills rows/columns/k beyond the matrix; boxes that
+//     lie wholly beyond N are not fetched; stores are predicated.
+//   * Every barrier wait is bounded (about two seconds of %globaltimer); on
+//     expiry the thread records a code in the status word, raises a CTA-wide
+//     abort flag, waits (bounded) for its own asynchronous work and leaves; the
+//     tensor memory is always released.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace gemm_gb300 {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;            // 16 KiB
+constexpr int B_BOX = 64 * BK * 2;              // one 64-column box: 8 KiB
+constexpr int B_STAGE = BN * BK * 2;            // 32 KiB
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int GROUP_M = 8;
+constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+
+constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
+constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + SMEM_TILES + 256 /*barriers*/;
+
+// Status codes ORed into the device status word.
+constexpr int ST_PRODUCER = 1, ST_MMA = 2, ST_EPILOGUE = 4, ST_DRAIN = 8;
+
+struct Bars {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Slow path of mbar_wait: spins with a time limit.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort, bool check_abort) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (check_abort && *abort) return false;
+            if (globaltimer() - t0 > TIMEOUT_NS) return false;
+        }
+    }
+}
+// Waits for the phase of `bar` with the given parity to complete.  Returns false
+// after TIMEOUT_NS, or early when `abort` is raised (if check_abort).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, bool check_abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, check_abort);
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(cols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+// D[tmem] (+)= A[smem] · B[smem], one M=128 N=256 K=16 step.
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when all previously issued MMAs of this thread complete.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+// 32 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), descriptor
+// version 1.  lbo/sbo in bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: FP32 accumulator, A and B of the same
+// 16-bit type (0 = f16, 1 = bf16), A K-major, B MN-major, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format) {
+    return (1u << 4)                      // D: FP32
+           | (ab_format << 7)             // A type
+           | (ab_format << 10)            // B type
+           | (0u << 15)                   // A K-major
+           | (1u << 16)                   // B MN-major
+           | ((uint32_t)(BN >> 3) << 17)  // N / 8
+           | ((uint32_t)(BM >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn) {
+    const int per_group = GROUP_M * tiles_n;
+    const int group = t / per_group;
+    const int first_m = group * GROUP_M;
+    const int gsize = min(tiles_m - first_m, GROUP_M);
+    const int r = t - group * per_group;
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16 *) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half *) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void store1(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void store1(__half *p, float x) { *p = __float2half_rn(x); }
+
+template <typename T, uint32_t AB_FORMAT>
+__global__ void __launch_bounds__(THREADS, 1)
+umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 T *__restrict__ C, int M, int N, int K, int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *a_tiles = smem;
+    uint8_t *b_tiles = smem + STAGES * A_STAGE;
+    Bars *bars = reinterpret_cast<Bars *>(smem + SMEM_TILES);
+    volatile int *abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int num_kb = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->acc_full[b], 1);
+            mbar_init(&bars->acc_empty[b], 128);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            const int n_left = N - tn * BN;
+            const int boxes = n_left >= BN ? 4 : (n_left + 63) / 64;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, true)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars->full[stage], (uint32_t)(A_STAGE + boxes * B_BOX));
+                tma_load_2d(a_tiles + stage * A_STAGE, &tmA, &bars->full[stage], kb * BK, tm * BM);
+                for (int j = 0; j < boxes; ++j)
+                    tma_load_2d(b_tiles + stage * B_STAGE + j * B_BOX, &tmB, &bars->full[stage],
+                                tn * BN + j * 64, kb * BK);
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) {
+            atomicOr(status, ST_PRODUCER);
+            *abort_flag = 1;
+        }
+        // Let every load this thread issued land before the CTA can exit.
+        for (long long i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i) {
+            const int s = (int)(i % STAGES);
+            const uint32_t par = (uint32_t)((i / STAGES) & 1);
+            if (!mbar_wait(&bars->full[s], par, abort_flag, false)) {
+                atomicOr(status, ST_DRAIN);
+                break;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = make_idesc(AB_FORMAT);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        const uint32_t a_base = smem_u32(a_tiles), b_base = smem_u32(b_tiles);
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+            const int buf = it & 1;
+            const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
+            if (!mbar_wait(&bars->acc_empty[buf], acc_par ^ 1u, abort_flag, true)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_addr = a_base + stage * A_STAGE;
+                const uint32_t b_addr = b_base + stage * B_STAGE;
+#pragma unroll
+                for (int ks = 0; ks < BK / UMMA_K; ++ks) {
+                    // A: K-major; a K step of 16 elements is 32 bytes inside the
+                    // 128-byte swizzle row.  8-row groups are 1024 bytes apart.
+                    const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
+                    // B: MN-major; a K step of 16 rows is two 1024-byte atoms.
+                    // 64-column boxes are B_BOX bytes apart (leading offset),
+                    // 8-row groups 1024 bytes apart (stride offset).
+                    const uint64_t bd = smem_desc_sw128(b_addr + ks * 2048, B_BOX, 1024);
+                    umma(d_tmem, ad, bd, idesc, (kb | ks) != 0);
+                }
+                umma_commit(&bars->empty[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            umma_commit(&bars->acc_full[buf]);
+        }
+        if (!ok) {
+            atomicOr(status, ST_MMA);
+            *abort_flag = 1;
+        }
+        // All MMAs of this thread complete before the CTA can release TMEM.
+        umma_commit(&bars->drain);
+        if (!mbar_wait(&bars->drain, 0, abort_flag, false)) atomicOr(status, ST_DRAIN);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+        const int row_in_tile = quarter * 32 + lane;
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            const int buf = it & 1;
+            const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
+            if (!mbar_wait(&bars->acc_full[buf], acc_par, abort_flag, true)) { ok = false; break; }
+            tc_fence_after();
+            __syncwarp();
+            const int row = tm * BM + row_in_tile;
+            const int n0 = tn * BN;
+            T *crow = C + (size_t)row * N;
+#pragma unroll 1
+            for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                const int c0 = n0 + chunk * 32;
+                if (c0 >= N) break;  // warp-uniform
+                uint32_t r[32];
+                tmem_ld_32cols(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + chunk * 32), r);
+                tmem_ld_wait();
+                if (row < M) {
+                    if (c0 + 32 <= N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(crow + c0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 v;
+                            v.x = pack2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]), (T *)nullptr);
+                            v.y = pack2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]), (T *)nullptr);
+                            v.z = pack2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]), (T *)nullptr);
+                            v.w = pack2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]), (T *)nullptr);
+                            dst[q] = v;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j < N) store1(crow + c0 + j, __uint_as_float(r[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->acc_empty[buf]);
+        }
+        if (!ok) {
+            atomicOr(status, ST_EPILOGUE);
+            *abort_flag = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major matrix [rows, cols] of 16-bit elements, box [box_rows, box_cols],
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int rows, int cols, int box_rows,
+              int box_cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, uint32_t F>
+cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_t s) {
+    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, p.A, dt, p.M, p.K, BM, BK)) return cudaErrorInvalidValue;
+    if (!make_map(&tb, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
+    auto kern = umma_gemm_kernel<T, F>;
+    static std::atomic<uint64_t> attr_done{0};  // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_release);
+    }
+    const long long tiles = (long long)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    kern<<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool umma_supported(const Problem &p) {
+    if (p.elt == Elt::F32) return false;
+    auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    // TMA: 16-byte aligned bases and row strides; vector epilogue stores need C
+    // rows 16-byte aligned too (N*2 % 16 == 0 already).
+    return al16(p.A) && al16(p.B) && al16(p.C) && (p.K % 8) == 0 && (p.N % 8) == 0;
+}
+
+cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s) {
+    if (!umma_supported(p)) return cudaErrorInvalidValue;
+    if (p.elt == Elt::BF16) return launch_typed<__nv_bfloat16, 1>(p, num_sms, status, s);
+    return launch_typed<__half, 0>(p, num_sms, status, s);
+}
+
+}  // namespace gemm_gb300

@@ -1,0 +1,129 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * Every entry point computes C = A·B: C[i,j] = sum_k A[i,k]*B[k,j], 2*M*N*K
+ * floating-point operations, with the sum accumulated in FP32 and rounded once
+ * to the output type (round to nearest, ties to even).  Sources of the
+ * operation:
+ *   - the FP32 SGEMM and its FLOP convention: "SGEMM measured and the three
+ *     ledgers" (section 2, the cuBLAS baseline in pure FP32 with TF32 off;
+ *     K3 step 3, GFLOP/s = 2*M*N*K / t);
+ *   - the half, column-major variant: "MTT S4000 FP16 GEMM", section 1 (the
+ *     fixed contest signature gemm_optimized(d_A, d_B, d_C, M, N, K): A, B, C
+ *     column-major, half in and out, FP32 accumulation);
+ *   - the bf16, row-major projection: "Chapter 5 Operators and Runtime",
+ *     section 5.2.1 (the FFN projection C = X·W, BF16 inputs, FP32 accumulator,
+ *     the element loop over i, j, k) and figure 5-7.
+ * alpha = 1 and beta = 0: C is write-only, never read.
+ *
+ * Pointers.  A, B and C are DEVICE pointers (cudaMalloc, torch CUDA tensors,
+ * or any memory the current device can address), owned by the caller.  The
+ * library keeps no reference to them after the call and allocates nothing per
+ * call.  Half and bf16 elements are passed as their 16-bit patterns.
+ *
+ * Leading dimensions are tight:
+ *   _rm (row-major):    A is [M,K] with lda = K, B is [K,N] with ldb = N,
+ *                       C is [M,N] with ldc = N.
+ *   _cm (column-major): A is [M,K] with lda = M, B is [K,N] with ldb = K,
+ *                       C is [M,N] with ldc = M.
+ * Any alignment is accepted.  Pointers or strides that are not 16-byte aligned
+ * select slower kernels; they are never an error.
+ *
+ * Execution.  Calls are asynchronous and ordered on the calling host thread's
+ * stream (gemm_set_stream; default: the legacy default stream).  A call returns
+ * once its kernel is enqueued; gemm_synchronize() waits for it.  Results are
+ * deterministic: the same inputs give bit-identical C on every run (no atomics,
+ * fixed summation order per element).
+ *
+ * Errors.  Every entry point returns a status; nothing is thrown across the ABI.
+ *   GEMM_ERR_INVALID_VALUE      a dimension < 0, or a null pointer needed by the
+ *                               call (A and B when K > 0; C when M*N > 0), or a
+ *                               forced kernel that cannot run this problem.
+ *   GEMM_ERR_ALIAS              C overlaps A or B.
+ *   GEMM_ERR_UNSUPPORTED_DEVICE the current device is not compute capability
+ *                               10.3 (GB300).  There is no fallback to other
+ *                               devices or to the CPU.
+ *   GEMM_ERR_CUDA               a CUDA runtime call or kernel launch failed.
+ *   GEMM_ERR_TIMEOUT            a kernel gave up waiting on one of its own
+ *                               pipeline barriers (reported by gemm_synchronize).
+ * M = 0 or N = 0 is a no-op returning GEMM_OK.  K = 0 fills C with zeros (the
+ * empty sum).
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+#if defined(_WIN32)
+#define GEMM_API __declspec(dllexport)
+#else
+#define GEMM_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm_status_t {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,
+    GEMM_ERR_ALIAS = 2,
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3,
+    GEMM_ERR_CUDA = 4,
+    GEMM_ERR_TIMEOUT = 5
+} gemm_status_t;
+
+/* Pure FP32 row-major SGEMM on the CUDA cores: FP32 FFMA only, no TF32 and no
+ * tensor cores ("SGEMM measured and the three ledgers", section 2).  A [M,K],
+ * B [K,N], C [M,N], all row-major float. */
+GEMM_API gemm_status_t gemm_f32_rm(const float *A, const float *B, float *C,
+                                   int M, int N, int K);
+
+/* Half column-major GEMM with FP32 accumulation ("MTT S4000 FP16 GEMM",
+ * section 1).  A [M,K] (lda = M), B [K,N] (ldb = K), C [M,N] (ldc = M), all
+ * column-major IEEE half bit patterns. */
+GEMM_API gemm_status_t gemm_f16_cm(const uint16_t *A, const uint16_t *B, uint16_t *C,
+                                   int M, int N, int K);
+
+/* BF16 row-major projection GEMM with FP32 accumulation ("Chapter 5 Operators
+ * and Runtime", section 5.2.1).  A [M,K], B [K,N], C [M,N], row-major bf16 bit
+ * patterns. */
+GEMM_API gemm_status_t gemm_bf16_rm(const uint16_t *A, const uint16_t *B, uint16_t *C,
+                                    int M, int N, int K);
+
+/* Stream for the calling host thread's subsequent calls: a cudaStream_t passed
+ * as void*.  NULL selects the legacy default stream.  The stream stays owned by
+ * the caller and must outlive the calls issued on it. */
+GEMM_API gemm_status_t gemm_set_stream(void *cuda_stream);
+
+/* The calling host thread's current stream (NULL = legacy default stream). */
+GEMM_API void *gemm_get_stream(void);
+
+/* Waits for the calling thread's stream; returns GEMM_ERR_CUDA for an
+ * asynchronous CUDA error and GEMM_ERR_TIMEOUT if a kernel of this library
+ * recorded a pipeline timeout on the current device (the record is cleared). */
+GEMM_API gemm_status_t gemm_synchronize(void);
+
+/* Static, human-readable name of a status code. */
+GEMM_API const char *gemm_status_string(gemm_status_t status);
+
+/* Name of the kernel the calling thread's last call dispatched to, e.g.
+ * "simt_f32_vec4", "umma_bf16", "gemv_bf16_vec", "zero_fill", "noop" (static
+ * string; for tests and benchmarks). */
+GEMM_API const char *gemm_last_kernel(void);
+
+/* Message of the last CUDA error seen by the calling thread ("" if none). */
+GEMM_API const char *gemm_last_error(void);
+
+/* Test and benchmark hook: forces the calling thread's later calls onto one
+ * kernel family -- "simt", "simt_scalar", "gemv", "gemv_scalar", "umma" -- or
+ * back to automatic dispatch with NULL or "".  A forced family that cannot run a
+ * given problem makes that call return GEMM_ERR_INVALID_VALUE; an unknown name
+ * is rejected here with GEMM_ERR_INVALID_VALUE. */
+GEMM_API gemm_status_t gemm_force_kernel(const char *family);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads and exports every symbol include/gemm.h
+declares; host-side argument checks that return before any device work.
+No GPU is needed: nothing here launches a kernel."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dense_matrix_multiply_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"GEMM_API\s+[\w\s\*]+?\b(gemm_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def built():
+    g.ensure_built()
+    return g.load()
+
+
+def test_header_declares_the_three_entry_points():
+    syms = declared_symbols()
+    for name in ("gemm_f32_rm", "gemm_f16_cm", "gemm_bf16_rm"):
+        assert name in syms
+    assert len(syms) == len(set(syms))
+
+
+def test_library_exports_every_declared_symbol(built):
+    for name in declared_symbols():
+        assert hasattr(built, name), name
+    # and the binding wraps each of them
+    assert set(declared_symbols()) == set(g.SIGNATURES)
+
+
+def test_only_the_api_is_exported(built):
+    out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert set(declared_symbols()) <= exported
+    assert not [s for s in exported if s.startswith("_ZN") and "gemm_gb300" in s]
+
+
+def test_library_is_built_for_sm_103a_only():
+    from dense_matrix_multiply_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(built):
+    for code, name in g.STATUS_NAMES.items():
+        assert g.gemm_status_string(code) == name
+    assert g.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def test_force_kernel_names(built):
+    for fam in ("simt", "simt_scalar", "gemv", "gemv_scalar", "umma", None, ""):
+        g.gemm_force_kernel(fam)
+    with pytest.raises(g.GemmError):
+        g.gemm_force_kernel("cpu")
+    g.gemm_force_kernel(None)
+
+
+def test_host_side_argument_errors(built):
+    lib = built
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.addressof(buf)
+    for fn in (lib.gemm_f32_rm, lib.gemm_f16_cm, lib.gemm_bf16_rm):
+        assert fn(p, p + 1024, p + 2048, -1, 4, 4) == 1          # negative dimension
+        assert fn(p, p + 1024, p + 2048, 4, 4, -4) == 1
+        assert fn(p, p + 1024, p + 2048, 0, 4, 4) == 0           # empty output: no-op
+        assert lib.gemm_last_kernel() == b"noop"
+        assert fn(p, p + 1024, p + 2048, 4, 0, 4) == 0
+        assert fn(p, p + 1024, None, 4, 4, 4) == 1                # null C
+        assert fn(None, p + 1024, p + 2048, 4, 4, 4) == 1         # null A with K > 0
+        assert fn(p, p + 16, p + 8, 4, 4, 4) == 2                 # C overlaps A and B
+        assert fn(p, p + 1024, p + 1024, 4, 4, 4) == 2            # C is B
+
+
+def test_stream_is_per_thread(built):
+    import threading
+    g.gemm_set_stream(1234)
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(g.gemm_get_stream()))
+    t.start()
+    t.join()
+    assert g.gemm_get_stream() == 1234 and seen == [0]
+    g.gemm_set_stream(None)
+    assert g.gemm_get_stream() == 0
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(g, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(g, "_lib", None)
+    with pytest.raises(RuntimeError, match="CUDA extension missing"):
+        g.load()
