@@ -239,3 +239,30 @@ def test_round_to_output_type():
     assert compare.round_to("bf16_rm", np.array([4100.0]))[0] == 4096.0
     assert compare.round_to("f16_cm", np.array([4100.0]))[0] == 4100.0
     assert compare.round_to("f32_rm", np.array([16777217.0]))[0] == 16777216.0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("K", [16, 64, 512, 4096])
+def test_half_tolerance_admits_the_exact_rounding(dtype, K):
+    """The correctly rounded value of C_ref always passes; for bf16 at small K, where
+    the ulp floor is what binds, a value two ulps off fails."""
+    rng = np.random.default_rng(K)
+    c = np.concatenate([rng.uniform(-20, 20, 20000), 2.0 ** np.arange(-5, 5) * (1 + 2.0 ** -9)])
+    if dtype == "f16":
+        r = c.astype(np.float16).astype(np.float64)
+    else:
+        r = compare.round_to("bf16_rm", c.astype(np.float32).astype(np.float64))
+    tol = compare.tol_half(c, K, dtype)
+    assert np.all(np.abs(r - c) <= tol)
+    off = r + 2.0 * compare.ulp_out(dtype, c) * np.sign(c)
+    if dtype == "bf16" and K <= 64:
+        big = np.abs(c) >= 1.0
+        assert np.all(np.abs(off - c)[big] > tol[big])
+
+
+def test_output_ulp_values():
+    assert compare.ulp_out("bf16", np.array([1.0]))[0] == 2.0 ** -7
+    assert compare.ulp_out("bf16", np.array([7.9]))[0] == 2.0 ** -5
+    assert compare.ulp_out("f16", np.array([1.0]))[0] == 2.0 ** -10
+    assert compare.ulp_out("f16", np.array([0.0]))[0] == 2.0 ** -24
+    assert compare.ulp_out("f16", np.array([1e-6]))[0] == 2.0 ** -24  # subnormal spacing
