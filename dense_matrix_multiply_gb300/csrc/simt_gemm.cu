@@ -30,13 +30,10 @@
 namespace gemm_gb300 {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 16, THREADS = 256;
+constexpr int BM = 128, BN = 128, THREADS = 256;
 constexpr int A_LD = BM + 4;  // padded row of the k-major A tile (floats)
 constexpr int B_LD = BN;      // row of the B tile (floats)
 constexpr int GROUP_M = 8;
-#ifndef SIMT_MIN_BLOCKS
-#define SIMT_MIN_BLOCKS 1
-#endif
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
@@ -60,8 +57,10 @@ __device__ __forceinline__ void raster(int pid, int tiles_m, int tiles_n, int &t
     tn = r / gsize;
 }
 
-template <typename TIn, typename TOut, bool VEC>
-__global__ void __launch_bounds__(THREADS, SIMT_MIN_BLOCKS)
+// BK: K step of a shared tile (8 or 16).  MINB: CTAs per SM the register
+// budget is sized for (__launch_bounds__).
+template <typename TIn, typename TOut, bool VEC, int BK, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB)
 simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__restrict__ C,
                  int M, int N, int K)
 {
@@ -77,14 +76,17 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
     raster(blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
 
-    // Global -> register staging.  A: 128 rows x 4 quads of k; B: 16 k-rows x
-    // 32 quads of n; each thread moves two quads of each.
-    float ra[2][4], rb[2][4];
+    // Global -> register staging.  A: 128 rows x QA quads of k; B: BK k-rows x
+    // 32 quads of n; each thread moves LA quads of A and LB quads of B.
+    constexpr int QA = BK / 4;
+    constexpr int LA = BM * QA / THREADS, LB = BK * (BN / 4) / THREADS;
+    static_assert(LA >= 1 && LB >= 1 && BM * QA % THREADS == 0, "tile/thread mapping");
+    float ra[LA][4], rb[LB][4];
     auto load_tile = [&](int k0) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LA; ++i) {
             const int idx = tid + i * THREADS;
-            const int row = idx >> 2, kq = (idx & 3) * 4;
+            const int row = idx / QA, kq = (idx % QA) * 4;
             const int gm = m0 + row, gk = k0 + kq;
             if (VEC) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -98,7 +100,7 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
             }
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LB; ++i) {
             const int idx = tid + i * THREADS;
             const int kr = idx >> 5, nq = (idx & 31) * 4;
             const int gk = k0 + kr, gn = n0 + nq;
@@ -116,14 +118,14 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
     };
     auto store_tile = [&](int buf) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LA; ++i) {
             const int idx = tid + i * THREADS;
-            const int row = idx >> 2, kq = (idx & 3) * 4;
+            const int row = idx / QA, kq = (idx % QA) * 4;
 #pragma unroll
             for (int j = 0; j < 4; ++j) As[buf][kq + j][row] = ra[i][j];
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LB; ++i) {
             const int idx = tid + i * THREADS;
             const int kr = idx >> 5, nq = (idx & 31) * 4;
             *reinterpret_cast<float4 *>(&Bs[buf][kr][nq]) =
@@ -186,11 +188,19 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
     }
 }
 
+// Tile configuration of the SIMT kernel: K step and CTAs per SM.
+#ifndef SIMT_BK
+#define SIMT_BK 16
+#endif
+#ifndef SIMT_MINB
+#define SIMT_MINB 1
+#endif
+
 template <typename TIn, typename TOut, bool VEC>
 cudaError_t launch_typed(const Problem &p, cudaStream_t s) {
     const long long tiles = (long long)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    simt_gemm_kernel<TIn, TOut, VEC><<<(unsigned)tiles, THREADS, 0, s>>>(
+    simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB><<<(unsigned)tiles, THREADS, 0, s>>>(
         static_cast<const TIn *>(p.A), static_cast<const TIn *>(p.B), static_cast<TOut *>(p.C),
         p.M, p.N, p.K);
     return cudaGetLastError();
