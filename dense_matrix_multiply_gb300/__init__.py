@@ -35,6 +35,7 @@ SIGNATURES = {
     "gemm_f32_rm": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_f16_cm": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_bf16_rm": ([_VP, _VP, _VP, _I, _I, _I], _I),
+    "gemm_bf16_rm_noalloc": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_set_stream": ([_VP], _I),
     "gemm_get_stream": ([], _VP),
     "gemm_synchronize": ([], _I),
@@ -120,6 +121,12 @@ def gemm_f16_cm(A, B, C, M: int, N: int, K: int) -> None:
 def gemm_bf16_rm(A, B, C, M: int, N: int, K: int) -> None:
     """C[M,N] = A[M,K]·B[K,N], row-major bf16, FP32 accumulation."""
     _call("gemm_bf16_rm", A, B, C, M, N, K)
+
+
+def gemm_bf16_rm_noalloc(A, B, C, M: int, N: int, K: int) -> None:
+    """As gemm_bf16_rm, on the tensor-core kernel with its scratch in a static
+    device array: the call allocates no device memory."""
+    _call("gemm_bf16_rm_noalloc", A, B, C, M, N, K)
 
 
 def gemm_set_stream(stream) -> None:

@@ -168,6 +168,41 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     return finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
 }
 
+// Capability and SM count of the current device, without allocating anything
+// (used only by the allocation-free entry point).
+struct PlainDeviceInfo {
+    std::once_flag once;
+    bool supported = false;
+    int num_sms = 0;
+    cudaError_t err = cudaSuccess;
+};
+PlainDeviceInfo g_plain_devices[kMaxDevices];
+
+gemm_status_t plain_device_info(PlainDeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    PlainDeviceInfo &d = g_plain_devices[dev];
+    std::call_once(d.once, [&] {
+        int major = 0, minor = 0;
+        cudaError_t err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        d.err = err;
+        d.supported = err == cudaSuccess && major == 10 && minor == 3;
+    });
+    if (d.err != cudaSuccess) { record_cuda_error(d.err); return GEMM_ERR_CUDA; }
+    if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return GEMM_OK;
+}
+
+void record_message(const char *msg) {
+    strncpy(t_last_error, msg, sizeof(t_last_error) - 1);
+    t_last_error[sizeof(t_last_error) - 1] = '\0';
+}
+
 }  // namespace
 
 extern "C" {
@@ -186,6 +221,42 @@ GEMM_API gemm_status_t gemm_f16_cm(const uint16_t *A, const uint16_t *B, uint16_
 
 GEMM_API gemm_status_t gemm_bf16_rm(const uint16_t *A, const uint16_t *B, uint16_t *C, int M, int N, int K) {
     return run(A, B, C, M, N, K, Elt::BF16);
+}
+
+// Allocation-free bf16 entry point: the tensor-core kernel with its status word
+// in a static device array instead of library-allocated memory.
+GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B, uint16_t *C, int M, int N,
+                                            int K) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) { t_last_kernel = "noop"; return GEMM_OK; }
+    if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_VALUE;
+    const size_t c_bytes = (size_t)M * N * 2;
+    if (overlaps(C, c_bytes, A, (size_t)M * K * 2) || overlaps(C, c_bytes, B, (size_t)K * N * 2))
+        return GEMM_ERR_ALIAS;
+    PlainDeviceInfo *dev = nullptr;
+    gemm_status_t st = plain_device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = t_stream;
+    if (K == 0) {
+        const unsigned grid = (unsigned)(dev->num_sms * 4);
+        if (aligned16(C)) {
+            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)C, c_bytes / 16, (uint8_t *)C + (c_bytes & ~(size_t)15),
+                                                  c_bytes & 15);
+        } else {
+            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)C, c_bytes);
+        }
+        return finish(cudaGetLastError(), "zero_fill");
+    }
+    Problem p{A, B, C, M, N, K, Elt::BF16};
+    if (!umma_supported(p)) {
+        record_message("gemm_bf16_rm_noalloc: A, B and C must be 16-byte aligned and K, N multiples of 8");
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    if (umma_noalloc_scratch_need(p) > kNoallocScratchBytes) {
+        record_message("gemm_bf16_rm_noalloc: problem needs more scratch than the static array holds");
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    return finish(launch_umma_noalloc(p, dev->num_sms, s), "umma_bf16_noalloc");
 }
 
 GEMM_API gemm_status_t gemm_set_stream(void *cuda_stream) {

@@ -36,4 +36,10 @@ cudaError_t launch_gemv(const Problem &p, bool vec, cudaStream_t s);
 cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s);
 bool umma_supported(const Problem &p);
 
+// Allocation-free variant of launch_umma: the status word lives in a static
+// device array of kNoallocScratchBytes bytes (see umma_gemm.cu).
+constexpr size_t kNoallocScratchBytes = 256;
+size_t umma_noalloc_scratch_need(const Problem &p);
+cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s);
+
 }  // namespace gemm_gb300

@@ -482,4 +482,43 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
     return launch_typed<__half, 0>(p, num_sms, status, s);
 }
 
+// ------------------------------------------------------- allocation-free variant
+// Scratch of the allocation-free entry point (gemm_bf16_rm_noalloc).  The
+// tensor-core kernel's only scratch is its 4-byte status word, in which a CTA
+// records a pipeline timeout.  The regular entry points keep that word in
+// memory the library cudaMallocs on first use of a device; this variant keeps
+// it in the file-scope array below instead, so it never allocates.  Every GPU
+// that loads the library holds these kNoallocScratchBytes until the process
+// exits.  All calls share the array: the word is cleared on the caller's
+// stream before each launch, and calls that overlap on the GPU race on it.
+static __device__ __align__(256) int g_noalloc_scratch[kNoallocScratchBytes / sizeof(int)];
+
+namespace {
+struct NoallocScratch {
+    std::once_flag once;
+    int *ptr = nullptr;  // device address of g_noalloc_scratch on this device
+    cudaError_t err = cudaSuccess;
+};
+NoallocScratch g_noalloc[64];
+}  // namespace
+
+size_t umma_noalloc_scratch_need(const Problem &) { return sizeof(int); }
+
+cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    NoallocScratch &d = g_noalloc[dev];
+    // Set-up, once per device, with that device current: in host code the
+    // array's name is only a host-side stand-in, so its device address is
+    // looked up here and passed to the kernel.
+    std::call_once(d.once, [&] { d.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.ptr), g_noalloc_scratch); });
+    if (d.err != cudaSuccess) return d.err;
+    if (umma_noalloc_scratch_need(p) > kNoallocScratchBytes) return cudaErrorInvalidValue;
+    e = cudaMemsetAsync(d.ptr, 0, sizeof(int), s);  // the status word starts at zero
+    if (e != cudaSuccess) return e;
+    return launch_umma(p, num_sms, d.ptr, s);
+}
+
 }  // namespace gemm_gb300

@@ -91,6 +91,34 @@ GEMM_API gemm_status_t gemm_f16_cm(const uint16_t *A, const uint16_t *B, uint16_
 GEMM_API gemm_status_t gemm_bf16_rm(const uint16_t *A, const uint16_t *B, uint16_t *C,
                                     int M, int N, int K);
 
+/* BF16 row-major GEMM that allocates no device memory.  The pages have no
+ * counterpart to this entry point: it is an interface addition for callers that
+ * cannot call cudaMalloc.  Some host applications own all device memory through
+ * their own allocator (a framework's caching pool that has already reserved the
+ * GPU's memory, or an embedding program with a fixed memory budget) and forbid
+ * allocations made behind its back; others run on latency-critical paths where
+ * cudaMalloc's implicit device-wide synchronisation is not acceptable.
+ *
+ * Same arguments, layout, rounding and error codes as gemm_bf16_rm, but always
+ * on the tensor-core kernel, so it needs 16-byte aligned A, B, C and K and N
+ * multiples of 8 (otherwise GEMM_ERR_INVALID_VALUE, with a message in
+ * gemm_last_error).  The kernel's scratch -- its 4-byte pipeline-timeout status
+ * word, the same for every M, N, K -- lives in a static device array of 256
+ * bytes that every GPU loading this library holds until the process exits;
+ * a problem needing more scratch than that would be refused with
+ * GEMM_ERR_INVALID_VALUE.  No call makes cudaMalloc, cudaFree or any other
+ * allocating call.
+ *
+ * The first call on a device looks up the array's device address (set-up, once
+ * per device, with that device current); make that first call before any
+ * stream capture.  Every call clears the status word on the caller's stream
+ * before its kernel runs; all calls share the array, so calls that overlap on
+ * the GPU race on it.  A timeout recorded there is not reported by
+ * gemm_synchronize, which reads only the status word of the allocating entry
+ * points. */
+GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B, uint16_t *C,
+                                            int M, int N, int K);
+
 /* Stream for the calling host thread's subsequent calls: a cudaStream_t passed
  * as void*.  NULL selects the legacy default stream.  The stream stays owned by
  * the caller and must outlive the calls issued on it. */
