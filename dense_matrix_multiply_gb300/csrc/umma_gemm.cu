@@ -61,15 +61,17 @@ constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + SMEM_TILES + 256 /*barrier
 // Status codes ORed into the device status word.
 constexpr int ST_PRODUCER = 1, ST_MMA = 2, ST_EPILOGUE = 4, ST_DRAIN = 8;
 
-struct Bars {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+template <int NSTAGES>
+struct BarsT {
+    uint64_t full[NSTAGES];
+    uint64_t empty[NSTAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+using Bars = BarsT<STAGES>;
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -178,6 +180,110 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---- CTA-pair (cta_group::2) forms.  A kernel uses one cta_group throughout.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// All threads of both CTAs of the cluster (warp-converged).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                    bool check_abort) {
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (check_abort && *abort) return false;
+            if (globaltimer() - t0 > TIMEOUT_NS) return false;
+        }
+    }
+}
+// Bounded wait with cluster-scope acquire (barriers that CTAs of the pair signal).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  bool check_abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return mbar_wait_cluster_slow(bar, parity, abort, check_abort);
+}
+// TMA load into this CTA's shared memory, completion counted on an mbarrier
+// that may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
+                                                 int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(cols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+// D[tmem of both CTAs] (+)= A[smem of both CTAs] · B[smem of both CTAs]: one
+// M=256 (128 rows per CTA) N=256 (128 columns of B per CTA) K=16 step.
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at this shared offset in every CTA of `mask` when
+// the pair's previously issued MMAs complete.
+__device__ __forceinline__ void umma_commit_pair_multicast(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), descriptor
 // version 1.  lbo/sbo in bytes.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -192,14 +298,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor for kind::f16: FP32 accumulator, A and B of the same
 // 16-bit type (0 = f16, 1 = bf16), A K-major, B MN-major, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format) {
-    return (1u << 4)                      // D: FP32
-           | (ab_format << 7)             // A type
-           | (ab_format << 10)            // B type
-           | (0u << 15)                   // A K-major
-           | (1u << 16)                   // B MN-major
-           | ((uint32_t)(BN >> 3) << 17)  // N / 8
-           | ((uint32_t)(BM >> 4) << 24); // M / 16
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m = BM, uint32_t n = BN) {
+    return (1u << 4)              // D: FP32
+           | (ab_format << 7)     // A type
+           | (ab_format << 10)    // B type
+           | (0u << 15)           // A K-major
+           | (1u << 16)           // B MN-major
+           | ((n >> 3) << 17)     // N / 8
+           | ((m >> 4) << 24);    // M / 16
 }
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &tm, int &tn) {
@@ -407,6 +513,233 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
+// ------------------------------------------------------------------ CTA pairs
+// The same product on 256 x 256 tiles computed by a cluster of two CTAs on
+// two SMs (tcgen05 cta_group::2).  CTA r of the pair holds rows r*128..+127 of
+// the A tile and columns r*128..+127 of the B tile in its own shared memory;
+// the leader's (rank 0) single MMA thread issues M=256, N=256, K=16 steps
+// that read both CTAs' shared memory and write each CTA's 128 accumulator
+// rows into that CTA's tensor memory.  Per CTA a stage is 32 KiB (half the B
+// bytes of the single-CTA tile), so six stages fit.
+//   * Both producers load their halves; every load completes on the LEADER's
+//     full[s] (the leader arms it with the bytes of both CTAs).
+//   * The leader's commit after a stage arrives on empty[s] of both CTAs
+//     (multicast), freeing the stage in both.
+//   * acc_full[b] of both CTAs is committed the same way; each CTA's 128
+//     epilogue threads read their own tensor memory and arrive on the
+//     leader's acc_empty[b] (256 arrivals).
+// No TMA multicast is used: each CTA fetches only its own operand halves.
+namespace pairk {
+constexpr int PBM = 256, PBN = 256;
+constexpr int PSTAGES = 6;
+constexpr int P_A_STAGE = 128 * BK * 2;                        // 16 KiB per CTA
+constexpr int P_B_STAGE = 128 * BK * 2;                        // 16 KiB per CTA (two 64-column boxes)
+constexpr uint32_t P_STAGE_TX = 2u * (P_A_STAGE + P_B_STAGE);  // bytes per stage, both CTAs
+constexpr int P_SMEM_TILES = PSTAGES * (P_A_STAGE + P_B_STAGE);
+constexpr int P_SMEM_BYTES = 1024 + P_SMEM_TILES + 256;
+constexpr int P_GROUP_M = 8;  // pair tiles per raster group
+using PBars = BarsT<PSTAGES>;
+static_assert(sizeof(PBars) <= 256, "barrier block");
+}  // namespace pairk
+
+template <typename T, uint32_t AB_FORMAT>
+__global__ void __launch_bounds__(THREADS, 1)
+umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 T *__restrict__ C, int M, int N, int K, int *status)
+{
+    using namespace pairk;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *a_tiles = smem;
+    uint8_t *b_tiles = smem + PSTAGES * P_A_STAGE;
+    PBars *bars = reinterpret_cast<PBars *>(smem + P_SMEM_TILES);
+    volatile int *abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = (int)cluster_id_x(), nclusters = (int)cluster_count_x();
+    const int tiles_m = (M + PBM - 1) / PBM, tiles_n = (N + PBN - 1) / PBN;
+    const int num_tiles = tiles_m * tiles_n;
+    const int num_kb = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->acc_full[b], 1);
+            mbar_init(&bars->acc_empty[b], 256);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised before any cross-CTA use
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    auto coords = [&](int t, int &tm, int &tn) {
+        const int per_group = P_GROUP_M * tiles_n;
+        const int group = t / per_group;
+        const int first_m = group * P_GROUP_M;
+        const int gsize = min(tiles_m - first_m, P_GROUP_M);
+        const int r = t - group * per_group;
+        tm = first_m + r % gsize;
+        tn = r / gsize;
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+            int tm, tn;
+            coords(t, tm, tn);
+            const int row0 = tm * PBM + (int)rank * 128;
+            const int col0 = tn * PBN + (int)rank * 128;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_cluster(&bars->empty[stage], phase ^ 1u, abort_flag, true)) { ok = false; break; }
+                const uint32_t full_leader = map_to_rank(&bars->full[stage], 0);
+                if (leader) mbar_arrive_expect_tx(&bars->full[stage], P_STAGE_TX);
+                uint8_t *a_dst = a_tiles + stage * P_A_STAGE;
+                uint8_t *b_dst = b_tiles + stage * P_B_STAGE;
+                tma_load_2d_pair(a_dst, &tmA, full_leader, kb * BK, row0);
+                tma_load_2d_pair(b_dst, &tmB, full_leader, col0, kb * BK);
+                tma_load_2d_pair(b_dst + B_BOX, &tmB, full_leader, col0 + 64, kb * BK);
+                ++issued;
+                if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) {
+            atomicOr(status, ST_PRODUCER);
+            *abort_flag = 1;
+        }
+        if (leader) {
+            // Every stage this pair armed has landed (both halves) before exit.
+            for (long long i = (issued > PSTAGES ? issued - PSTAGES : 0); i < issued; ++i) {
+                const int s = (int)(i % PSTAGES);
+                const uint32_t par = (uint32_t)((i / PSTAGES) & 1);
+                if (!mbar_wait_cluster(&bars->full[s], par, abort_flag, false)) {
+                    atomicOr(status, ST_DRAIN);
+                    break;
+                }
+            }
+        } else if (!ok) {
+            // The peer cannot observe the leader's barriers: give loads already
+            // issued into its own shared memory time to land.
+            const unsigned long long t0 = globaltimer();
+            while (globaltimer() - t0 < 100000ull) { }
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------------------ MMA issuer (leader)
+        constexpr uint32_t idesc = make_idesc(AB_FORMAT, PBM, PBN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        const uint32_t a_base = smem_u32(a_tiles), b_base = smem_u32(b_tiles);
+        for (int t = cluster; t < num_tiles && ok; t += nclusters, ++it) {
+            const int buf = it & 1;
+            const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
+            if (!mbar_wait_cluster(&bars->acc_empty[buf], acc_par ^ 1u, abort_flag, true)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * PBN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_cluster(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_addr = a_base + stage * P_A_STAGE;
+                const uint32_t b_addr = b_base + stage * P_B_STAGE;
+#pragma unroll
+                for (int ks = 0; ks < BK / UMMA_K; ++ks) {
+                    const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(b_addr + ks * 2048, B_BOX, 1024);
+                    umma_pair(d_tmem, ad, bd, idesc, (kb | ks) != 0);
+                }
+                umma_commit_pair_multicast(&bars->empty[stage], 0x3);
+                if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            umma_commit_pair_multicast(&bars->acc_full[buf], 0x3);
+        }
+        if (!ok) {
+            atomicOr(status, ST_MMA);
+            *abort_flag = 1;
+        }
+        umma_commit_pair(&bars->drain);
+        if (!mbar_wait_cluster(&bars->drain, 0, abort_flag, false)) atomicOr(status, ST_DRAIN);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const int row_in_tile = (int)rank * 128 + quarter * 32 + lane;
+        int it = 0;
+        bool ok = true;
+        for (int t = cluster; t < num_tiles; t += nclusters, ++it) {
+            int tm, tn;
+            coords(t, tm, tn);
+            const int buf = it & 1;
+            const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
+            if (!mbar_wait_cluster(&bars->acc_full[buf], acc_par, abort_flag, true)) { ok = false; break; }
+            tc_fence_after();
+            __syncwarp();
+            const int row = tm * PBM + row_in_tile;
+            const int n0 = tn * PBN;
+            T *crow = C + (size_t)row * N;
+#pragma unroll 1
+            for (int chunk = 0; chunk < PBN / 32; ++chunk) {
+                const int c0 = n0 + chunk * 32;
+                if (c0 >= N) break;  // warp-uniform
+                uint32_t r[32];
+                tmem_ld_32cols(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * PBN + chunk * 32), r);
+                tmem_ld_wait();
+                if (row < M) {
+                    if (c0 + 32 <= N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(crow + c0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 v;
+                            v.x = pack2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]), (T *)nullptr);
+                            v.y = pack2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]), (T *)nullptr);
+                            v.z = pack2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]), (T *)nullptr);
+                            v.w = pack2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]), (T *)nullptr);
+                            dst[q] = v;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j < N) store1(crow + c0 + j, __uint_as_float(r[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(map_to_rank(&bars->acc_empty[buf], 0));
+        }
+        if (!ok) {
+            atomicOr(status, ST_EPILOGUE);
+            *abort_flag = 1;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();  // no CTA leaves while its peer may still touch its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -466,6 +799,61 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     return cudaGetLastError();
 }
 
+// Largest number of co-resident two-CTA clusters of the pair kernel, per device
+// (0: the pair kernel cannot be launched).
+template <typename T, uint32_t F>
+int pair_clusters_max(int dev) {
+    static std::atomic<int> cached[64];
+    static std::once_flag once[64];
+    std::call_once(once[dev & 63], [&] {
+        auto kern = umma_pair_kernel<T, F>;
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pairk::P_SMEM_BYTES) ==
+                cudaSuccess &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2, 1, 1);
+            cfg.blockDim = dim3(THREADS, 1, 1);
+            cfg.dynamicSmemBytes = pairk::P_SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        cached[dev & 63].store(n);
+    });
+    return cached[dev & 63].load();
+}
+
+template <typename T, uint32_t F>
+cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, cudaStream_t s) {
+    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, p.A, dt, p.M, p.K, 128, BK)) return cudaErrorInvalidValue;
+    if (!make_map(&tb, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
+    const long long tiles = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * ((p.N + pairk::PBN - 1) / pairk::PBN);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pairk::P_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F>, ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, status);
+}
+
 }  // namespace
 
 bool umma_supported(const Problem &p) {
@@ -478,6 +866,18 @@ bool umma_supported(const Problem &p) {
 
 cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s) {
     if (!umma_supported(p)) return cudaErrorInvalidValue;
+    // 256-row tiles on CTA pairs once M fills more than one 128-row tile.
+    if (p.M > BM) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const int cmax = p.elt == Elt::BF16 ? pair_clusters_max<__nv_bfloat16, 1>(dev)
+                                            : pair_clusters_max<__half, 0>(dev);
+        if (cmax > 0) {
+            return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(p, cmax, status, s)
+                                      : launch_pair_typed<__half, 0>(p, cmax, status, s);
+        }
+    }
     if (p.elt == Elt::BF16) return launch_typed<__nv_bfloat16, 1>(p, num_sms, status, s);
     return launch_typed<__half, 0>(p, num_sms, status, s);
 }
