@@ -147,10 +147,10 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
         return finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
     case Family::Gemv:
         if (M > kGemvMaxM || !gemv_vec_ok) return GEMM_ERR_INVALID_VALUE;
-        return finish(launch_gemv(p, true, s), kernel_name("gemv", elt));
+        return finish(launch_gemv(p, true, dev->num_sms, s), kernel_name("gemv", elt));
     case Family::GemvScalar:
         if (M > kGemvMaxM) return GEMM_ERR_INVALID_VALUE;
-        return finish(launch_gemv(p, false, s), kernel_name("gemv_scalar", elt));
+        return finish(launch_gemv(p, false, dev->num_sms, s), kernel_name("gemv_scalar", elt));
     case Family::Umma:
         if (!umma_supported(p)) return GEMM_ERR_INVALID_VALUE;
         return finish(launch_umma(p, dev->num_sms, dev->status, s), kernel_name("umma", elt));
@@ -159,8 +159,8 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     }
 
     if (M <= kGemvMaxM)
-        return gemv_vec_ok ? finish(launch_gemv(p, true, s), kernel_name("gemv", elt))
-                           : finish(launch_gemv(p, false, s), kernel_name("gemv_scalar", elt));
+        return gemv_vec_ok ? finish(launch_gemv(p, true, dev->num_sms, s), kernel_name("gemv", elt))
+                           : finish(launch_gemv(p, false, dev->num_sms, s), kernel_name("gemv_scalar", elt));
     if (elt == Elt::F32)
         return simt_vec_ok ? finish(launch_simt(p, true, s), kernel_name("simt", elt))
                            : finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
@@ -249,7 +249,8 @@ GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B
     }
     Problem p{A, B, C, M, N, K, Elt::BF16};
     if (!umma_supported(p)) {
-        record_message("gemm_bf16_rm_noalloc: A, B and C must be 16-byte aligned and K, N multiples of 8");
+        record_message("gemm_bf16_rm_noalloc: needs B and C 16-byte aligned with N % 8 == 0, and A 16-byte "
+                       "aligned with K % 8 == 0 or 8-byte aligned with K % 4 == 0");
         return GEMM_ERR_INVALID_VALUE;
     }
     if (umma_noalloc_scratch_need(p) > kNoallocScratchBytes) {

@@ -24,11 +24,12 @@ struct Problem {
 // f32 only).  Returns the launch status.
 cudaError_t launch_simt(const Problem &p, bool vec4, cudaStream_t s);
 
-// Skinny-M kernel (M <= kGemvMaxM): streams B once, FP32 accumulation, fixed
-// order reduction in shared memory.  vec: 16-byte loads of B (needs N a
-// multiple of the vector width and a 16-byte aligned B).
+// Skinny-M kernel (M <= kGemvMaxM): streams B once, FP32 accumulation, K split
+// over a thread-block cluster, fixed-order reduction in shared and distributed
+// shared memory.  vec: 16-byte loads of B (needs N a multiple of the vector
+// width and a 16-byte aligned B).  num_sms sizes the split.
 constexpr int kGemvMaxM = 8;
-cudaError_t launch_gemv(const Problem &p, bool vec, cudaStream_t s);
+cudaError_t launch_gemv(const Problem &p, bool vec, int num_sms, cudaStream_t s);
 
 // tcgen05 tensor-core kernel for 16-bit inputs.  Needs 16-byte aligned A, B, C
 // and K*2, N*2 multiples of 16 bytes (TMA strides).  num_sms: persistent grid

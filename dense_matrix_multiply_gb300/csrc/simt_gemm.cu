@@ -4,18 +4,20 @@
 // blocking and 128-bit shared loads; the 800 -> 10600 GFLOPS SGEMM blog,
 // versions 2-4 -- shared tiles, register micro-tiles, double buffering; chapter
 // 5 of the AI-infra book, section 5.2.3 -- bank-conflict-free layouts):
-//   * CTA tile 128 x 128, K step 16, 256 threads, 8 x 8 outputs per thread held
-//     in 64 FP32 registers.
+//   * CTA tile 128 x 128, K step 8, 128 threads (4 warps), 16 x 8 outputs per
+//     thread held in 128 FP32 registers; two CTAs per SM (~230 registers per
+//     thread), so one CTA's barrier wait overlaps the other's FFMA stream.
 //   * A is stored k-major in shared memory (transposed on the way in), so one
 //     128-bit shared load gives four consecutive rows; B is stored as it lies
-//     (n contiguous).  Per k: two LDS.128 of A, two of B, 64 FFMA.
-//   * Each warp covers a 32 x 64 sub-tile as 4 x 8 lanes; a lane owns rows
-//     {4t..4t+3, 16+4t..16+4t+3} and columns {4u..4u+3, 32+4u..32+4u+3}, so the
-//     A and B fragment loads of a warp touch 64 and 128 contiguous bytes: one
+//     (n contiguous).  Per k: four LDS.128 of A, two of B, 128 FFMA.
+//   * Each warp covers a 64 x 64 sub-tile as 4 x 8 lanes; a lane owns rows
+//     {4t..4t+3} + {0, 16, 32, 48} and columns {4u..4u+3} + {0, 32}, so the A
+//     and B fragment loads of a warp touch 64 and 128 contiguous bytes: one
 //     shared-memory wavefront each, no bank conflict.
 //   * Two shared buffers; the next K tile is fetched into registers (LDG.128)
 //     while the current one is computed, then stored into the other buffer: one
-//     barrier per K tile.
+//     barrier per K tile.  The bounds predicates on these loads also keep them
+//     at the top of the iteration, ahead of the FFMA stream that hides them.
 //   * Grouped rasterisation: runs of 8 row-tiles sweep the column tiles so that
 //     concurrently resident CTAs share A rows and B columns in L2.
 //   * Ragged M, N, K: loads are predicated with zero fill, stores are predicated.
@@ -30,7 +32,7 @@
 namespace gemm_gb300 {
 namespace {
 
-constexpr int BM = 128, BN = 128, THREADS = 256;
+constexpr int BM = 128, BN = 128, THREADS = 128;
 constexpr int A_LD = BM + 4;  // padded row of the k-major A tile (floats)
 constexpr int B_LD = BN;      // row of the B tile (floats)
 constexpr int GROUP_M = 8;
@@ -69,7 +71,7 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int wm = warp >> 1, wn = warp & 1;     // 4 x 2 warps
+    const int wm = warp >> 1, wn = warp & 1;     // 2 x 2 warps
     const int lm = lane >> 3, ln = lane & 7;     // 4 x 8 lanes
 
     int tm, tn;
@@ -133,13 +135,13 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
         }
     };
 
-    float acc[8][8];
+    float acc[16][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 16; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-    const int a_off = wm * 32 + lm * 4;  // + {0, 16}
+    const int a_off = wm * 64 + lm * 4;  // + {0, 16, 32, 48}
     const int b_off = wn * 64 + ln * 4;  // + {0, 32}
     const int ktiles = (K + BK - 1) / BK;
 
@@ -152,14 +154,19 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
         if (t + 1 < ktiles) load_tile((t + 1) * BK);
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][kk][a_off]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][kk][a_off + 16]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][b_off]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][b_off + 32]);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float a[16], b[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(&As[buf][kk][a_off + 16 * q]);
+                a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(&Bs[buf][kk][b_off + 32 * q]);
+                b[4 * q] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
@@ -167,10 +174,10 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
         __syncthreads();
     }
 
-    // Epilogue: each thread writes its 8 rows x (2 x 4) columns.
+    // Epilogue: each thread writes its 16 rows x (2 x 4) columns.
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int gm = m0 + a_off + (i < 4 ? i : 12 + i);
+    for (int i = 0; i < 16; ++i) {
+        const int gm = m0 + a_off + 16 * (i >> 2) + (i & 3);
         if (gm >= M) continue;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -190,10 +197,10 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 
 // Tile configuration of the SIMT kernel: K step and CTAs per SM.
 #ifndef SIMT_BK
-#define SIMT_BK 16
+#define SIMT_BK 8
 #endif
 #ifndef SIMT_MINB
-#define SIMT_MINB 1
+#define SIMT_MINB 2
 #endif
 
 template <typename TIn, typename TOut, bool VEC>

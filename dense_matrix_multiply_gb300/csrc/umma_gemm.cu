@@ -329,10 +329,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half *) {
 __device__ __forceinline__ void store1(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void store1(__half *p, float x) { *p = __float2half_rn(x); }
 
-template <typename T, uint32_t AB_FORMAT>
-__global__ void __launch_bounds__(THREADS, 1)
+// A_CPASYNC: A's rows cannot be described by a TMA map (row stride or base not
+// 16-byte aligned).  Then four extra warps (6-9) copy the A tile with 8-byte
+// cp.async into the same 128-byte-swizzled layout TMA would write, and also
+// issue B's TMA loads; full[s] counts their 128 arrivals plus B's bytes.
+template <typename T, uint32_t AB_FORMAT, bool A_CPASYNC>
+__global__ void __launch_bounds__(A_CPASYNC ? THREADS + 128 : THREADS, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 T *__restrict__ C, int M, int N, int K, int *status)
+                 const T *__restrict__ A, T *__restrict__ C, int M, int N, int K, int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -349,7 +353,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->full[s], A_CPASYNC ? 128 : 1);
             mbar_init(&bars->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -359,7 +363,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        tma_prefetch_desc(&tmA);
+        if (!A_CPASYNC) tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
@@ -371,7 +375,59 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
 
-    if (warp == 0 && lane == 0) {
+    if (A_CPASYNC && warp >= 6) {
+        // ------------------------------------------------ producer: cp.async A + TMA B
+        const int ptid = threadIdx.x - 6 * 32;  // 0..127
+        constexpr int LAG = 2;                  // stages of copies in flight per thread
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+        auto publish = [&](long long j) {       // this thread's copies of load j have landed
+            const int sj = (int)(j % STAGES);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (ptid == 0) mbar_arrive_expect_tx(&bars->full[sj], (uint32_t)B_STAGE);
+            else mbar_arrive(&bars->full[sj]);
+        };
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, tm, tn);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, true)) { ok = false; break; }
+                if (ptid == 0) {
+                    for (int j = 0; j < 4; ++j)
+                        tma_load_2d(b_tiles + stage * B_STAGE + j * B_BOX, &tmB, &bars->full[stage],
+                                    tn * BN + j * 64, kb * BK);
+                }
+                uint8_t *a_dst = a_tiles + stage * A_STAGE;
+#pragma unroll 4
+                for (int j = 0; j < 16; ++j) {
+                    const int idx = j * 128 + ptid;
+                    const int row = idx >> 4, c8 = idx & 15;  // 8-byte piece c8 of the row's 128 bytes
+                    const int gm = tm * BM + row, gk = kb * BK + c8 * 4;
+                    const bool in = gm < M && gk < K;      // K % 4 == 0: a piece is all in or all out
+                    const T *src = in ? A + (size_t)gm * K + gk : A;
+                    const uint32_t dst = smem_u32(a_dst + row * 128 + (((c8 >> 1) ^ (row & 7)) << 4) + ((c8 & 1) << 3));
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(in ? 8 : 0)
+                                 : "memory");
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                if (issued >= LAG) {
+                    asm volatile("cp.async.wait_group 2;" ::: "memory");
+                    publish(issued - LAG);
+                }
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (ok) {
+            for (long long j = (issued > LAG ? issued - LAG : 0); j < issued; ++j) publish(j);
+        } else {
+            atomicOr(status, ST_PRODUCER);
+            *abort_flag = 1;
+        }
+    } else if (!A_CPASYNC && warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer
         int stage = 0;
         uint32_t phase = 0;
@@ -452,7 +508,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // All MMAs of this thread complete before the CTA can release TMEM.
         umma_commit(&bars->drain);
         if (!mbar_wait(&bars->drain, 0, abort_flag, false)) atomicOr(status, ST_DRAIN);
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
         const int row_in_tile = quarter * 32 + lane;
@@ -775,13 +831,17 @@ bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, uint32_t F>
+template <typename T, uint32_t F, bool A_CPASYNC>
 cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_t s) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, p.A, dt, p.M, p.K, BM, BK)) return cudaErrorInvalidValue;
     if (!make_map(&tb, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
-    auto kern = umma_gemm_kernel<T, F>;
+    if (A_CPASYNC) {
+        ta = tb;  // unused by the kernel
+    } else if (!make_map(&ta, p.A, dt, p.M, p.K, BM, BK)) {
+        return cudaErrorInvalidValue;
+    }
+    auto kern = umma_gemm_kernel<T, F, A_CPASYNC>;
     static std::atomic<uint64_t> attr_done{0};  // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -795,7 +855,8 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     const long long tiles = (long long)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    kern<<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, status);
+    kern<<<grid, A_CPASYNC ? THREADS + 128 : THREADS, SMEM_BYTES, s>>>(
+        ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K, status);
     return cudaGetLastError();
 }
 
@@ -856,16 +917,27 @@ cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, c
 
 }  // namespace
 
+namespace {
+bool aligned(const void *q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; }
+// TMA can describe A: 16-byte aligned base and row stride.
+bool a_tma_ok(const Problem &p) { return aligned(p.A, 16) && (p.K % 8) == 0; }
+// 8-byte cp.async can fetch A: 8-byte aligned base and row stride.
+bool a_cpasync_ok(const Problem &p) { return aligned(p.A, 8) && (p.K % 4) == 0; }
+}  // namespace
+
 bool umma_supported(const Problem &p) {
     if (p.elt == Elt::F32) return false;
-    auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
-    // TMA: 16-byte aligned bases and row strides; vector epilogue stores need C
-    // rows 16-byte aligned too (N*2 % 16 == 0 already).
-    return al16(p.A) && al16(p.B) && al16(p.C) && (p.K % 8) == 0 && (p.N % 8) == 0;
+    // B through TMA (16-byte aligned base and row stride); C rows 16-byte
+    // aligned for the vector epilogue stores; A through TMA or cp.async.
+    return aligned(p.B, 16) && aligned(p.C, 16) && (p.N % 8) == 0 && (a_tma_ok(p) || a_cpasync_ok(p));
 }
 
 cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s) {
     if (!umma_supported(p)) return cudaErrorInvalidValue;
+    if (!a_tma_ok(p)) {
+        return p.elt == Elt::BF16 ? launch_typed<__nv_bfloat16, 1, true>(p, num_sms, status, s)
+                                  : launch_typed<__half, 0, true>(p, num_sms, status, s);
+    }
     // 256-row tiles on CTA pairs once M fills more than one 128-row tile.
     if (p.M > BM) {
         int dev = 0;
@@ -878,8 +950,8 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
                                       : launch_pair_typed<__half, 0>(p, cmax, status, s);
         }
     }
-    if (p.elt == Elt::BF16) return launch_typed<__nv_bfloat16, 1>(p, num_sms, status, s);
-    return launch_typed<__half, 0>(p, num_sms, status, s);
+    if (p.elt == Elt::BF16) return launch_typed<__nv_bfloat16, 1, false>(p, num_sms, status, s);
+    return launch_typed<__half, 0, false>(p, num_sms, status, s);
 }
 
 // ------------------------------------------------------- allocation-free variant

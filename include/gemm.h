@@ -100,9 +100,10 @@ GEMM_API gemm_status_t gemm_bf16_rm(const uint16_t *A, const uint16_t *B, uint16
  * cudaMalloc's implicit device-wide synchronisation is not acceptable.
  *
  * Same arguments, layout, rounding and error codes as gemm_bf16_rm, but always
- * on the tensor-core kernel, so it needs 16-byte aligned A, B, C and K and N
- * multiples of 8 (otherwise GEMM_ERR_INVALID_VALUE, with a message in
- * gemm_last_error).  The kernel's scratch -- its 4-byte pipeline-timeout status
+ * on the tensor-core kernel, so it needs B and C 16-byte aligned with N a
+ * multiple of 8, and A either 16-byte aligned with K a multiple of 8 or 8-byte
+ * aligned with K a multiple of 4 (otherwise GEMM_ERR_INVALID_VALUE, with a
+ * message in gemm_last_error).  The kernel's scratch -- its 4-byte pipeline-timeout status
  * word, the same for every M, N, K -- lives in a static device array of 256
  * bytes that every GPU loading this library holds until the process exits;
  * a problem needing more scratch than that would be refused with

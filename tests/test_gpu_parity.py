@@ -103,7 +103,9 @@ MID_CASES = [
     ("bf16_rm", 300, 520, 264, None, "umma_bf16"),
     ("bf16_rm", 129, 264, 520, None, "umma_bf16"),
     ("bf16_rm", 640, 1024, 1024, None, "umma_bf16"),
-    ("bf16_rm", 130, 200, 100, None, "simt_bf16_scalar"),
+    ("bf16_rm", 130, 200, 100, None, "umma_bf16"),          # K % 8 = 4: A through cp.async
+    ("bf16_rm", 300, 264, 4100 - 3840, None, "umma_bf16"),  # K = 260
+    ("bf16_rm", 130, 200, 102, None, "simt_bf16_scalar"),   # K % 4 = 2: no tensor-core path
     ("bf16_rm", 256, 256, 256, "simt_scalar", "simt_bf16_scalar"),
     ("bf16_rm", 4, 520, 1000, None, "gemv_bf16_vec"),
     ("bf16_rm", 7, 130, 77, None, "gemv_bf16_scalar"),

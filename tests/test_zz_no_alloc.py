@@ -27,7 +27,7 @@ def _bits_to_f64(t: torch.Tensor) -> np.ndarray:
     return (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("shape", [(1024, 12288, 4096), (1000, 1000, 1000), (300, 520, 264)])
+@pytest.mark.parametrize("shape", [(1024, 12288, 4096), (1000, 1000, 1000), (300, 520, 264), (256, 512, 100)])
 def test_noalloc_matches_allocating_entry_point(lib, shape):
     M, N, K = shape
     clib = g.load()
@@ -62,9 +62,9 @@ def test_noalloc_rejects_what_the_tensor_core_kernel_cannot_run(lib):
     clib = g.load()
     buf = torch.zeros(1 << 20, dtype=torch.int16, device="cuda")
     p = buf.data_ptr()
-    # K = 100 is not a multiple of 8: no TMA descriptor for A's rows
-    st = clib.gemm_bf16_rm_noalloc(p, p + 2 * 200 * 100, p + 2 * 400 * 100, 200, 128, 100)
-    assert st == 1 and b"multiples of 8" in clib.gemm_last_error()
+    # K = 102: A's rows are only 4-byte aligned, neither TMA nor 8-byte cp.async
+    st = clib.gemm_bf16_rm_noalloc(p, p + 2 * 200 * 102, p + 2 * 400 * 102, 200, 128, 102)
+    assert st == 1 and b"aligned" in clib.gemm_last_error()
     # unaligned A
     st = clib.gemm_bf16_rm_noalloc(p + 2, p + 2 * 300 * 128, p + 2 * 600 * 128, 256, 128, 128)
     assert st == 1
