@@ -31,10 +31,13 @@ cudaError_t launch_simt(const Problem &p, bool vec4, cudaStream_t s);
 constexpr int kGemvMaxM = 8;
 cudaError_t launch_gemv(const Problem &p, bool vec, int num_sms, cudaStream_t s);
 
-// tcgen05 tensor-core kernel for 16-bit inputs.  Needs 16-byte aligned A, B, C
-// and K*2, N*2 multiples of 16 bytes (TMA strides).  num_sms: persistent grid
-// size.  status: device word the kernel ORs a timeout code into.
-cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s);
+// tcgen05 tensor-core kernel for 16-bit inputs.  Needs B and C 16-byte aligned
+// with N % 8 == 0 (TMA for B, vector stores for C), and A either TMA-describable
+// (16-byte aligned, K % 8 == 0) or 8-byte aligned with K % 4 == 0.  num_sms:
+// persistent grid size.  status: device word the kernel ORs a timeout code
+// into.  may_allocate: large problems with unaligned A rows may stage A in
+// stream-ordered scratch (cudaMallocAsync); without it they use cp.async.
+cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s, bool may_allocate = true);
 bool umma_supported(const Problem &p);
 
 // Allocation-free variant of launch_umma: the status word lives in a static

@@ -37,6 +37,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -413,6 +414,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 asm volatile("cp.async.commit_group;" ::: "memory");
                 if (issued >= LAG) {
+                    static_assert(LAG == 2, "wait_group immediate below");
                     asm volatile("cp.async.wait_group 2;" ::: "memory");
                     publish(issued - LAG);
                 }
@@ -819,11 +821,11 @@ EncodeTiledFn encode_fn() {
 // 2-D row-major matrix [rows, cols] of 16-bit elements, box [box_rows, box_cols],
 // 128-byte swizzle, zero fill out of bounds.
 bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int rows, int cols, int box_rows,
-              int box_cols) {
+              int box_cols, long long row_elems = 0) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)(row_elems > 0 ? row_elems : cols) * 2};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -891,11 +893,13 @@ int pair_clusters_max(int dev) {
     return cached[dev & 63].load();
 }
 
+// lda: row stride of A in elements (0: K).
 template <typename T, uint32_t F>
-cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, cudaStream_t s) {
+cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, cudaStream_t s,
+                              long long lda = 0) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, p.A, dt, p.M, p.K, 128, BK)) return cudaErrorInvalidValue;
+    if (!make_map(&ta, p.A, dt, p.M, p.K, 128, BK, lda)) return cudaErrorInvalidValue;
     if (!make_map(&tb, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
     const long long tiles = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * ((p.N + pairk::PBN - 1) / pairk::PBN);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
@@ -925,6 +929,20 @@ bool a_tma_ok(const Problem &p) { return aligned(p.A, 16) && (p.K % 8) == 0; }
 bool a_cpasync_ok(const Problem &p) { return aligned(p.A, 8) && (p.K % 4) == 0; }
 }  // namespace
 
+// Copies A [M, K] (rows 8-byte aligned, K % 4 == 0) into rows of lda elements
+// (16-byte aligned), so that TMA can describe it.  Elements K..lda-1 of a row
+// are left as they are: the tensor map declares K columns, so TMA never reads
+// them.
+__global__ void pad_rows_kernel(const uint2 *__restrict__ A, uint2 *__restrict__ Ap, long long rows,
+                                long long chunks_per_row, long long lda_chunks) {
+    const long long total = rows * chunks_per_row;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const long long r = i / chunks_per_row, c = i - r * chunks_per_row;
+        Ap[r * lda_chunks + c] = __ldg(A + i);
+    }
+}
+
 bool umma_supported(const Problem &p) {
     if (p.elt == Elt::F32) return false;
     // B through TMA (16-byte aligned base and row stride); C rows 16-byte
@@ -932,9 +950,39 @@ bool umma_supported(const Problem &p) {
     return aligned(p.B, 16) && aligned(p.C, 16) && (p.N % 8) == 0 && (a_tma_ok(p) || a_cpasync_ok(p));
 }
 
-cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s) {
+cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s, bool may_allocate) {
     if (!umma_supported(p)) return cudaErrorInvalidValue;
     if (!a_tma_ok(p)) {
+        // Large problems: stage A once into 16-byte-aligned rows (stream-ordered
+        // scratch from the device's default pool) and run the CTA-pair kernel;
+        // the copy costs 4*M*K bytes of traffic against 2*M*N*K FLOPs.  If that
+        // scratch is not available, or for small problems, A is fetched with
+        // cp.async by the single-CTA kernel instead.
+        if (may_allocate && p.M > BM && p.N >= 1024) {
+            int dev = 0;
+            cudaError_t e = cudaGetDevice(&dev);
+            if (e != cudaSuccess) return e;
+            const int cmax = p.elt == Elt::BF16 ? pair_clusters_max<__nv_bfloat16, 1>(dev)
+                                                : pair_clusters_max<__half, 0>(dev);
+            const long long lda = ((long long)p.K + 7) / 8 * 8;
+            void *ap = nullptr;
+            if (cmax > 0 && cudaMallocAsync(&ap, (size_t)p.M * lda * 2, s) == cudaSuccess) {
+                const long long chunks = (long long)p.M * (p.K / 4);
+                const int grid = (int)std::min<long long>((chunks + 255) / 256, (long long)num_sms * 16);
+                pad_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint2 *>(p.A), static_cast<uint2 *>(ap),
+                                                     p.M, p.K / 4, lda / 4);
+                e = cudaGetLastError();
+                if (e == cudaSuccess) {
+                    Problem q = p;
+                    q.A = ap;
+                    e = p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(q, cmax, status, s, lda)
+                                           : launch_pair_typed<__half, 0>(q, cmax, status, s, lda);
+                }
+                const cudaError_t f = cudaFreeAsync(ap, s);
+                return e != cudaSuccess ? e : f;
+            }
+            cudaGetLastError();  // fall through to cp.async
+        }
         return p.elt == Elt::BF16 ? launch_typed<__nv_bfloat16, 1, true>(p, num_sms, status, s)
                                   : launch_typed<__half, 0, true>(p, num_sms, status, s);
     }
@@ -990,7 +1038,7 @@ cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s) {
     if (umma_noalloc_scratch_need(p) > kNoallocScratchBytes) return cudaErrorInvalidValue;
     e = cudaMemsetAsync(d.ptr, 0, sizeof(int), s);  // the status word starts at zero
     if (e != cudaSuccess) return e;
-    return launch_umma(p, num_sms, d.ptr, s);
+    return launch_umma(p, num_sms, d.ptr, s, /*may_allocate=*/false);
 }
 
 }  // namespace gemm_gb300

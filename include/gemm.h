@@ -18,8 +18,14 @@
  *
  * Pointers.  A, B and C are DEVICE pointers (cudaMalloc, torch CUDA tensors,
  * or any memory the current device can address), owned by the caller.  The
- * library keeps no reference to them after the call and allocates nothing per
- * call.  Half and bf16 elements are passed as their 16-bit patterns.
+ * library keeps no reference to them after the call.  Half and bf16 elements
+ * are passed as their 16-bit patterns.  Memory the library uses besides A, B,
+ * C: one 4-byte status word per device (cudaMalloc on first use); and, only for
+ * a 16-bit problem with M > 128, N >= 1024 whose A rows are not 16-byte
+ * aligned (e.g. bf16 with K = 4100), an aligned copy of A taken from the
+ * device's default stream-ordered pool (cudaMallocAsync / cudaFreeAsync on the
+ * caller's stream); if that allocation fails the call uses a slower kernel
+ * instead.
  *
  * Leading dimensions are tight:
  *   _rm (row-major):    A is [M,K] with lda = K, B is [K,N] with ldb = N,

@@ -106,6 +106,8 @@ MID_CASES = [
     ("bf16_rm", 130, 200, 100, None, "umma_bf16"),          # K % 8 = 4: A through cp.async
     ("bf16_rm", 300, 264, 4100 - 3840, None, "umma_bf16"),  # K = 260
     ("bf16_rm", 130, 200, 102, None, "simt_bf16_scalar"),   # K % 4 = 2: no tensor-core path
+    ("bf16_rm", 520, 1032, 260, None, "umma_bf16"),         # unaligned A staged, CTA pairs
+    ("f16_cm", 1032, 520, 260, None, "umma_f16"),
     ("bf16_rm", 256, 256, 256, "simt_scalar", "simt_bf16_scalar"),
     ("bf16_rm", 4, 520, 1000, None, "gemv_bf16_vec"),
     ("bf16_rm", 7, 130, 77, None, "gemv_bf16_scalar"),

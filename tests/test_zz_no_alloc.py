@@ -27,7 +27,8 @@ def _bits_to_f64(t: torch.Tensor) -> np.ndarray:
     return (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("shape", [(1024, 12288, 4096), (1000, 1000, 1000), (300, 520, 264), (256, 512, 100)])
+@pytest.mark.parametrize("shape", [(1024, 12288, 4096), (1000, 1000, 1000), (300, 520, 264), (256, 512, 100),
+                                   (1024, 2048, 1028)])
 def test_noalloc_matches_allocating_entry_point(lib, shape):
     M, N, K = shape
     clib = g.load()
