@@ -456,7 +456,8 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
     p.add_argument("--paths", nargs="*", default=["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144",
                                                    "ffn_bf16_rm_1024x12288x4096", "edge_bf16_rm_1x12288x4096",
-                                                   "edge_f32_rm_1x12288x4096"])
+                                                   "edge_f32_rm_1x12288x4096", "edge_bf16_rm_8192x4096x4100",
+                                                   "edge_f32_rm_8192x4096x4100", "sgemm_f32_rm_256"])
     p.add_argument("--path-steps", type=int, default=50)
     p.add_argument("--no-paths", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -589,36 +589,51 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // No TMA multicast is used: each CTA fetches only its own operand halves.
 namespace pairk {
 constexpr int PBM = 256, PBN = 256;
-constexpr int PSTAGES = 6;
 constexpr int P_A_STAGE = 128 * BK * 2;                        // 16 KiB per CTA
 constexpr int P_B_STAGE = 128 * BK * 2;                        // 16 KiB per CTA (two 64-column boxes)
 constexpr uint32_t P_STAGE_TX = 2u * (P_A_STAGE + P_B_STAGE);  // bytes per stage, both CTAs
-constexpr int P_SMEM_TILES = PSTAGES * (P_A_STAGE + P_B_STAGE);
-constexpr int P_SMEM_BYTES = 1024 + P_SMEM_TILES + 256;
-constexpr int P_GROUP_M = 8;  // pair tiles per raster group
-using PBars = BarsT<PSTAGES>;
-static_assert(sizeof(PBars) <= 256, "barrier block");
+constexpr int P_STG_BOX = 32 * 64 * 2;                         // one 32-row x 64-column output box
+constexpr int P_GROUP_M = 8;                                   // pair tiles per raster group
+// Shared memory: NST operand stages, then (TMA-store epilogue) two staging
+// boxes per epilogue warp, then the barriers.
+__host__ __device__ constexpr int smem_tiles(int nst) { return nst * (P_A_STAGE + P_B_STAGE); }
+__host__ __device__ constexpr int smem_staging(bool tma_store) { return tma_store ? 4 * 2 * P_STG_BOX : 0; }
+__host__ __device__ constexpr int smem_bytes(int nst, bool tma_store) {
+    return 1024 + smem_tiles(nst) + smem_staging(tma_store) + 256;
+}
+static_assert(smem_bytes(7, false) <= 232448 && smem_bytes(6, true) <= 232448, "shared memory budget");
 }  // namespace pairk
 
-template <typename T, uint32_t AB_FORMAT>
+// bn: the tile's N extent, a multiple of 32 in [128, 256], chosen per problem
+// to fill the last wave (each CTA still loads 128 columns of B per stage and
+// the MMA reads bn/2 of them; accumulator buffers stay 256 columns apart).
+// PSTAGES: operand stages.  TMA_ST: the epilogue stages each warp's 32 x 64
+// output boxes in 128-byte-swizzled shared memory and writes them with TMA
+// stores (full-line writes) instead of per-thread 16-byte stores; bn must then
+// be a multiple of 64.
+template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool TMA_ST>
 __global__ void __launch_bounds__(THREADS, 1)
 umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 T *__restrict__ C, int M, int N, int K, int *status)
+                 const __grid_constant__ CUtensorMap tmC, T *__restrict__ C, int M, int N, int K, int *status,
+                 int bn)
 {
     using namespace pairk;
+    using PBars = BarsT<PSTAGES>;
+    static_assert(sizeof(PBars) <= 256, "barrier block");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *a_tiles = smem;
     uint8_t *b_tiles = smem + PSTAGES * P_A_STAGE;
-    PBars *bars = reinterpret_cast<PBars *>(smem + P_SMEM_TILES);
+    uint8_t *staging = smem + smem_tiles(PSTAGES);
+    PBars *bars = reinterpret_cast<PBars *>(smem + smem_tiles(PSTAGES) + smem_staging(TMA_ST));
     volatile int *abort_flag = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int cluster = (int)cluster_id_x(), nclusters = (int)cluster_count_x();
-    const int tiles_m = (M + PBM - 1) / PBM, tiles_n = (N + PBN - 1) / PBN;
+    const int tiles_m = (M + PBM - 1) / PBM, tiles_n = (N + bn - 1) / bn;
     const int num_tiles = tiles_m * tiles_n;
     const int num_kb = (K + BK - 1) / BK;
 
@@ -636,6 +651,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (TMA_ST) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
@@ -666,7 +682,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int tm, tn;
             coords(t, tm, tn);
             const int row0 = tm * PBM + (int)rank * 128;
-            const int col0 = tn * PBN + (int)rank * 128;
+            const int col0 = tn * bn + (int)rank * (bn >> 1);
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!mbar_wait_cluster(&bars->empty[stage], phase ^ 1u, abort_flag, true)) { ok = false; break; }
                 const uint32_t full_leader = map_to_rank(&bars->full[stage], 0);
@@ -702,7 +718,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer (leader)
-        constexpr uint32_t idesc = make_idesc(AB_FORMAT, PBM, PBN);
+        const uint32_t idesc = make_idesc(AB_FORMAT, PBM, (uint32_t)bn);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -741,6 +757,8 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
         const int row_in_tile = (int)rank * 128 + quarter * 32 + lane;
+        uint8_t *my_stg = staging + quarter * 2 * P_STG_BOX;  // this warp's two staging boxes
+        int sb = 0;
         int it = 0;
         bool ok = true;
         for (int t = cluster; t < num_tiles; t += nclusters, ++it) {
@@ -752,37 +770,77 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tc_fence_after();
             __syncwarp();
             const int row = tm * PBM + row_in_tile;
-            const int n0 = tn * PBN;
-            T *crow = C + (size_t)row * N;
+            const int n0 = tn * bn;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * PBN);
+            if constexpr (TMA_ST) {
+                const int box_row0 = tm * PBM + (int)rank * 128 + quarter * 32;  // warp-uniform
 #pragma unroll 1
-            for (int chunk = 0; chunk < PBN / 32; ++chunk) {
-                const int c0 = n0 + chunk * 32;
-                if (c0 >= N) break;  // warp-uniform
-                uint32_t r[32];
-                tmem_ld_32cols(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * PBN + chunk * 32), r);
-                tmem_ld_wait();
-                if (row < M) {
-                    if (c0 + 32 <= N) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(crow + c0);
+                for (int g = 0; g < (bn >> 6); ++g) {
+                    const int c0 = n0 + g * 64;
+                    if (c0 >= N) break;  // warp-uniform
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32cols(t_row + (uint32_t)(g * 64), r0);
+                    tmem_ld_32cols(t_row + (uint32_t)(g * 64 + 32), r1);
+                    tmem_ld_wait();
+                    // The store issued two boxes ago read this staging box.
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    __syncwarp();
+                    uint8_t *rowp = my_stg + sb * P_STG_BOX + lane * 128;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 v;
-                            v.x = pack2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]), (T *)nullptr);
-                            v.y = pack2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]), (T *)nullptr);
-                            v.z = pack2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]), (T *)nullptr);
-                            v.w = pack2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]), (T *)nullptr);
-                            dst[q] = v;
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t *src = c < 4 ? &r0[8 * c] : &r1[8 * (c - 4)];
+                        uint4 v;
+                        v.x = pack2(__uint_as_float(src[0]), __uint_as_float(src[1]), (T *)nullptr);
+                        v.y = pack2(__uint_as_float(src[2]), __uint_as_float(src[3]), (T *)nullptr);
+                        v.z = pack2(__uint_as_float(src[4]), __uint_as_float(src[5]), (T *)nullptr);
+                        v.w = pack2(__uint_as_float(src[6]), __uint_as_float(src[7]), (T *)nullptr);
+                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (lane & 7)) << 4)) = v;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && box_row0 < M) {
+                        asm volatile(
+                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                                reinterpret_cast<uint64_t>(&tmC)),
+                            "r"(c0), "r"(box_row0), "r"(smem_u32(my_stg + sb * P_STG_BOX))
+                            : "memory");
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                    sb ^= 1;
+                }
+            } else {
+                T *crow = C + (size_t)row * N;
+#pragma unroll 1
+                for (int chunk = 0; chunk < (bn >> 5); ++chunk) {
+                    const int c0 = n0 + chunk * 32;
+                    if (c0 >= N) break;  // warp-uniform
+                    uint32_t r[32];
+                    tmem_ld_32cols(t_row + (uint32_t)(chunk * 32), r);
+                    tmem_ld_wait();
+                    if (row < M) {
+                        if (c0 + 32 <= N) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(crow + c0);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint4 v;
+                                v.x = pack2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]), (T *)nullptr);
+                                v.y = pack2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]), (T *)nullptr);
+                                v.z = pack2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]), (T *)nullptr);
+                                v.w = pack2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]), (T *)nullptr);
+                                dst[q] = v;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (c0 + j < N) store1(crow + c0 + j, __uint_as_float(r[j]));
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (c0 + j < N) store1(crow + c0 + j, __uint_as_float(r[j]));
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive_cluster(map_to_rank(&bars->acc_empty[buf], 0));
         }
+        if (TMA_ST && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         if (!ok) {
             atomicOr(status, ST_EPILOGUE);
             *abort_flag = 1;
@@ -862,6 +920,14 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     return cudaGetLastError();
 }
 
+// Pair-kernel configuration: 128-byte TMA-store epilogue with six operand
+// stages (the staging boxes take the seventh stage's shared memory).
+#ifndef PAIR_TMA_STORE
+#define PAIR_TMA_STORE 1
+#endif
+constexpr bool kPairTmaStore = PAIR_TMA_STORE != 0;
+constexpr int kPairStages = kPairTmaStore ? 6 : 7;
+
 // Largest number of co-resident two-CTA clusters of the pair kernel, per device
 // (0: the pair kernel cannot be launched).
 template <typename T, uint32_t F>
@@ -869,15 +935,15 @@ int pair_clusters_max(int dev) {
     static std::atomic<int> cached[64];
     static std::once_flag once[64];
     std::call_once(once[dev & 63], [&] {
-        auto kern = umma_pair_kernel<T, F>;
+        auto kern = umma_pair_kernel<T, F, kPairStages, kPairTmaStore>;
+        const int smem = pairk::smem_bytes(kPairStages, kPairTmaStore);
         int n = 0;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pairk::P_SMEM_BYTES) ==
-                cudaSuccess &&
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2, 1, 1);
             cfg.blockDim = dim3(THREADS, 1, 1);
-            cfg.dynamicSmemBytes = pairk::P_SMEM_BYTES;
+            cfg.dynamicSmemBytes = smem;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
             attr[0].val.clusterDim.x = 2;
@@ -898,16 +964,35 @@ template <typename T, uint32_t F>
 cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, cudaStream_t s,
                               long long lda = 0) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     if (!make_map(&ta, p.A, dt, p.M, p.K, 128, BK, lda)) return cudaErrorInvalidValue;
     if (!make_map(&tb, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
-    const long long tiles = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * ((p.N + pairk::PBN - 1) / pairk::PBN);
+    if (kPairTmaStore) {
+        if (!make_map(&tc, p.C, dt, p.M, p.N, 32, 64)) return cudaErrorInvalidValue;
+    } else {
+        tc = tb;  // unused by the kernel
+    }
+    // N extent of a tile: the one of 256, 192, 128 (TMA-store boxes are 64
+    // columns wide) with the fewest waves of tiles over the clusters, widest on
+    // ties: per-tile time is set mostly by the operand feed, which does not
+    // shrink with the tile's N.
+    const long long tiles_m = (p.M + pairk::PBM - 1) / pairk::PBM;
+    int bn = 256;
+    long long best = -1;
+    const int step = kPairTmaStore ? 64 : 32;
+    for (int cand = 256; cand >= 128; cand -= step) {
+        const long long t = tiles_m * ((p.N + cand - 1) / cand);
+        const long long waves = (t + clusters_max - 1) / clusters_max;
+        const long long cost = waves * (cand > 224 ? cand : 224);
+        if (best < 0 || cost < best) { best = cost; bn = cand; }
+    }
+    const long long tiles = tiles_m * ((p.N + bn - 1) / bn);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pairk::P_SMEM_BYTES;
+    cfg.dynamicSmemBytes = pairk::smem_bytes(kPairStages, kPairTmaStore);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -916,7 +1001,8 @@ cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, c
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F>, ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, status);
+    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, kPairStages, kPairTmaStore>, ta, tb, tc,
+                              static_cast<T *>(p.C), p.M, p.N, p.K, status, bn);
 }
 
 }  // namespace
