@@ -142,9 +142,9 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     switch (t_force) {
     case Family::Simt:
         if (elt == Elt::F32 && !simt_vec_ok) return GEMM_ERR_INVALID_VALUE;
-        return finish(launch_simt(p, elt == Elt::F32, s), kernel_name("simt", elt));
+        return finish(launch_simt(p, elt == Elt::F32, dev->num_sms, s), kernel_name("simt", elt));
     case Family::SimtScalar:
-        return finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
+        return finish(launch_simt(p, false, dev->num_sms, s), kernel_name("simt_scalar", elt));
     case Family::Gemv:
         if (M > kGemvMaxM || !gemv_vec_ok) return GEMM_ERR_INVALID_VALUE;
         return finish(launch_gemv(p, true, dev->num_sms, s), kernel_name("gemv", elt));
@@ -162,10 +162,10 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
         return gemv_vec_ok ? finish(launch_gemv(p, true, dev->num_sms, s), kernel_name("gemv", elt))
                            : finish(launch_gemv(p, false, dev->num_sms, s), kernel_name("gemv_scalar", elt));
     if (elt == Elt::F32)
-        return simt_vec_ok ? finish(launch_simt(p, true, s), kernel_name("simt", elt))
-                           : finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
+        return simt_vec_ok ? finish(launch_simt(p, true, dev->num_sms, s), kernel_name("simt", elt))
+                           : finish(launch_simt(p, false, dev->num_sms, s), kernel_name("simt_scalar", elt));
     if (umma_supported(p)) return finish(launch_umma(p, dev->num_sms, dev->status, s), kernel_name("umma", elt));
-    return finish(launch_simt(p, false, s), kernel_name("simt_scalar", elt));
+    return finish(launch_simt(p, false, dev->num_sms, s), kernel_name("simt_scalar", elt));
 }
 
 // Capability and SM count of the current device, without allocating anything

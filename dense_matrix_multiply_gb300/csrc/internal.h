@@ -21,8 +21,9 @@ struct Problem {
 
 // FP32 (or 16-bit fallback) SIMT kernel on the CUDA cores.  vec4: float4
 // global loads/stores (needs K % 4 == 0, N % 4 == 0 and 16-byte aligned bases;
-// f32 only).  Returns the launch status.
-cudaError_t launch_simt(const Problem &p, bool vec4, cudaStream_t s);
+// f32 only).  num_sms sizes the split of a partly filled last wave.  Returns
+// the launch status.
+cudaError_t launch_simt(const Problem &p, bool vec4, int num_sms, cudaStream_t s);
 
 // Skinny-M kernel (M <= kGemvMaxM): streams B once, FP32 accumulation, K split
 // over a thread-block cluster, fixed-order reduction in shared and distributed

@@ -60,12 +60,17 @@ __device__ __forceinline__ void raster(int pid, int tiles_m, int tiles_n, int &t
 }
 
 // BK: K step of a shared tile (8 or 16).  MINB: CTAs per SM the register
-// budget is sized for (__launch_bounds__).
-template <typename TIn, typename TOut, bool VEC, int BK, int MINB>
+// budget is sized for (__launch_bounds__).  MT: rows of C per CTA, 128 (a whole
+// 128 x 128 tile) or 64 (half a tile: CTA 2j+h computes rows 64h..64h+63 of
+// tile tile_begin + j, each thread 8 x 8 outputs).  Half tiles spread a
+// problem too small to fill the GPU over twice as many CTAs.
+template <typename TIn, typename TOut, bool VEC, int BK, int MINB, int MT>
 __global__ void __launch_bounds__(THREADS, MINB)
 simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__restrict__ C,
-                 int M, int N, int K)
+                 int M, int N, int K, int tile_begin)
 {
+    static_assert(MT == 128 || MT == 64, "CTA covers a whole or half tile");
+    constexpr int RG = MT / 32;  // groups of four rows per thread
     __shared__ __align__(16) float As[2][BK][A_LD];
     __shared__ __align__(16) float Bs[2][BK][B_LD];
 
@@ -75,14 +80,15 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
     const int lm = lane >> 3, ln = lane & 7;     // 4 x 8 lanes
 
     int tm, tn;
-    raster(blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
+    const int pid = tile_begin + (MT == BM ? (int)blockIdx.x : (int)(blockIdx.x >> 1));
+    raster(pid, (M + BM - 1) / BM, (N + BN - 1) / BN, tm, tn);
+    const int m0 = tm * BM + (MT == BM ? 0 : (int)(blockIdx.x & 1) * MT), n0 = tn * BN;
 
     // Global -> register staging.  A: 128 rows x QA quads of k; B: BK k-rows x
     // 32 quads of n; each thread moves LA quads of A and LB quads of B.
     constexpr int QA = BK / 4;
-    constexpr int LA = BM * QA / THREADS, LB = BK * (BN / 4) / THREADS;
-    static_assert(LA >= 1 && LB >= 1 && BM * QA % THREADS == 0, "tile/thread mapping");
+    constexpr int LA = MT * QA / THREADS, LB = BK * (BN / 4) / THREADS;
+    static_assert(LA >= 1 && LB >= 1 && MT * QA % THREADS == 0, "tile/thread mapping");
     float ra[LA][4], rb[LB][4];
     auto load_tile = [&](int k0) {
 #pragma unroll
@@ -135,13 +141,13 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
         }
     };
 
-    float acc[16][8];
+    float acc[4 * RG][8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < 4 * RG; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-    const int a_off = wm * 64 + lm * 4;  // + {0, 16, 32, 48}
+    const int a_off = wm * (MT / 2) + lm * 4;  // + 16 * {0 .. RG-1}
     const int b_off = wn * 64 + ln * 4;  // + {0, 32}
     const int ktiles = (K + BK - 1) / BK;
 
@@ -154,9 +160,9 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
         if (t + 1 < ktiles) load_tile((t + 1) * BK);
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
-            float a[16], b[8];
+            float a[4 * RG], b[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < RG; ++q) {
                 const float4 v = *reinterpret_cast<const float4 *>(&As[buf][kk][a_off + 16 * q]);
                 a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
             }
@@ -166,7 +172,7 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
                 b[4 * q] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 4 * RG; ++i)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
@@ -174,9 +180,9 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
         __syncthreads();
     }
 
-    // Epilogue: each thread writes its 16 rows x (2 x 4) columns.
+    // Epilogue: each thread writes its 4*RG rows x (2 x 4) columns.
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 4 * RG; ++i) {
         const int gm = m0 + a_off + 16 * (i >> 2) + (i & 3);
         if (gm >= M) continue;
 #pragma unroll
@@ -204,25 +210,46 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 #endif
 
 template <typename TIn, typename TOut, bool VEC>
-cudaError_t launch_typed(const Problem &p, cudaStream_t s) {
+cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     const long long tiles = (long long)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
-    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB><<<(unsigned)tiles, THREADS, 0, s>>>(
-        static_cast<const TIn *>(p.A), static_cast<const TIn *>(p.B), static_cast<TOut *>(p.C),
-        p.M, p.N, p.K);
-    return cudaGetLastError();
+    if (2 * tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const TIn *A = static_cast<const TIn *>(p.A);
+    const TIn *B = static_cast<const TIn *>(p.B);
+    TOut *C = static_cast<TOut *>(p.C);
+    // A problem too small to fill half of one round of resident CTAs runs as
+    // half tiles: twice the CTAs, half the rows each.  (Splitting only the last
+    // round of a large problem into a second launch measured slower: a lone
+    // CTA already runs near the SM's full rate, and the second launch waits
+    // for the first to drain.)
+    const long long slots = (long long)num_sms * SIMT_MINB;
+    const long long split = 2 * tiles <= slots ? tiles : 0;
+    const long long whole = tiles - split;
+    if (whole > 0) {
+        simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 128><<<(unsigned)whole, THREADS, 0, s>>>(
+            A, B, C, p.M, p.N, p.K, 0);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (split > 0) {
+        simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 64><<<(unsigned)(2 * split), THREADS, 0, s>>>(
+            A, B, C, p.M, p.N, p.K, (int)whole);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_simt(const Problem &p, bool vec4, cudaStream_t s) {
+cudaError_t launch_simt(const Problem &p, bool vec4, int num_sms, cudaStream_t s) {
     switch (p.elt) {
     case Elt::F32:
-        return vec4 ? launch_typed<float, float, true>(p, s) : launch_typed<float, float, false>(p, s);
+        return vec4 ? launch_typed<float, float, true>(p, num_sms, s)
+                    : launch_typed<float, float, false>(p, num_sms, s);
     case Elt::F16:
-        return launch_typed<__half, __half, false>(p, s);
+        return launch_typed<__half, __half, false>(p, num_sms, s);
     case Elt::BF16:
-        return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(p, s);
+        return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(p, num_sms, s);
     }
     return cudaErrorInvalidValue;
 }
