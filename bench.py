@@ -177,7 +177,7 @@ def kernel_kind(name: str) -> str:
 
 
 def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, peaks: dict, peaks_src: str,
-                 sm_mhz: float | None, sms: int, workload: str):
+                 sm_mhz: float | None, sms: int, workload: str, prop_mhz: float | None = None):
     es = 4 if variant.startswith("f32") else 2
     flops = metrics.gemm_flops(M, N, K)
     algo_bytes = metrics.min_bytes(M, N, K, es)
@@ -203,7 +203,14 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
     out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
            "traffic": traffic, "algorithmic_flops": flops, "algorithmic_bytes": algo_bytes,
            "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {max_mhz:.0f} MHz (max SM clock)"}
+    if prop_mhz:
+        # the pages' main convention: the clock the device reports (cudaDevAttrClockRate)
+        p1 = metrics.simt_fp32_peak(sms, prop_mhz * 1e6, FP32_LANES_PER_SM) / 1e12
+        out["peak_at_device_prop_clock"] = p1
+        out["frac_at_device_prop_clock"] = achieved / p1
+        out["device_prop_clock_mhz"] = prop_mhz
     if sm_mhz:
+        # numerator and denominator at the clock sampled during the timed region
         p2 = metrics.simt_fp32_peak(sms, sm_mhz * 1e6, FP32_LANES_PER_SM) / 1e12
         out["peak_at_measured_clock"] = p2
         out["frac_at_measured_clock"] = achieved / p2
@@ -249,7 +256,7 @@ def cpu_sample(variant, A, B, M, N, K, budget_s: float):
 
 # ------------------------------------------------------------------ our arm
 def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler_uuid=None, e2e=True,
-                     cpu_budget=0.0, clocks=True):
+                     cpu_budget=0.0, clocks=True, prop_mhz=None):
     import torch
     import dense_matrix_multiply_gb300 as g
 
@@ -291,7 +298,7 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         "workload": name, "variant": variant, "M": M, "N": N, "K": K, "kernel": kernel,
         "ms_per_step": ms / steps, "tflops": flops / s_per / 1e12, "steps": steps, "ms_total": ms,
         "roofline": roofline_for(kind, variant, M, N, K, s_per, peaks, peaks_src,
-                                 clk["sm_mhz"] if clk else None, sms, name),
+                                 clk["sm_mhz"] if clk else None, sms, name, prop_mhz),
         "clocks": clk, "footprint_bytes": int(dA.numel() * dA.element_size() + dB.numel() * dB.element_size()
                                               + dC.numel() * dC.element_size()),
     }
@@ -340,7 +347,9 @@ def run_ours(args):
         g.ensure_built()
     g.load()
     peaks, peaks_src = read_peaks()
-    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+    prop_mhz = getattr(props, "clock_rate", 0) / 1000.0 or None  # kHz -> MHz
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -353,7 +362,7 @@ def run_ours(args):
                            sampler_uuid=uuid, e2e=not args.no_e2e,
                            cpu_budget=(args.cpu_seconds if (rank == 0 and world == 1
                                                             and not args.no_cpu_baseline) else 0.0),
-                           clocks=(rank == 0))
+                           clocks=(rank == 0), prop_mhz=prop_mhz)
     ms_total = res["ms_total"]
     if world > 1:
         t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
@@ -366,7 +375,7 @@ def run_ours(args):
             if wl == args.workload:
                 continue
             r = measure_workload(wl, max(5, args.path_steps), 3, peaks, peaks_src, sms, stream,
-                                 sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True)
+                                 sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True, prop_mhz=prop_mhz)
             paths.append({k: r[k] for k in ("workload", "kernel", "M", "N", "K", "ms_per_step", "tflops",
                                             "roofline", "clocks")})
 
