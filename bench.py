@@ -56,7 +56,12 @@ L2_BYTES = 129e6
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture, keyed by workload; valid only while the kernel's source is the one
 # captured (sha256 prefix of the .cu file), else reported as null.
-TRAFFIC = {}
+TRAFFIC = {
+    "sgemm_f32_rm_4096": {"bytes": 337679616 + 50706688, "source": "b22fd08de2f1"},
+    "hgemm_f16_cm_8192": {"bytes": 1050453000 + 126245632, "source": "bcb7c3e88c63"},
+    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110205952 + 12045568, "source": "bcb7c3e88c63"},
+    "edge_bf16_rm_1x12288x4096": {"bytes": 100692992 + 3278080, "source": "6b92562cc100"},
+}
 
 KERNEL_SOURCE = {
     "simt": "simt_gemm.cu",
