@@ -77,6 +77,9 @@ def all_workloads():
     for (M, N, K) in synthetic.EDGE_SHAPES:
         for v in ("f32_rm", "bf16_rm"):
             out[f"edge_{v}_{M}x{N}x{K}"] = (synthetic.EDGE_CONFIG_ID, (v, M, N, K, "uniform", 1.0, "uniform", 1.0))
+    # the FFN gate/up projection with its SiLU * U epilogue fused (two GEMMs)
+    out["ffn_gate_up_bf16_silu_mul_1024x12288x4096"] = (3, ("bf16_silu_mul", 1024, 12288, 4096, "normal", 1.0,
+                                                             "normal", 1.0 / 64.0))
     return out
 
 
@@ -184,8 +187,12 @@ def kernel_kind(name: str) -> str:
 def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, peaks: dict, peaks_src: str,
                  sm_mhz: float | None, sms: int, workload: str, prop_mhz: float | None = None):
     es = 4 if variant.startswith("f32") else 2
-    flops = metrics.gemm_flops(M, N, K)
-    algo_bytes = metrics.min_bytes(M, N, K, es)
+    if variant == "bf16_silu_mul":  # two products, X read once: X, W_g, W_u, Z
+        flops = 2 * metrics.gemm_flops(M, N, K)
+        algo_bytes = es * (M * K + 2 * K * N + M * N)
+    else:
+        flops = metrics.gemm_flops(M, N, K)
+        algo_bytes = metrics.min_bytes(M, N, K, es)
     tr = TRAFFIC.get(workload)
     traffic = None
     if tr and tr.get("source") == source_hash(kind if kind in KERNEL_SOURCE else "simt"):
@@ -239,7 +246,17 @@ def time_device(fn, steps: int, warmup: int, stream):
     return start.elapsed_time(end)
 
 
-def cpu_sample(variant, A, B, M, N, K, budget_s: float):
+def oracle_rows(variant, A, B, M, N, K, rows, extra=()):
+    """The oracle on output rows `rows`; returns the FLOPs that took."""
+    import oracle
+    if variant == "bf16_silu_mul":
+        oracle.silu_mul(A, B, extra[0], M, N, K, rows=rows)
+        return 4.0 * len(rows) * N * K
+    oracle.gemm_rows(variant, A, B, M, N, K, rows)
+    return 2.0 * len(rows) * N * K
+
+
+def cpu_sample(variant, A, B, M, N, K, budget_s: float, extra=()):
     """Times the oracle on a bounded sample of output rows of the same problem.
     Returns (flop/s, rows, seconds, threads)."""
     import oracle
@@ -247,16 +264,16 @@ def cpu_sample(variant, A, B, M, N, K, budget_s: float):
     # calibrate on one row per thread
     rows = np.arange(min(threads, M), dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.gemm_rows(variant, A, B, M, N, K, rows)
+    oracle_rows(variant, A, B, M, N, K, rows, extra)
     dt = time.perf_counter() - t0
     per_round = max(dt, 1e-6)
     rounds = max(1, int(budget_s / per_round))
     nrows = int(min(M, rows.size * rounds))
     sel = np.arange(nrows, dtype=np.int64) % M
     t0 = time.perf_counter()
-    oracle.gemm_rows(variant, A, B, M, N, K, sel)
+    fl = oracle_rows(variant, A, B, M, N, K, sel, extra)
     dt = time.perf_counter() - t0
-    return 2.0 * nrows * N * K / dt, nrows, dt, threads
+    return fl / dt, nrows, dt, threads
 
 
 # ------------------------------------------------------------------ our arm
@@ -266,16 +283,33 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     import dense_matrix_multiply_gb300 as g
 
     cfg, (variant, M, N, K, da, sa, db, sb) = all_workloads()[name]
-    A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
-    dA, dB, dC = device_inputs(variant, A, B, M, N)
-    entry = getattr(g.load(), ENTRY[variant])
     g.gemm_set_stream(stream)
-    pa, pb, pc = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
+    extra = []
+    if variant == "bf16_silu_mul":
+        A = synthetic.matrix("bf16", M, K, synthetic.seed_for(cfg, 1), da, sa)
+        B = synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 2), db, sb)
+        Wu = synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 3), db, sb)
+        dA, dB, dC = device_inputs("bf16_rm", A, B, M, N)
+        dWu = torch.from_numpy(Wu.view(np.int16)).cuda()
+        extra = [Wu]
+        fn = g.load().gemm_bf16_rm_silu_mul
+        pa, pb, pu, pc = dA.data_ptr(), dB.data_ptr(), dWu.data_ptr(), dC.data_ptr()
+
+        def call():
+            return fn(pa, pb, pu, pc, M, N, K)
+    else:
+        A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
+        dA, dB, dC = device_inputs(variant, A, B, M, N)
+        fn = getattr(g.load(), ENTRY[variant])
+        pa, pb, pc = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
+
+        def call():
+            return fn(pa, pb, pc, M, N, K)
 
     def step():
-        st = entry(pa, pb, pc, M, N, K)
+        st = call()
         if st != 0:
-            raise RuntimeError(f"{ENTRY[variant]} failed: {g.gemm_status_string(st)} {g.gemm_last_error()}")
+            raise RuntimeError(f"{name} failed: {g.gemm_status_string(st)} {g.gemm_last_error()}")
 
     step()
     g.gemm_synchronize()
@@ -297,10 +331,10 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         sampler.stop()
         clk = sampler.summary(t_host0, t_host1)
 
-    flops = metrics.gemm_flops(M, N, K)
+    flops = metrics.gemm_flops(M, N, K) * (2 if variant == "bf16_silu_mul" else 1)
     s_per = ms / 1e3 / steps
     res = {
-        "workload": name, "variant": variant, "M": M, "N": N, "K": K, "kernel": kernel,
+        "workload": name, "variant": variant, "M": M, "N": N, "K": K, "kernel": kernel, "flops_per_step": flops,
         "ms_per_step": ms / steps, "tflops": flops / s_per / 1e12, "steps": steps, "ms_total": ms,
         "roofline": roofline_for(kind, variant, M, N, K, s_per, peaks, peaks_src,
                                  clk["sm_mhz"] if clk else None, sms, name, prop_mhz),
@@ -312,23 +346,28 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         hA = torch.from_numpy(A.view(np.int16) if A.dtype != np.float32 else A).pin_memory()
         hB = torch.from_numpy(B.view(np.int16) if B.dtype != np.float32 else B).pin_memory()
         hC = torch.empty_like(dC, device="cpu").pin_memory()
+        hX = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in extra]
+        dX = [dWu] if extra else []
 
         def e2e_step():
             with torch.cuda.stream(stream):
                 dA.copy_(hA, non_blocking=True)
                 dB.copy_(hB, non_blocking=True)
+                for h, d in zip(hX, dX):
+                    d.copy_(h, non_blocking=True)
                 step()
                 hC.copy_(dC, non_blocking=True)
 
         n_e2e = max(3, min(steps, 20))
         ms_e2e = time_device(e2e_step, n_e2e, 2, stream)
         res["e2e"] = {"value": flops * n_e2e / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
-                      "h2d_bytes_per_step": int(hA.numel() * hA.element_size() + hB.numel() * hB.element_size()),
+                      "h2d_bytes_per_step": int(hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+                                                + sum(h.numel() * h.element_size() for h in hX)),
                       "d2h_bytes_per_step": int(hC.numel() * hC.element_size()),
                       "ms_per_step": ms_e2e / n_e2e, "steps": n_e2e}
 
     if cpu_budget > 0:
-        fps, nrows, dt, threads = cpu_sample(variant, A, B, M, N, K, cpu_budget)
+        fps, nrows, dt, threads = cpu_sample(variant, A, B, M, N, K, cpu_budget, extra)
         res["cpu_baseline"] = {"value": fps / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                "sample": f"{nrows} of {M} output rows ({nrows}x{N}x{K} FMAs, FP64 oracle) "
                                          f"in {dt:.1f} s"}
@@ -386,7 +425,7 @@ def run_ours(args):
 
     if rank == 0:
         M, N, K = res["M"], res["N"], res["K"]
-        flops_all = metrics.gemm_flops(M, N, K) * args.steps * world
+        flops_all = res["flops_per_step"] * args.steps * world
         value = flops_all / (ms_total / 1e3) / 1e12
         clk = res["clocks"] or {}
         line = {
@@ -428,23 +467,29 @@ def run_reference(args):
         return
     import oracle
     cfg, (variant, M, N, K, da, sa, db, sb) = all_workloads()[args.workload]
-    A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
+    extra = ()
+    if variant == "bf16_silu_mul":
+        A = synthetic.matrix("bf16", M, K, synthetic.seed_for(cfg, 1), da, sa)
+        B = synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 2), db, sb)
+        extra = (synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 3), db, sb),)
+    else:
+        A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
     threads = oracle.num_threads()
     # size each step so that warmup + steps take about args.ref_seconds in total
     rows = np.arange(min(threads, M), dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.gemm_rows(variant, A, B, M, N, K, rows)
+    oracle_rows(variant, A, B, M, N, K, rows, extra)
     per_round = max(time.perf_counter() - t0, 1e-6)
     per_step = args.ref_seconds / max(1, args.steps + args.warmup)
     nrows = int(min(M, max(1, round(per_step / per_round)) * rows.size))
     sel = np.arange(nrows, dtype=np.int64) % M
     for _ in range(args.warmup):
-        oracle.gemm_rows(variant, A, B, M, N, K, sel)
+        oracle_rows(variant, A, B, M, N, K, sel, extra)
     t0 = time.perf_counter()
+    flops = 0.0
     for _ in range(args.steps):
-        oracle.gemm_rows(variant, A, B, M, N, K, sel)
+        flops += oracle_rows(variant, A, B, M, N, K, sel, extra)
     dt = time.perf_counter() - t0
-    flops = 2.0 * nrows * N * K * args.steps
     value = flops / dt / 1e12
     sample = f"{nrows} of {M} output rows per step ({nrows}x{N}x{K} FMAs, FP64 oracle)"
     line = {
@@ -471,7 +516,8 @@ def main(argv=None):
     p.add_argument("--paths", nargs="*", default=["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144",
                                                    "ffn_bf16_rm_1024x12288x4096", "edge_bf16_rm_1x12288x4096",
                                                    "edge_f32_rm_1x12288x4096", "edge_bf16_rm_8192x4096x4100",
-                                                   "edge_f32_rm_8192x4096x4100", "sgemm_f32_rm_256"])
+                                                   "edge_f32_rm_8192x4096x4100", "sgemm_f32_rm_256",
+                                                   "ffn_gate_up_bf16_silu_mul_1024x12288x4096"])
     p.add_argument("--path-steps", type=int, default=50)
     p.add_argument("--no-paths", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

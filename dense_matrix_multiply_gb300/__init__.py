@@ -36,6 +36,7 @@ SIGNATURES = {
     "gemm_f16_cm": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_bf16_rm": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_bf16_rm_noalloc": ([_VP, _VP, _VP, _I, _I, _I], _I),
+    "gemm_bf16_rm_silu_mul": ([_VP, _VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_set_stream": ([_VP], _I),
     "gemm_get_stream": ([], _VP),
     "gemm_synchronize": ([], _I),
@@ -127,6 +128,15 @@ def gemm_bf16_rm_noalloc(A, B, C, M: int, N: int, K: int) -> None:
     """As gemm_bf16_rm, on the tensor-core kernel with its scratch in a static
     device array: the call allocates no device memory."""
     _call("gemm_bf16_rm_noalloc", A, B, C, M, N, K)
+
+
+def gemm_bf16_rm_silu_mul(X, W_g, W_u, Z, M: int, N: int, K: int) -> None:
+    """Z[M,N] = SiLU(X W_g) * (X W_u), bf16 row-major, the FFN gate/up projection."""
+    lib = load()
+    _bind_torch_stream(X, W_g, W_u, Z)
+    st = lib.gemm_bf16_rm_silu_mul(_addr(X), _addr(W_g), _addr(W_u), _addr(Z), int(M), int(N), int(K))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_bf16_rm_silu_mul", lib.gemm_last_error().decode())
 
 
 def gemm_set_stream(stream) -> None:

@@ -260,6 +260,37 @@ GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B
     return finish(launch_umma_noalloc(p, dev->num_sms, s), "umma_bf16_noalloc");
 }
 
+GEMM_API gemm_status_t gemm_bf16_rm_silu_mul(const uint16_t *X, const uint16_t *Wg, const uint16_t *Wu, uint16_t *Z,
+                                             int M, int N, int K) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) { t_last_kernel = "noop"; return GEMM_OK; }
+    if (!Z || (K > 0 && (!X || !Wg || !Wu))) return GEMM_ERR_INVALID_VALUE;
+    const size_t z_bytes = (size_t)M * N * 2, w_bytes = (size_t)K * N * 2;
+    if (overlaps(Z, z_bytes, X, (size_t)M * K * 2) || overlaps(Z, z_bytes, Wg, w_bytes) ||
+        overlaps(Z, z_bytes, Wu, w_bytes))
+        return GEMM_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    gemm_status_t st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = t_stream;
+    if (K == 0) {  // G = U = 0, SiLU(0) * 0 = 0
+        const unsigned grid = (unsigned)(dev->num_sms * 4);
+        if (aligned16(Z)) {
+            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)Z, z_bytes / 16, (uint8_t *)Z + (z_bytes & ~(size_t)15),
+                                                  z_bytes & 15);
+        } else {
+            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)Z, z_bytes);
+        }
+        return finish(cudaGetLastError(), "zero_fill");
+    }
+    Problem p{X, Wg, Z, M, N, K, Elt::BF16};
+    if (!umma_silu_mul_supported(p, Wu)) {
+        record_message("gemm_bf16_rm_silu_mul: needs X, W_g, W_u, Z 16-byte aligned and K, N multiples of 8");
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    return finish(launch_umma_silu_mul(p, Wu, dev->status, s), "umma_bf16_silu_mul");
+}
+
 GEMM_API gemm_status_t gemm_set_stream(void *cuda_stream) {
     t_stream = static_cast<cudaStream_t>(cuda_stream);
     return GEMM_OK;

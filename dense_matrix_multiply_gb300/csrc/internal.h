@@ -41,6 +41,12 @@ cudaError_t launch_gemv(const Problem &p, bool vec, int num_sms, cudaStream_t s)
 cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s, bool may_allocate = true);
 bool umma_supported(const Problem &p);
 
+// Fused FFN gate/up projection Z = SiLU(X W_g) * (X W_u) on the tensor-core
+// CTA pairs: p.A = X [M,K], p.B = W_g [K,N], p.C = Z [M,N], w_u = W_u [K,N],
+// all bf16 row-major, 16-byte aligned, K % 8 == 0, N % 8 == 0.
+bool umma_silu_mul_supported(const Problem &p, const void *w_u);
+cudaError_t launch_umma_silu_mul(const Problem &p, const void *w_u, int *status, cudaStream_t s);
+
 // Allocation-free variant of launch_umma: the status word lives in a static
 // device array of kNoallocScratchBytes bytes (see umma_gemm.cu).
 constexpr size_t kNoallocScratchBytes = 256;

@@ -330,6 +330,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half *) {
 __device__ __forceinline__ void store1(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void store1(__half *p, float x) { *p = __float2half_rn(x); }
 
+// One element of Z = SiLU(G) * U with the unfused chain's rounding points: G and
+// U rounded to the storage type, T = round(SiLU(G)) with SiLU(g) = g / (1 + e^-g)
+// evaluated in FP32 with the fast exponential and division intrinsics (their
+// error, ~1e-6 relative, is far below the 2^-9 of T's rounding), then T * U
+// (exact in FP32 for 16-bit factors), returned in FP32 for the final rounding.
+// For g -> -inf the denominator overflows to +inf and T -> 0, SiLU's limit.
+__device__ __forceinline__ float silu_f32(float gb) { return __fdividef(gb, 1.0f + __expf(-gb)); }
+__device__ __forceinline__ float silu_mul(float g, float u, __nv_bfloat16 *) {
+    const float gb = __bfloat162float(__float2bfloat16_rn(g));
+    const float ub = __bfloat162float(__float2bfloat16_rn(u));
+    const float t = __bfloat162float(__float2bfloat16_rn(silu_f32(gb)));
+    return t * ub;
+}
+__device__ __forceinline__ float silu_mul(float g, float u, __half *) {
+    const float gb = __half2float(__float2half_rn(g));
+    const float ub = __half2float(__float2half_rn(u));
+    const float t = __half2float(__float2half_rn(silu_f32(gb)));
+    return t * ub;
+}
+
 // A_CPASYNC: A's rows cannot be described by a TMA map (row stride or base not
 // 16-byte aligned).  Then four extra warps (6-9) copy the A tile with 8-byte
 // cp.async into the same 128-byte-swizzled layout TMA would write, and also
@@ -611,12 +631,22 @@ static_assert(smem_bytes(7, false) <= 232448 && smem_bytes(6, true) <= 232448, "
 // output boxes in 128-byte-swizzled shared memory and writes them with TMA
 // stores (full-line writes) instead of per-thread 16-byte stores; bn must then
 // be a multiple of 64.
-template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool TMA_ST>
+// DUAL (the FFN gate/up projection, "Chapter 5 Operators and Runtime",
+// section 5.3.1): two weight matrices, tmB = W_g and tmB2 = W_u.  A tile is
+// 256 x 128 of Z.  Per K step CTA r loads columns [64r, 64r + 64) of the tile
+// from W_g into its first B box and the same columns of W_u into its second,
+// so ONE N = 256 MMA (each CTA supplying 128 B columns) yields G and U side by
+// side: accumulator columns 128r + [0, 64) hold G and 128r + [64, 128) hold U
+// for Z columns 64r + [0, 64).  The epilogue keeps the unfused chain's
+// rounding points: G and U rounded to the output type, T = round(SiLU(G)),
+// Z = round(T * U).  G, U and T never leave the SM.
+template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool TMA_ST, bool DUAL = false>
 __global__ void __launch_bounds__(THREADS, 1)
 umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmC, T *__restrict__ C, int M, int N, int K, int *status,
-                 int bn)
+                 int bn, const __grid_constant__ CUtensorMap tmB2)
 {
+    static_assert(!DUAL || TMA_ST, "the fused gate/up epilogue writes through TMA stores");
     using namespace pairk;
     using PBars = BarsT<PSTAGES>;
     static_assert(sizeof(PBars) <= 256, "barrier block");
@@ -690,8 +720,14 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 uint8_t *a_dst = a_tiles + stage * P_A_STAGE;
                 uint8_t *b_dst = b_tiles + stage * P_B_STAGE;
                 tma_load_2d_pair(a_dst, &tmA, full_leader, kb * BK, row0);
-                tma_load_2d_pair(b_dst, &tmB, full_leader, col0, kb * BK);
-                tma_load_2d_pair(b_dst + B_BOX, &tmB, full_leader, col0 + 64, kb * BK);
+                if (DUAL) {
+                    // same 64 columns of W_g and of W_u
+                    tma_load_2d_pair(b_dst, &tmB, full_leader, col0, kb * BK);
+                    tma_load_2d_pair(b_dst + B_BOX, &tmB2, full_leader, col0, kb * BK);
+                } else {
+                    tma_load_2d_pair(b_dst, &tmB, full_leader, col0, kb * BK);
+                    tma_load_2d_pair(b_dst + B_BOX, &tmB, full_leader, col0 + 64, kb * BK);
+                }
                 ++issued;
                 if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
             }
@@ -718,7 +754,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer (leader)
-        const uint32_t idesc = make_idesc(AB_FORMAT, PBM, (uint32_t)bn);
+        const uint32_t idesc = make_idesc(AB_FORMAT, PBM, DUAL ? 256u : (uint32_t)bn);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -772,7 +808,49 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int row = tm * PBM + row_in_tile;
             const int n0 = tn * bn;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * PBN);
-            if constexpr (TMA_ST) {
+            if constexpr (DUAL) {
+                const int box_row0 = tm * PBM + (int)rank * 128 + quarter * 32;  // warp-uniform
+#pragma unroll 1
+                for (int g = 0; g < 2; ++g) {
+                    const int c0 = n0 + g * 64;
+                    if (c0 >= N) break;  // warp-uniform
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    __syncwarp();
+                    uint8_t *rowp = my_stg + sb * P_STG_BOX + lane * 128;
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t rg[32], ru[32];
+                        tmem_ld_32cols(t_row + (uint32_t)(g * 128 + h * 32), rg);
+                        tmem_ld_32cols(t_row + (uint32_t)(g * 128 + 64 + h * 32), ru);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            float z[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                z[e] = silu_mul(__uint_as_float(rg[8 * c + e]), __uint_as_float(ru[8 * c + e]),
+                                                (T *)nullptr);
+                            uint4 v;
+                            v.x = pack2(z[0], z[1], (T *)nullptr);
+                            v.y = pack2(z[2], z[3], (T *)nullptr);
+                            v.z = pack2(z[4], z[5], (T *)nullptr);
+                            v.w = pack2(z[6], z[7], (T *)nullptr);
+                            *reinterpret_cast<uint4 *>(rowp + (((h * 4 + c) ^ (lane & 7)) << 4)) = v;
+                        }
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && box_row0 < M) {
+                        asm volatile(
+                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                                reinterpret_cast<uint64_t>(&tmC)),
+                            "r"(c0), "r"(box_row0), "r"(smem_u32(my_stg + sb * P_STG_BOX))
+                            : "memory");
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                    sb ^= 1;
+                }
+            } else if constexpr (TMA_ST) {
                 const int box_row0 = tm * PBM + (int)rank * 128 + quarter * 32;  // warp-uniform
 #pragma unroll 1
                 for (int g = 0; g < (bn >> 6); ++g) {
@@ -930,12 +1008,12 @@ constexpr int kPairStages = kPairTmaStore ? 6 : 7;
 
 // Largest number of co-resident two-CTA clusters of the pair kernel, per device
 // (0: the pair kernel cannot be launched).
-template <typename T, uint32_t F>
+template <typename T, uint32_t F, bool DUAL = false>
 int pair_clusters_max(int dev) {
     static std::atomic<int> cached[64];
     static std::once_flag once[64];
     std::call_once(once[dev & 63], [&] {
-        auto kern = umma_pair_kernel<T, F, kPairStages, kPairTmaStore>;
+        auto kern = umma_pair_kernel<T, F, kPairStages, kPairTmaStore, DUAL>;
         const int smem = pairk::smem_bytes(kPairStages, kPairTmaStore);
         int n = 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
@@ -1002,7 +1080,38 @@ cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, c
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, kPairStages, kPairTmaStore>, ta, tb, tc,
-                              static_cast<T *>(p.C), p.M, p.N, p.K, status, bn);
+                              static_cast<T *>(p.C), p.M, p.N, p.K, status, bn, tb);
+}
+
+// Z = SiLU(X W_g) * (X W_u): p.A = X [M,K], p.B = W_g [K,N], p.C = Z [M,N];
+// w_u = W_u [K,N].  256 x 128 tiles of Z on CTA pairs.
+template <typename T, uint32_t F>
+cudaError_t launch_pair_silu_mul_typed(const Problem &p, const void *w_u, int clusters_max, int *status,
+                                       cudaStream_t s) {
+    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap ta, tg, tu, tc;
+    if (!make_map(&ta, p.A, dt, p.M, p.K, 128, BK)) return cudaErrorInvalidValue;
+    if (!make_map(&tg, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
+    if (!make_map(&tu, w_u, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
+    if (!make_map(&tc, p.C, dt, p.M, p.N, 32, 64)) return cudaErrorInvalidValue;
+    const int bn = 128;
+    const long long tiles = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * ((p.N + bn - 1) / bn);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pairk::smem_bytes(kPairStages, kPairTmaStore);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, kPairStages, kPairTmaStore, true>, ta, tg, tc,
+                              static_cast<T *>(p.C), p.M, p.N, p.K, status, bn, tu);
 }
 
 }  // namespace
@@ -1125,6 +1234,22 @@ cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s) {
     e = cudaMemsetAsync(d.ptr, 0, sizeof(int), s);  // the status word starts at zero
     if (e != cudaSuccess) return e;
     return launch_umma(p, num_sms, d.ptr, s, /*may_allocate=*/false);
+}
+
+bool umma_silu_mul_supported(const Problem &p, const void *w_u) {
+    if (p.elt != Elt::BF16 || !kPairTmaStore) return false;
+    return aligned(p.A, 16) && aligned(p.B, 16) && aligned(w_u, 16) && aligned(p.C, 16) && (p.K % 8) == 0 &&
+           (p.N % 8) == 0;
+}
+
+cudaError_t launch_umma_silu_mul(const Problem &p, const void *w_u, int *status, cudaStream_t s) {
+    if (!umma_silu_mul_supported(p, w_u)) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int cmax = pair_clusters_max<__nv_bfloat16, 1, true>(dev);
+    if (cmax <= 0) return cudaErrorNotSupported;
+    return launch_pair_silu_mul_typed<__nv_bfloat16, 1>(p, w_u, cmax, status, s);
 }
 
 }  // namespace gemm_gb300

@@ -97,6 +97,19 @@ GEMM_API gemm_status_t gemm_f16_cm(const uint16_t *A, const uint16_t *B, uint16_
 GEMM_API gemm_status_t gemm_bf16_rm(const uint16_t *A, const uint16_t *B, uint16_t *C,
                                     int M, int N, int K);
 
+/* Fused FFN gate/up projection ("Chapter 5 Operators and Runtime", section 5.3.1
+ * and example 5-4): Z = SiLU(X·W_g) ⊙ (X·W_u), with SiLU(x) = x / (1 + e^-x) and ⊙
+ * the element-wise product.  All bf16 row-major with tight strides: X [M,K],
+ * W_g [K,N], W_u [K,N], Z [M,N].  Both products accumulate in FP32 on the tensor
+ * cores; the fused epilogue keeps the rounding points of the unfused chain
+ * (section 5.3.1, figure 5-15): G and U rounded to bf16, T = bf16(SiLU(G)) with
+ * SiLU evaluated in FP32, Z = bf16(T·U).  G, U and T are never written to
+ * memory.  Needs X, W_g, W_u, Z 16-byte aligned and K, N multiples of 8
+ * (GEMM_ERR_INVALID_VALUE otherwise); Z must not overlap an input
+ * (GEMM_ERR_ALIAS).  K = 0 gives Z = 0. */
+GEMM_API gemm_status_t gemm_bf16_rm_silu_mul(const uint16_t *X, const uint16_t *W_g, const uint16_t *W_u,
+                                             uint16_t *Z, int M, int N, int K);
+
 /* BF16 row-major GEMM that allocates no device memory.  The pages have no
  * counterpart to this entry point: it is an interface addition for callers that
  * cannot call cudaMalloc.  Some host applications own all device memory through

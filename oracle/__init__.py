@@ -141,6 +141,43 @@ def gemm_entries(variant: str, A, B, M: int, N: int, K: int, ii, jj):
     return C, S
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 values rounded once to the nearest bf16 value (ties to even),
+    returned as float64: the significand is scaled to 8 bits and rounded with
+    numpy's round-half-to-even.  Normal range only (no overflow or subnormal
+    handling, which the callers' values never reach)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                      # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """SiLU(x) = x / (1 + e^-x) in float64 ("Chapter 5 Operators and Runtime",
+    section 5.3.1)."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def silu_mul(X, W_g, W_u, M: int, N: int, K: int, rows=None):
+    """The FFN gate/up chain of section 5.3.1 with its rounding points:
+    G = X W_g and U = X W_u (FP64 sums of the stored bf16 inputs), each rounded
+    to bf16; T = bf16(SiLU(G)); Z = bf16(T * U).  Returns a dict of float64
+    arrays of shape [M, N] (or [len(rows), N] when rows is given): Z, the rounded
+    intermediates G, U, T, and S_G, S_U = sum_k |x_ik w_kj| of the two products."""
+    if rows is None:
+        G, S_G = gemm("bf16_rm", X, W_g, M, N, K)
+        U, S_U = gemm("bf16_rm", X, W_u, M, N, K)
+    else:
+        G, S_G = gemm_rows("bf16_rm", X, W_g, M, N, K, rows)
+        U, S_U = gemm_rows("bf16_rm", X, W_u, M, N, K, rows)
+    G = round_bf16(G)
+    U = round_bf16(U)
+    T = round_bf16(silu(G))
+    Z = round_bf16(T * U)
+    return {"Z": Z, "G": G, "U": U, "T": T, "S_G": S_G, "S_U": S_U}
+
+
 def decode(dtype: str, bits) -> np.ndarray:
     """The oracle's own decoder of half/bf16 bit patterns, as float64."""
     lib = _load()

@@ -92,3 +92,26 @@ def round_to(variant: str, x: np.ndarray) -> np.ndarray:
     lsb = (b >> np.uint64(16)) & np.uint64(1)
     r = (((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)).astype(np.uint32)
     return r.view(np.float32).astype(np.float64)
+
+
+def tol_silu_mul(G: np.ndarray, U: np.ndarray, T: np.ndarray, Z: np.ndarray,
+                 S_G: np.ndarray, S_U: np.ndarray) -> np.ndarray:
+    """Tolerance of Z = bf16(bf16(SiLU(G)) * U) against the oracle's rounded G, U, T, Z.
+
+    The GPU's FP32 sums may differ from the exact ones by the FP32 accumulation
+    allowance 1e-5 * sum_k |a_ik b_kj| (S_G, S_U) -- large relative to G or U when
+    their terms nearly cancel -- and then round to the neighbouring bf16 value;
+    SiLU is evaluated in FP32.  So:
+      dG = 2^-7 |G| + 1e-5 S_G,   dU = 2^-7 |U| + 1e-5 S_U   (one bf16 step each;
+                                                             2^-7 bounds a step)
+      dT = |SiLU'(G)| dG + 2^-7 |T|,  SiLU'(g) = s (1 + g (1 - s)), s = 1/(1+e^-g)
+      dZ = dT |U| + |T| dU + ulp(Z).
+    """
+    G, U, T, Z, S_G, S_U = (np.asarray(a, dtype=np.float64) for a in (G, U, T, Z, S_G, S_U))
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-G))
+    slope = np.abs(s * (1.0 + G * (1.0 - s)))
+    dG = 2.0 ** -7 * np.abs(G) + 1e-5 * S_G
+    dU = 2.0 ** -7 * np.abs(U) + 1e-5 * S_U
+    dT = slope * dG + 2.0 ** -7 * np.abs(T)
+    return dT * np.abs(U) + np.abs(T) * dU + ulp_out("bf16", Z)

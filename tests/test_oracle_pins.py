@@ -266,3 +266,76 @@ def test_output_ulp_values():
     assert compare.ulp_out("f16", np.array([1.0]))[0] == 2.0 ** -10
     assert compare.ulp_out("f16", np.array([0.0]))[0] == 2.0 ** -24
     assert compare.ulp_out("f16", np.array([1e-6]))[0] == 2.0 ** -24  # subnormal spacing
+
+
+def test_round_bf16_matches_float32_path_and_ties():
+    """Rounding float64 to bf16 once equals the float32 route wherever the value is
+    already a float32 (no double rounding there), and ties go to even."""
+    rng = np.random.default_rng(21)
+    x = rng.uniform(-50, 50, 5000).astype(np.float32).astype(np.float64)
+    assert np.array_equal(oracle.round_bf16(x), compare.round_to("bf16_rm", x))
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to even -> 1
+    assert oracle.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert oracle.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2 * 2.0 ** -7
+    assert oracle.round_bf16(np.array([-3.0]))[0] == -3.0
+
+
+def test_silu_identities():
+    """SiLU(0) = 0; SiLU(x) - SiLU(-x) = x; SiLU -> x for large x, -> 0 for very
+    negative x; SiLU(x) = x * sigmoid(x) with the library logistic function."""
+    from scipy.special import expit
+    x = np.linspace(-30, 30, 2001)
+    s = oracle.silu(x)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    assert np.allclose(s - oracle.silu(-x), x, rtol=0, atol=1e-12)
+    assert np.allclose(s, x * expit(x), rtol=1e-14, atol=1e-300)
+    assert abs(oracle.silu(np.array([40.0]))[0] - 40.0) < 1e-15 * 40
+    assert abs(oracle.silu(np.array([-40.0]))[0]) < 1e-15
+
+
+def test_silu_mul_brute_force_small():
+    """The gate/up chain on tiny integer inputs against a pure-Python evaluation of
+    the same definition (exact integer sums, math.exp, the same rounding points)."""
+    import math
+    M, N, K = 3, 5, 4
+    rng = np.random.default_rng(17)
+    x = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    wg = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    wu = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    enc = lambda a: (a.reshape(-1).view(np.uint32) >> 16).astype(np.uint16)
+    r = oracle.silu_mul(enc(x), enc(wg), enc(wu), M, N, K)
+    Z, G, U, T = r["Z"], r["G"], r["U"], r["T"]
+    rb = lambda v: float(oracle.round_bf16(np.array([v]))[0])
+    for i in range(M):
+        for j in range(N):
+            g = rb(sum(int(x[i, k]) * int(wg[k, j]) for k in range(K)))
+            u = rb(sum(int(x[i, k]) * int(wu[k, j]) for k in range(K)))
+            t = rb(g / (1.0 + math.exp(-g)))
+            assert (G[i, j], U[i, j], T[i, j]) == (g, u, t)
+            assert Z[i, j] == rb(t * u)
+
+
+def test_silu_mul_tolerance_admits_one_step_moves():
+    """Moving G or U by one bf16 step (a rounding-boundary flip) stays within the
+    tolerance, and so does an FP32-level error in a cancelling U; a 5% error in
+    Z does not."""
+    rng = np.random.default_rng(3)
+    g = oracle.round_bf16(rng.normal(0, 2, 4000))
+    u = oracle.round_bf16(rng.normal(0, 2, 4000))
+    s_g = np.abs(g) + 1.0
+    s_u = np.abs(u) + 1.0
+    t = oracle.round_bf16(oracle.silu(g))
+    z = oracle.round_bf16(t * u)
+    tol = compare.tol_silu_mul(g, u, t, z, s_g, s_u)
+    g2 = g + compare.ulp_out("bf16", g)
+    t2 = oracle.round_bf16(oracle.silu(g2))
+    z2 = oracle.round_bf16(t2 * u)
+    assert np.all(np.abs(z2 - z) <= tol)
+    u2 = u + compare.ulp_out("bf16", u)
+    z3 = oracle.round_bf16(t * u2)
+    assert np.all(np.abs(z3 - z) <= tol)
+    u4 = oracle.round_bf16(u + 0.9e-5 * s_u)
+    z4 = oracle.round_bf16(t * u4)
+    assert np.all(np.abs(z4 - z) <= tol)
+    big = (np.abs(z) > 0.5) & (g > 0)
+    assert np.all((np.abs(1.05 * z - z) > tol)[big])
