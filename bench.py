@@ -276,6 +276,24 @@ def cpu_sample(variant, A, B, M, N, K, budget_s: float, extra=()):
     return fl / dt, nrows, dt, threads
 
 
+# ------------------------------------------------------------------ replicas
+def slowest_rank_ms(ms: float, world: int, device: str = "cpu") -> float:
+    """The timed region's length on the slowest rank (every rank gets it)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(flops_per_step: float, steps: int, world: int, ms_slowest: float) -> float:
+    """Whole-job TFLOP/s of `world` independent replicas (weak scaling): the FLOPs
+    of all ranks divided by the slowest rank's time."""
+    return flops_per_step * steps * world / (ms_slowest / 1e3) / 1e12
+
+
 # ------------------------------------------------------------------ our arm
 def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler_uuid=None, e2e=True,
                      cpu_budget=0.0, clocks=True, prop_mhz=None):
@@ -408,10 +426,7 @@ def run_ours(args):
                                                             and not args.no_cpu_baseline) else 0.0),
                            clocks=(rank == 0), prop_mhz=prop_mhz)
     ms_total = res["ms_total"]
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = slowest_rank_ms(ms_total, world, device="cuda")
 
     paths = []
     if not args.no_paths and rank == 0:
@@ -425,8 +440,7 @@ def run_ours(args):
 
     if rank == 0:
         M, N, K = res["M"], res["N"], res["K"]
-        flops_all = res["flops_per_step"] * args.steps * world
-        value = flops_all / (ms_total / 1e3) / 1e12
+        value = replica_throughput(res["flops_per_step"], args.steps, world, ms_total)
         clk = res["clocks"] or {}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
