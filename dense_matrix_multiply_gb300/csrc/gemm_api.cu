@@ -14,7 +14,7 @@ using namespace gemm_gb300;
 
 namespace {
 
-enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma };
+enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma, UmmaStall };
 
 thread_local cudaStream_t t_stream = nullptr;
 thread_local const char *t_last_kernel = "none";
@@ -154,6 +154,9 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     case Family::Umma:
         if (!umma_supported(p)) return GEMM_ERR_INVALID_VALUE;
         return finish(launch_umma(p, dev->num_sms, dev->status, s), kernel_name("umma", elt));
+    case Family::UmmaStall:
+        if (elt == Elt::F32) return GEMM_ERR_INVALID_VALUE;
+        return finish(launch_umma_stall_test(p, dev->num_sms, dev->status, s), "umma_stall");
     case Family::Auto:
         break;
     }
@@ -338,6 +341,7 @@ GEMM_API gemm_status_t gemm_force_kernel(const char *family) {
     else if (!strcmp(family, "gemv")) t_force = Family::Gemv;
     else if (!strcmp(family, "gemv_scalar")) t_force = Family::GemvScalar;
     else if (!strcmp(family, "umma")) t_force = Family::Umma;
+    else if (!strcmp(family, "umma_stall")) t_force = Family::UmmaStall;
     else return GEMM_ERR_INVALID_VALUE;
     return GEMM_OK;
 }

@@ -41,6 +41,11 @@ cudaError_t launch_gemv(const Problem &p, bool vec, int num_sms, cudaStream_t s)
 cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s, bool may_allocate = true);
 bool umma_supported(const Problem &p);
 
+// Test of the bounded pipeline waits: the single-CTA tensor-core kernel with a
+// producer that issues no load, so every CTA takes its timeout path (~2 s) and
+// records a code in *status.  Returns the launch status.
+cudaError_t launch_umma_stall_test(const Problem &p, int num_sms, int *status, cudaStream_t s);
+
 // Fused FFN gate/up projection Z = SiLU(X W_g) * (X W_u) on the tensor-core
 // CTA pairs: p.A = X [M,K], p.B = W_g [K,N], p.C = Z [M,N], w_u = W_u [K,N],
 // all bf16 row-major, 16-byte aligned, K % 8 == 0, N % 8 == 0.

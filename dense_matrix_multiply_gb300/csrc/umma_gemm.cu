@@ -357,7 +357,7 @@ __device__ __forceinline__ float silu_mul(float g, float u, __half *) {
 template <typename T, uint32_t AB_FORMAT, bool A_CPASYNC>
 __global__ void __launch_bounds__(A_CPASYNC ? THREADS + 128 : THREADS, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const T *__restrict__ A, T *__restrict__ C, int M, int N, int K, int *status)
+                 const T *__restrict__ A, T *__restrict__ C, int M, int N, int K, int *status, int stall)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -455,7 +455,9 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        // stall != 0 (a test of the bounded waits): issue no load at all, so the
+        // MMA thread's first wait runs out and the CTA takes its timeout path.
+        for (int t = blockIdx.x; t < num_tiles && ok && !stall; t += gridDim.x) {
             int tm, tn;
             tile_coords(t, tiles_m, tiles_n, tm, tn);
             const int n_left = N - tn * BN;
@@ -970,7 +972,7 @@ bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int ro
 }
 
 template <typename T, uint32_t F, bool A_CPASYNC>
-cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_t s) {
+cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_t s, int stall = 0) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
     if (!make_map(&tb, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
@@ -994,7 +996,7 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
     kern<<<grid, A_CPASYNC ? THREADS + 128 : THREADS, SMEM_BYTES, s>>>(
-        ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K, status);
+        ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K, status, stall);
     return cudaGetLastError();
 }
 
@@ -1250,6 +1252,12 @@ cudaError_t launch_umma_silu_mul(const Problem &p, const void *w_u, int *status,
     const int cmax = pair_clusters_max<__nv_bfloat16, 1, true>(dev);
     if (cmax <= 0) return cudaErrorNotSupported;
     return launch_pair_silu_mul_typed<__nv_bfloat16, 1>(p, w_u, cmax, status, s);
+}
+
+cudaError_t launch_umma_stall_test(const Problem &p, int num_sms, int *status, cudaStream_t s) {
+    if (!umma_supported(p) || !a_tma_ok(p)) return cudaErrorInvalidValue;
+    if (p.elt == Elt::BF16) return launch_typed<__nv_bfloat16, 1, false>(p, num_sms, status, s, 1);
+    return launch_typed<__half, 0, false>(p, num_sms, status, s, 1);
 }
 
 }  // namespace gemm_gb300

@@ -165,9 +165,13 @@ GEMM_API const char *gemm_last_error(void);
 
 /* Test and benchmark hook: forces the calling thread's later calls onto one
  * kernel family -- "simt", "simt_scalar", "gemv", "gemv_scalar", "umma" -- or
- * back to automatic dispatch with NULL or "".  A forced family that cannot run a
- * given problem makes that call return GEMM_ERR_INVALID_VALUE; an unknown name
- * is rejected here with GEMM_ERR_INVALID_VALUE. */
+ * back to automatic dispatch with NULL or "".  A forced family that cannot run
+ * a given problem makes that call return GEMM_ERR_INVALID_VALUE; an unknown
+ * name is rejected here with GEMM_ERR_INVALID_VALUE.
+ * "umma_stall" tests the tensor-core kernel's bounded waits: a 16-bit call whose
+ * A, B and C suit the TMA kernel launches it with a producer that issues no
+ * loads, every CTA gives up after about two seconds, C is left unwritten and
+ * the next gemm_synchronize returns GEMM_ERR_TIMEOUT. */
 GEMM_API gemm_status_t gemm_force_kernel(const char *family);
 
 #ifdef __cplusplus

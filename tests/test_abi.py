@@ -59,7 +59,7 @@ def test_status_strings(built):
 
 
 def test_force_kernel_names(built):
-    for fam in ("simt", "simt_scalar", "gemv", "gemv_scalar", "umma", None, ""):
+    for fam in ("simt", "simt_scalar", "gemv", "gemv_scalar", "umma", "umma_stall", None, ""):
         g.gemm_force_kernel(fam)
     with pytest.raises(g.GemmError):
         g.gemm_force_kernel("cpu")
