@@ -10,7 +10,12 @@ Every function here is pinned by ``tests/test_oracle_pins.py`` against brute
 force on small integer inputs (exact rational arithmetic), closed forms
 (ones·ones = K, I·B = B), the row-major/column-major transpose identity,
 bit-exhaustive checks of the half and bf16 decoders, and a float64 library
-matmul on the decoded values.
+matmul on the decoded values.  ``gemm_ex`` (the general form with alpha,
+beta, operation flags, leading dimensions and batches) is pinned by
+``tests/test_oracle_ex_pins.py``: exact integer results for every layout and
+operation pair with NaN-filled padding, reduction to ``gemm`` in the plain
+case, and the row-/column-major transpose identity.  ``silu_mul`` is pinned by
+brute force and by SiLU's identities in ``tests/test_oracle_pins.py``.
 """
 
 from __future__ import annotations
@@ -57,6 +62,10 @@ def _load():
                                              vp, i64, dp, dp]
             lib.oracle_gemm_entries.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64,
                                                 vp, vp, i64, dp, dp]
+            d = ctypes.c_double
+            lib.oracle_gemm_ex.argtypes = [ctypes.c_int] * 4 + [i64, i64, i64, d,
+                                           vp, i64, i64, vp, i64, i64, d, vp, i64, i64, i64,
+                                           dp, dp, dp, dp]
             lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
             lib.oracle_decode_f16.restype = ctypes.c_double
             lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
@@ -139,6 +148,55 @@ def gemm_entries(variant: str, A, B, M: int, N: int, K: int, ii, jj):
     if rc:
         raise RuntimeError(f"oracle_gemm_entries failed ({rc})")
     return C, S
+
+
+OPS = {"N": 0, "T": 1}
+
+
+def gemm_ex(dtype: str, layout: str, op_a: str, op_b: str, M: int, N: int, K: int,
+            alpha: float, A, lda: int, stride_a: int, B, ldb: int, stride_b: int,
+            beta: float, C, ldc: int, stride_c: int, batch: int = 1) -> dict:
+    """General form C_b <- alpha op(A_b) op(B_b) + beta C_b, b < batch ("SGEMM
+    measured and the three ledgers", sections 2 and 3).  dtype 'f32' | 'f16' |
+    'bf16', layout 'rm' | 'cm', op_a / op_b 'N' | 'T'; A, B, C are flat storage
+    buffers (C may be None when beta == 0).  Returns a dict of float64 arrays
+    of shape [batch, M, N]: C (the result), P (the product sum), S (the sum of
+    absolute products) and BC (beta * C_in)."""
+    lib = _load()
+    want = np.float32 if dtype == "f32" else np.uint16
+
+    def flat(x):
+        if x is None:
+            return np.zeros(1, dtype=want)
+        x = np.ascontiguousarray(x).reshape(-1)
+        if x.dtype != want:
+            raise TypeError(f"{dtype} buffer must be {np.dtype(want).name}, got {x.dtype}")
+        return x
+
+    a, b, c = flat(A), flat(B), flat(C)
+    # The storage each matrix spans must lie inside its buffer.
+    a_rows, a_cols = (M, K) if op_a == "N" else (K, M)
+    b_rows, b_cols = (K, N) if op_b == "N" else (N, K)
+    for name, buf, r, cc, ld, st, used in (
+            ("A", a, a_rows, a_cols, lda, stride_a, alpha != 0 and K > 0),
+            ("B", b, b_rows, b_cols, ldb, stride_b, alpha != 0 and K > 0),
+            ("C", c, M, N, ldc, stride_c, beta != 0)):
+        if not used or batch == 0 or r == 0 or cc == 0:
+            continue
+        inner, outer = (cc, r) if layout == "rm" else (r, cc)
+        if ld < inner:
+            raise ValueError(f"ld{name.lower()} {ld} < {inner}")
+        span = (batch - 1) * st + (outer - 1) * ld + inner
+        if span > buf.size:
+            raise ValueError(f"{name} spans {span} elements, buffer holds {buf.size}")
+    out = {k: np.empty(batch * M * N, dtype=np.float64) for k in ("C", "P", "S", "BC")}
+    rc = lib.oracle_gemm_ex(DTYPES[dtype], LAYOUTS[layout], OPS[op_a], OPS[op_b], M, N, K, float(alpha),
+                            _ptr(a), lda, stride_a, _ptr(b), ldb, stride_b, float(beta), _ptr(c), ldc,
+                            stride_c, batch, _ptr(out["C"]), _ptr(out["P"]), _ptr(out["S"]),
+                            _ptr(out["BC"]))
+    if rc:
+        raise RuntimeError(f"oracle_gemm_ex failed ({rc})")
+    return {k: v.reshape(batch, M, N) for k, v in out.items()}
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:

@@ -115,3 +115,50 @@ def tol_silu_mul(G: np.ndarray, U: np.ndarray, T: np.ndarray, Z: np.ndarray,
     dU = 2.0 ** -7 * np.abs(U) + 1e-5 * S_U
     dT = slope * dG + 2.0 ** -7 * np.abs(T)
     return dT * np.abs(U) + np.abs(T) * dU + ulp_out("bf16", Z)
+
+
+def tol_ex(variant: str, ref: dict, K: int, alpha: float) -> np.ndarray:
+    """Tolerance of the general form alpha op(A) op(B) + beta C against
+    ``oracle.gemm_ex``'s outputs (P, S, BC, C).
+
+    The device sums the products in FP32 (acc), forms alpha * acc + beta * c in
+    FP32 and rounds once to the output type.  So the allowance is the variant's
+    own rule applied to the scaled product -- 1e-5 |alpha| S for FP32, the
+    half/bf16 rule at |alpha P| -- plus 2^-22 (|alpha P| + |beta c|) for the two
+    FP32 roundings of the combination (each at most 2^-24 relative), plus, for
+    16-bit outputs, one output ulp at |C| for the final rounding of the combined
+    value.  With alpha = 1 and beta = 0 this is the plain rule plus the
+    2^-22 |P| term."""
+    dtype = variant.split("_")[0]
+    P, S, BC, C = (np.asarray(ref[k], dtype=np.float64) for k in ("P", "S", "BC", "C"))
+    prod = alpha * P
+    if alpha == 0 or K == 0:
+        base = np.zeros_like(P)
+    elif dtype == "f32":
+        base = tol_f32(abs(alpha) * S)
+    else:
+        base = tol_half(prod, K, dtype)
+    t = base + 2.0 ** -22 * (np.abs(prod) + np.abs(BC))
+    if dtype != "f32":
+        t = t + ulp_out(dtype, C)
+    return t
+
+
+def check_ex(variant: str, C: np.ndarray, ref: dict, K: int, alpha: float) -> dict:
+    """Element-wise comparison of a general-form result (float64, shape of ref['C'])."""
+    C = np.asarray(C, dtype=np.float64)
+    C_ref = np.asarray(ref["C"], dtype=np.float64)
+    if C.shape != C_ref.shape:
+        raise ValueError(f"shape {C.shape} != reference shape {C_ref.shape}")
+    tol = tol_ex(variant, ref, K, alpha)
+    err = np.abs(C - C_ref)
+    bad = ~(err <= tol)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(tol > 0, err / np.where(tol > 0, tol, 1.0), np.where(err > 0, np.inf, 0.0))
+    return {
+        "n": int(C.size),
+        "n_bad": int(bad.sum()),
+        "max_abs_err": float(np.nanmax(err)) if C.size else 0.0,
+        "max_err_over_tol": float(np.nanmax(ratio)) if C.size else 0.0,
+        "ok": bool(not bad.any()),
+    }

@@ -210,6 +210,74 @@ int oracle_gemm_entries(int dtype, int layout, const void *A, const void *B,
     return 0;
 }
 
+/*
+ * General form, one problem per batch index b = 0 .. batch-1:
+ *
+ *     C_b <- alpha * op(A_b) * op(B_b) + beta * C_b
+ *
+ * ("SGEMM measured and the three ledgers", section 2: the library call with
+ * operation flags, leading dimensions and the row-/column-major reading of the
+ * same bytes; section 3, kernel K1: C = alpha * acc + beta * C).  op(X) is X or
+ * its transpose.  Storage of element (r, c) of a stored matrix with leading
+ * dimension ld: row-major X[r*ld + c], column-major X[r + c*ld].  op(A) is
+ * M x K: A is stored M x K (op 'N') or K x M (op 'T'); op(B) is K x N: B is
+ * stored K x N or N x K; C is M x N.  Matrix b starts stride elements after
+ * matrix b-1 (stride 0 reuses one matrix for every b).
+ *
+ * Outputs, each [batch, M, N] row-major and independent of the layout:
+ *   C:  alpha * P + beta * c_in in double;
+ *   P:  the plain product sum, sum_k op(A)[i,k] op(B)[k,j] (ascending k);
+ *   S:  sum_k |op(A)[i,k] op(B)[k,j]|;
+ *   BC: beta * c_in.
+ * As in the BLAS convention, C_in is not read when beta == 0 (a NaN there does
+ * not reach the result), and A and B are not read when alpha == 0 or K == 0
+ * (the product term is then exactly zero).
+ */
+static int64_t off_stored(int layout, int64_t ld, int64_t r, int64_t c)
+{
+    return layout == ORACLE_ROW_MAJOR ? r * ld + c : r + c * ld;
+}
+
+int oracle_gemm_ex(int dtype, int layout, int op_a, int op_b,
+                   int64_t M, int64_t N, int64_t K, double alpha,
+                   const void *A, int64_t lda, int64_t stride_a,
+                   const void *B, int64_t ldb, int64_t stride_b,
+                   double beta, const void *Cin, int64_t ldc, int64_t stride_c,
+                   int64_t batch, double *C, double *P, double *S, double *BC)
+{
+    if (bad_args(dtype, layout, M, N, K) || batch < 0) return 1;
+    if ((op_a != 0 && op_a != 1) || (op_b != 0 && op_b != 1)) return 1;
+    if (stride_a < 0 || stride_b < 0 || stride_c < 0) return 1;
+    const int use_ab = alpha != 0.0 && K > 0;
+    const int64_t rows = batch * M;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t b = r / M, i = r % M;
+        double *c = C + r * N, *p = P + r * N, *s = S + r * N, *bc = BC + r * N;
+        for (int64_t j = 0; j < N; ++j) { p[j] = 0.0; s[j] = 0.0; }
+        if (use_ab) {
+            const int64_t a0 = b * stride_a, b0 = b * stride_b;
+            for (int64_t k = 0; k < K; ++k) {
+                /* op(A)[i,k]: stored (i,k) for 'N', stored (k,i) for 'T' */
+                const int64_t ia = op_a == 0 ? off_stored(layout, lda, i, k) : off_stored(layout, lda, k, i);
+                const double a = elem(A, dtype, a0 + ia);
+                for (int64_t j = 0; j < N; ++j) {
+                    /* op(B)[k,j]: stored (k,j) for 'N', stored (j,k) for 'T' */
+                    const int64_t ib = op_b == 0 ? off_stored(layout, ldb, k, j) : off_stored(layout, ldb, j, k);
+                    const double v = a * elem(B, dtype, b0 + ib);
+                    p[j] += v;
+                    s[j] += fabs(v);
+                }
+            }
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            bc[j] = beta == 0.0 ? 0.0 : beta * elem(Cin, dtype, b * stride_c + off_stored(layout, ldc, i, j));
+            c[j] = (use_ab ? alpha * p[j] : 0.0) + bc[j];
+        }
+    }
+    return 0;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
