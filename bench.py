@@ -11,7 +11,9 @@ launching stream), the roofline of the kernel, the oracle's CPU throughput
 on a bounded sample, an end-to-end number through host buffers, the clocks seen
 during the timed region and -- under "paths" -- the same measurements for the
 tensor-core workloads (FP16 column-major 8192^3 and 3072x5120x6144, BF16 FFN
-projection) and the M = 1 decode shapes.
+projection, the fused FFN gate/up projection), the M = 1 decode shapes, and the
+general form (gemm_ex: X W^T with W stored [N, K], a strided batch, FP32 with a
+transposed B).
 
 --impl reference times the CPU oracle (the reference arm of this build) on
 the same workload and prints its line with "impl": "reference".
@@ -80,7 +82,21 @@ def all_workloads():
     # the FFN gate/up projection with its SiLU * U epilogue fused (two GEMMs)
     out["ffn_gate_up_bf16_silu_mul_1024x12288x4096"] = (3, ("bf16_silu_mul", 1024, 12288, 4096, "normal", 1.0,
                                                              "normal", 1.0 / 64.0))
+    # the general form (gemm_ex): a linear layer's X W^T with W stored [N, K],
+    # a strided batch, and FP32 with a transposed B on the SIMT kernel
+    for dtype, ops, batch, (M, N, K) in (("bf16", "NT", 1, (8192, 8192, 8192)),
+                                         ("f16", "NN", 32, (1024, 1024, 1024)),
+                                         ("f32", "NT", 1, (4096, 4096, 4096))):
+        tag = f"gemm_ex_{dtype}_rm_{ops}" + (f"_batch{batch}" if batch > 1 else "") + f"_{M}x{N}x{K}"
+        out[tag] = (synthetic.EDGE_CONFIG_ID, (f"ex:{dtype}:rm:{ops[0]}:{ops[1]}:{batch}", M, N, K,
+                                               "uniform", 1.0, "uniform", 1.0))
     return out
+
+
+def ex_parse(variant: str):
+    """'ex:<dtype>:<layout>:<op_a>:<op_b>:<batch>' -> its fields (batch as int)."""
+    _, dtype, layout, op_a, op_b, batch = variant.split(":")
+    return dtype, layout, op_a, op_b, int(batch)
 
 
 def read_peaks():
@@ -186,10 +202,14 @@ def kernel_kind(name: str) -> str:
 
 def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, peaks: dict, peaks_src: str,
                  sm_mhz: float | None, sms: int, workload: str, prop_mhz: float | None = None):
-    es = 4 if variant.startswith("f32") else 2
+    es = 4 if variant.startswith("f32") or variant.startswith("ex:f32") else 2
     if variant == "bf16_silu_mul":  # two products, X read once: X, W_g, W_u, Z
         flops = 2 * metrics.gemm_flops(M, N, K)
         algo_bytes = es * (M * K + 2 * K * N + M * N)
+    elif variant.startswith("ex:"):  # batch independent products, beta = 0 (C not read)
+        batch = ex_parse(variant)[4]
+        flops = batch * metrics.gemm_flops(M, N, K)
+        algo_bytes = batch * metrics.min_bytes(M, N, K, es)
     else:
         flops = metrics.gemm_flops(M, N, K)
         algo_bytes = metrics.min_bytes(M, N, K, es)
@@ -315,6 +335,20 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
 
         def call():
             return fn(pa, pb, pu, pc, M, N, K)
+    elif variant.startswith("ex:"):
+        # tight strides: A stored [M,K] or [K,M], B [K,N] or [N,K], batch matrices back to back
+        dtype, layout, op_a, op_b, batch = ex_parse(variant)
+        A = synthetic.matrix(dtype, batch * M, K, synthetic.seed_for(cfg, 5), da, sa)
+        B = synthetic.matrix(dtype, batch * K, N, synthetic.seed_for(cfg, 6), db, sb)
+        dA, dB, dC = device_inputs(dtype + "_rm", A, B, batch * M, N)
+        lda = M if op_a == "T" else K
+        ldb = K if op_b == "T" else N
+        fn = g.load().gemm_ex
+        args_ex = (g.DTYPES[dtype], g.LAYOUTS[layout], g.OPS[op_a], g.OPS[op_b], M, N, K, 1.0,
+                   dA.data_ptr(), lda, M * K, dB.data_ptr(), ldb, K * N, 0.0, dC.data_ptr(), N, M * N, batch)
+
+        def call():
+            return fn(*args_ex)
     else:
         A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
         dA, dB, dC = device_inputs(variant, A, B, M, N)
@@ -349,7 +383,8 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         sampler.stop()
         clk = sampler.summary(t_host0, t_host1)
 
-    flops = metrics.gemm_flops(M, N, K) * (2 if variant == "bf16_silu_mul" else 1)
+    flops = metrics.gemm_flops(M, N, K) * (2 if variant == "bf16_silu_mul" else
+                                           ex_parse(variant)[4] if variant.startswith("ex:") else 1)
     s_per = ms / 1e3 / steps
     res = {
         "workload": name, "variant": variant, "M": M, "N": N, "K": K, "kernel": kernel, "flops_per_step": flops,
@@ -531,7 +566,10 @@ def main(argv=None):
                                                    "ffn_bf16_rm_1024x12288x4096", "edge_bf16_rm_1x12288x4096",
                                                    "edge_f32_rm_1x12288x4096", "edge_bf16_rm_8192x4096x4100",
                                                    "edge_f32_rm_8192x4096x4100", "sgemm_f32_rm_256",
-                                                   "ffn_gate_up_bf16_silu_mul_1024x12288x4096"])
+                                                   "ffn_gate_up_bf16_silu_mul_1024x12288x4096",
+                                                   "gemm_ex_bf16_rm_NT_8192x8192x8192",
+                                                   "gemm_ex_f16_rm_NN_batch32_1024x1024x1024",
+                                                   "gemm_ex_f32_rm_NT_4096x4096x4096"])
     p.add_argument("--path-steps", type=int, default=50)
     p.add_argument("--no-paths", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -37,6 +37,9 @@ SIGNATURES = {
     "gemm_bf16_rm": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_bf16_rm_noalloc": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_bf16_rm_silu_mul": ([_VP, _VP, _VP, _VP, _I, _I, _I], _I),
+    "gemm_ex": ([_I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _VP, ctypes.c_int64, ctypes.c_int64,
+                 _VP, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, _VP, ctypes.c_int64, ctypes.c_int64,
+                 _I], _I),
     "gemm_set_stream": ([_VP], _I),
     "gemm_get_stream": ([], _VP),
     "gemm_synchronize": ([], _I),
@@ -137,6 +140,26 @@ def gemm_bf16_rm_silu_mul(X, W_g, W_u, Z, M: int, N: int, K: int) -> None:
     st = lib.gemm_bf16_rm_silu_mul(_addr(X), _addr(W_g), _addr(W_u), _addr(Z), int(M), int(N), int(K))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_bf16_rm_silu_mul", lib.gemm_last_error().decode())
+
+
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+LAYOUTS = {"rm": 0, "cm": 1}
+OPS = {"N": 0, "T": 1}
+
+
+def gemm_ex(dtype: str, layout: str, op_a: str, op_b: str, M: int, N: int, K: int, alpha: float,
+            A, lda: int, stride_a: int, B, ldb: int, stride_b: int, beta: float, C, ldc: int,
+            stride_c: int, batch: int = 1) -> None:
+    """C_b = alpha op(A_b) op(B_b) + beta C_b for b < batch.  dtype 'f32' | 'f16' |
+    'bf16', layout 'rm' | 'cm', op_a / op_b 'N' | 'T'; leading dimensions and
+    strides in elements (see include/gemm.h for the storage rules)."""
+    lib = load()
+    _bind_torch_stream(A, B, C)
+    st = lib.gemm_ex(DTYPES[dtype], LAYOUTS[layout], OPS[op_a], OPS[op_b], int(M), int(N), int(K),
+                     float(alpha), _addr(A), int(lda), int(stride_a), _addr(B), int(ldb), int(stride_b),
+                     float(beta), _addr(C), int(ldc), int(stride_c), int(batch))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_ex", lib.gemm_last_error().decode())
 
 
 def gemm_set_stream(stream) -> None:

@@ -1,5 +1,7 @@
 // C ABI of the library: argument checks, per-thread stream, device check,
 // dispatch to the kernels.  See include/gemm.h for the contract.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -42,6 +44,28 @@ __global__ void zero_fill_kernel(uint4 *p, size_t n16, uint8_t *tail, size_t nta
 __global__ void zero_fill_bytes_kernel(uint8_t *p, size_t n) {
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0;
+}
+
+__device__ __forceinline__ float elt_to_f32(float x) { return x; }
+__device__ __forceinline__ float elt_to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float elt_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void elt_from_f32(float *p, float x) { *p = x; }
+__device__ __forceinline__ void elt_from_f32(__half *p, float x) { *p = __float2half_rn(x); }
+__device__ __forceinline__ void elt_from_f32(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// The general form when the product term is absent (alpha == 0 or K == 0):
+// C_b = beta * C_b over row-major [M, N] matrices with leading dimension ldc,
+// and C_b = 0 without reading it when beta == 0.
+template <typename T>
+__global__ void scale_c_kernel(T *C, int M, int N, long long ldc, long long sc, long long batch, float beta) {
+    const long long per = (long long)M * N, total = batch * per;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const long long b = i / per, r = i - b * per;
+        const long long row = r / N, col = r - row * N;
+        T *p = C + b * sc + row * ldc + col;
+        elt_from_f32(p, beta == 0.0f ? 0.0f : beta * elt_to_f32(*p));
+    }
 }
 
 void record_cuda_error(cudaError_t e) {
@@ -206,9 +230,144 @@ void record_message(const char *msg) {
     t_last_error[sizeof(t_last_error) - 1] = '\0';
 }
 
+// a * b + c for non-negative operands; false if it exceeds 2^62.
+bool mul_add(long long a, long long b, long long c, long long *out) {
+    const long long lim = 1LL << 62;
+    if (a < 0 || b < 0 || c < 0) return false;
+    if (a != 0 && b > (lim - c) / a) return false;
+    *out = a * b + c;
+    return true;
+}
+
+// Elements from the first to one past the last one that `batch` stored
+// matrices of [outer, inner] (leading dimension ld, matrix stride `stride`)
+// touch: (batch - 1) * stride + (outer - 1) * ld + inner.  false on overflow.
+bool span_elems(long long batch, long long stride, long long outer, long long ld, long long inner, long long *out) {
+    long long one = 0, all = 0;
+    if (outer < 1 || inner < 1 || batch < 1) { *out = 0; return true; }
+    if (!mul_add(outer - 1, ld, inner, &one)) return false;
+    if (!mul_add(batch - 1, stride, one, &all)) return false;
+    *out = all;
+    return true;
+}
+
+gemm_status_t run_ex(int dtype, int layout, int op_a, int op_b, int M, int N, int K, float alpha, const void *A,
+                     long long lda, long long sa, const void *B, long long ldb, long long sb, float beta, void *C,
+                     long long ldc, long long sc, int batch) {
+    if (dtype < GEMM_F32 || dtype > GEMM_BF16) return GEMM_ERR_INVALID_VALUE;
+    if (layout != GEMM_ROW_MAJOR && layout != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_VALUE;
+    if ((op_a != GEMM_OP_N && op_a != GEMM_OP_T) || (op_b != GEMM_OP_N && op_b != GEMM_OP_T))
+        return GEMM_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || batch < 0 || sa < 0 || sb < 0 || sc < 0) return GEMM_ERR_INVALID_VALUE;
+    const Elt elt = dtype == GEMM_F32 ? Elt::F32 : dtype == GEMM_F16 ? Elt::F16 : Elt::BF16;
+    const long long es = elt == Elt::F32 ? 4 : 2;
+    // Column-major C = op(A) op(B) is row-major C^T = op(B)^T op(A)^T on the
+    // same buffers ("SGEMM measured and the three ledgers", section 2): swap the
+    // operands, their flags, leading dimensions and strides, and M with N.
+    if (layout == GEMM_COL_MAJOR) {
+        const void *tp = A; A = B; B = tp;
+        long long t = lda; lda = ldb; ldb = t;
+        t = sa; sa = sb; sb = t;
+        int ti = op_a; op_a = op_b; op_b = ti;
+        ti = M; M = N; N = ti;
+    }
+    // Row-major from here on.  A is stored [M,K] ('N') or [K,M] ('T'); B is
+    // stored [K,N] or [N,K]; C is [M,N].
+    const bool a_t = op_a == GEMM_OP_T, b_t = op_b == GEMM_OP_T;
+    const long long a_inner = a_t ? M : K, a_outer = a_t ? K : M;
+    const long long b_inner = b_t ? K : N, b_outer = b_t ? N : K;
+    const long long one = 1;
+    if (ldc < (N > 1 ? N : one) || lda < (a_inner > 1 ? a_inner : one) || ldb < (b_inner > 1 ? b_inner : one))
+        return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0 || batch == 0) { t_last_kernel = "noop"; return GEMM_OK; }
+    const bool use_ab = alpha != 0.0f && K > 0;
+    if (!C || (use_ab && (!A || !B))) return GEMM_ERR_INVALID_VALUE;
+    long long c_one = 0, c_span = 0, a_span = 0, b_span = 0;
+    if (!span_elems(1, 0, M, ldc, N, &c_one) || !span_elems(batch, sc, M, ldc, N, &c_span))
+        return GEMM_ERR_INVALID_VALUE;
+    if (batch > 1 && sc < c_one) return GEMM_ERR_INVALID_VALUE;  // the C matrices would overlap
+    if (use_ab) {
+        if (!span_elems(batch, sa, a_outer, lda, a_inner, &a_span) ||
+            !span_elems(batch, sb, b_outer, ldb, b_inner, &b_span))
+            return GEMM_ERR_INVALID_VALUE;
+        if (c_span > (1LL << 62) / es || a_span > (1LL << 62) / es || b_span > (1LL << 62) / es)
+            return GEMM_ERR_INVALID_VALUE;
+        if (overlaps(C, (size_t)(c_span * es), A, (size_t)(a_span * es)) ||
+            overlaps(C, (size_t)(c_span * es), B, (size_t)(b_span * es)))
+            return GEMM_ERR_ALIAS;
+    }
+
+    DeviceInfo *dev = nullptr;
+    gemm_status_t st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = t_stream;
+
+    if (!use_ab) {
+        if (t_force != Family::Auto) return GEMM_ERR_INVALID_VALUE;
+        const unsigned grid = (unsigned)(dev->num_sms * 8);
+        switch (elt) {
+        case Elt::F32: scale_c_kernel<<<grid, 256, 0, s>>>((float *)C, M, N, ldc, sc, batch, beta); break;
+        case Elt::F16: scale_c_kernel<<<grid, 256, 0, s>>>((__half *)C, M, N, ldc, sc, batch, beta); break;
+        case Elt::BF16: scale_c_kernel<<<grid, 256, 0, s>>>((__nv_bfloat16 *)C, M, N, ldc, sc, batch, beta); break;
+        }
+        return finish(cudaGetLastError(), "scale_c");
+    }
+
+    ProblemEx p = {};
+    p.A = A;
+    p.B = B;
+    p.C = C;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.batch = batch;
+    p.a_t = a_t;
+    p.b_t = b_t;
+    p.lda = lda;
+    p.ldb = ldb;
+    p.ldc = ldc;
+    p.sa = sa;
+    p.sb = sb;
+    p.sc = sc;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.elt = elt;
+    static const char *simt_names[3] = {"simt_ex_f32", "simt_ex_f16", "simt_ex_bf16"};
+    const char *simt_name = simt_ex_vec(p) ? "simt_ex_f32_vec4" : simt_names[(int)elt];
+    const char *umma_name = elt == Elt::BF16 ? "umma_ex_bf16" : "umma_ex_f16";
+
+    switch (t_force) {
+    case Family::Simt:
+        return finish(launch_simt_ex(p, s), simt_name);
+    case Family::Umma: {
+        if (!umma_ex_supported(p)) return GEMM_ERR_INVALID_VALUE;
+        const cudaError_t e = launch_umma_ex(p, dev->status, s);
+        if (e == cudaErrorNotSupported) return GEMM_ERR_INVALID_VALUE;
+        return finish(e, umma_name);
+    }
+    case Family::Auto:
+        break;
+    default:
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    if (elt != Elt::F32 && umma_ex_supported(p)) {
+        const cudaError_t e = launch_umma_ex(p, dev->status, s);
+        if (e != cudaErrorNotSupported) return finish(e, umma_name);
+    }
+    return finish(launch_simt_ex(p, s), simt_name);
+}
+
 }  // namespace
 
 extern "C" {
+
+GEMM_API gemm_status_t gemm_ex(gemm_dtype_t dtype, gemm_layout_t layout, gemm_op_t op_a, gemm_op_t op_b, int M,
+                               int N, int K, float alpha, const void *A, int64_t lda, int64_t stride_a,
+                               const void *B, int64_t ldb, int64_t stride_b, float beta, void *C, int64_t ldc,
+                               int64_t stride_c, int batch) {
+    return run_ex((int)dtype, (int)layout, (int)op_a, (int)op_b, M, N, K, alpha, A, lda, stride_a, B, ldb,
+                  stride_b, beta, C, ldc, stride_c, batch);
+}
 
 GEMM_API gemm_status_t gemm_f32_rm(const float *A, const float *B, float *C, int M, int N, int K) {
     return run(A, B, C, M, N, K, Elt::F32);

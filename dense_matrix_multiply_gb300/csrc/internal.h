@@ -1,7 +1,8 @@
 // Internal launcher interface shared by the C-ABI layer and the kernels.
-// Every problem reaching a launcher is row-major with tight leading
-// dimensions: C[M,N] = A[M,K] · B[K,N], M, N, K >= 1.  The column-major half
-// entry point is mapped onto this form before dispatch (C^T = B^T · A^T).
+// Every problem reaching a launcher is row-major: Problem is the tight
+// C[M,N] = A[M,K] · B[K,N] with M, N, K >= 1; ProblemEx the general form.
+// Column-major problems are mapped onto row-major ones before dispatch
+// (C^T = B^T · A^T).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -19,11 +20,34 @@ struct Problem {
     Elt elt;
 };
 
+// The general form, row-major: C_b = alpha * op(A_b) * op(B_b) + beta * C_b
+// for b < batch.  a_t: A is stored [K, M] (op(A) = A^T), else [M, K]; b_t: B is
+// stored [N, K], else [K, N]; C is [M, N].  Leading dimensions and batch
+// strides in elements; a batch stride may be 0 for A or B (one matrix for
+// every b).  C is read only when beta != 0.  M, N, K, batch >= 1 and
+// alpha != 0 when this reaches a launcher.
+struct ProblemEx {
+    const void *A;
+    const void *B;
+    void *C;
+    int M, N, K, batch;
+    bool a_t, b_t;
+    long long lda, ldb, ldc;
+    long long sa, sb, sc;
+    float alpha, beta;
+    Elt elt;
+};
+
 // FP32 (or 16-bit fallback) SIMT kernel on the CUDA cores.  vec4: float4
 // global loads/stores (needs K % 4 == 0, N % 4 == 0 and 16-byte aligned bases;
 // f32 only).  num_sms sizes the split of a partly filled last wave.  Returns
 // the launch status.
 cudaError_t launch_simt(const Problem &p, bool vec4, int num_sms, cudaStream_t s);
+
+// The general form on the SIMT kernel (any alignment, any leading dimension;
+// FP32 or 16-bit).  Vector loads where every operand allows them.
+cudaError_t launch_simt_ex(const ProblemEx &p, cudaStream_t s);
+bool simt_ex_vec(const ProblemEx &p);  // whether launch_simt_ex uses float4 loads
 
 // Skinny-M kernel (M <= kGemvMaxM): streams B once, FP32 accumulation, K split
 // over a thread-block cluster, fixed-order reduction in shared and distributed
@@ -40,6 +64,14 @@ cudaError_t launch_gemv(const Problem &p, bool vec, int num_sms, cudaStream_t s)
 // stream-ordered scratch (cudaMallocAsync); without it they use cp.async.
 cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s, bool may_allocate = true);
 bool umma_supported(const Problem &p);
+
+// The general form on the tensor-core CTA pairs (16-bit only).  Needs A, B, C
+// 16-byte aligned, every leading dimension (and, for batch > 1, every nonzero
+// batch stride) and every stored matrix's contiguous extent a multiple of 8
+// elements.  Returns
+// cudaErrorNotSupported, before any launch, when the problem does not qualify.
+bool umma_ex_supported(const ProblemEx &p);
+cudaError_t launch_umma_ex(const ProblemEx &p, int *status, cudaStream_t s);
 
 // Test of the bounded pipeline waits: the single-CTA tensor-core kernel with a
 // producer that issues no load, so every CTA takes its timeout path (~2 s) and

@@ -24,8 +24,18 @@
 // The same template with 16-bit inputs (converted to FP32 when staged) and
 // 16-bit outputs (rounded to nearest even once) serves as the tensor path's
 // fallback for strides TMA cannot describe.
+//
+// EX: the general form ("SGEMM measured and the three ledgers", section 2,
+// operation flags and leading dimensions; section 3, kernel K1,
+// alpha * acc + beta * C): C_b = alpha * op(A_b) op(B_b) + beta * C_b with
+// blockIdx.y the batch index.  TA: A stored [K, M]; its tile is then loaded
+// along m and stored k-major as it lies.  TB: B stored [N, K]; its tile is
+// loaded along k and transposed into the n-contiguous layout on the way in,
+// into rows padded by four floats so that the transposing stores of a warp
+// fall in 32 distinct banks.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <algorithm>
 
 #include "internal.h"
 
@@ -59,20 +69,37 @@ __device__ __forceinline__ void raster(int pid, int tiles_m, int tiles_n, int &t
     tn = r / gsize;
 }
 
+// Leading dimensions, batch strides (elements) and scalars of the general form.
+struct SimtEx {
+    long long lda, ldb, ldc;
+    long long sa, sb, sc;
+    float alpha, beta;
+};
+
 // BK: K step of a shared tile (8 or 16).  MINB: CTAs per SM the register
 // budget is sized for (__launch_bounds__).  MT: rows of C per CTA, 128 (a whole
 // 128 x 128 tile) or 64 (half a tile: CTA 2j+h computes rows 64h..64h+63 of
 // tile tile_begin + j, each thread 8 x 8 outputs).  Half tiles spread a
 // problem too small to fill the GPU over twice as many CTAs.
-template <typename TIn, typename TOut, bool VEC, int BK, int MINB, int MT>
+template <typename TIn, typename TOut, bool VEC, int BK, int MINB, int MT, bool EX = false, bool TA = false,
+          bool TB = false>
 __global__ void __launch_bounds__(THREADS, MINB)
 simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__restrict__ C,
-                 int M, int N, int K, int tile_begin)
+                 int M, int N, int K, int tile_begin, SimtEx ex)
 {
     static_assert(MT == 128 || MT == 64, "CTA covers a whole or half tile");
+    static_assert(EX || (!TA && !TB), "transposed operands need the general form");
     constexpr int RG = MT / 32;  // groups of four rows per thread
+    constexpr int BLD = TB ? B_LD + 4 : B_LD;
     __shared__ __align__(16) float As[2][BK][A_LD];
-    __shared__ __align__(16) float Bs[2][BK][B_LD];
+    __shared__ __align__(16) float Bs[2][BK][BLD];
+
+    const long long lda = EX ? ex.lda : K, ldb = EX ? ex.ldb : N, ldc = EX ? ex.ldc : N;
+    if (EX) {
+        A += (long long)blockIdx.y * ex.sa;
+        B += (long long)blockIdx.y * ex.sb;
+        C += (long long)blockIdx.y * ex.sc;
+    }
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -84,43 +111,54 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
     raster(pid, (M + BM - 1) / BM, (N + BN - 1) / BN, tm, tn);
     const int m0 = tm * BM + (MT == BM ? 0 : (int)(blockIdx.x & 1) * MT), n0 = tn * BN;
 
-    // Global -> register staging.  A: 128 rows x QA quads of k; B: BK k-rows x
-    // 32 quads of n; each thread moves LA quads of A and LB quads of B.
+    // Global -> register staging: LA quads of A and LB quads of B per thread.
+    // A [M,K]: MT rows x QA quads of k.  A stored [K,M] (TA): BK k-rows x MT/4
+    // quads of m.  B [K,N]: BK k-rows x 32 quads of n.  B stored [N,K] (TB): BN
+    // rows x QA quads of k.
     constexpr int QA = BK / 4;
     constexpr int LA = MT * QA / THREADS, LB = BK * (BN / 4) / THREADS;
     static_assert(LA >= 1 && LB >= 1 && MT * QA % THREADS == 0, "tile/thread mapping");
+    static_assert(BK * (MT / 4) == LA * THREADS && BN * QA == LB * THREADS, "transposed mappings");
     float ra[LA][4], rb[LB][4];
     auto load_tile = [&](int k0) {
 #pragma unroll
         for (int i = 0; i < LA; ++i) {
             const int idx = tid + i * THREADS;
-            const int row = idx / QA, kq = (idx % QA) * 4;
-            const int gm = m0 + row, gk = k0 + kq;
+            // (gm, gk) of the quad's first element; the quad runs along k, or
+            // along m when A is stored [K,M].
+            const int gm = TA ? m0 + (idx % (MT / 4)) * 4 : m0 + idx / QA;
+            const int gk = TA ? k0 + idx / (MT / 4) : k0 + (idx % QA) * 4;
+            const size_t off = TA ? (size_t)gk * lda + gm : (size_t)gm * lda + gk;
             if (VEC) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (gm < M && gk < K)
-                    v = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gm * K + gk));
+                if (gm < M && gk < K) v = __ldg(reinterpret_cast<const float4 *>(A + off));
                 ra[i][0] = v.x; ra[i][1] = v.y; ra[i][2] = v.z; ra[i][3] = v.w;
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    ra[i][j] = (gm < M && gk + j < K) ? to_f32(A[(size_t)gm * K + gk + j]) : 0.f;
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = TA ? (gm + j < M && gk < K) : (gm < M && gk + j < K);
+                    ra[i][j] = in ? to_f32(A[off + j]) : 0.f;
+                }
             }
         }
 #pragma unroll
         for (int i = 0; i < LB; ++i) {
             const int idx = tid + i * THREADS;
-            const int kr = idx >> 5, nq = (idx & 31) * 4;
-            const int gk = k0 + kr, gn = n0 + nq;
+            // (gk, gn) of the quad's first element; the quad runs along n, or
+            // along k when B is stored [N,K].
+            const int gk = TB ? k0 + (idx % QA) * 4 : k0 + (idx >> 5);
+            const int gn = TB ? n0 + idx / QA : n0 + (idx & 31) * 4;
+            const size_t off = TB ? (size_t)gn * ldb + gk : (size_t)gk * ldb + gn;
             if (VEC) {
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (gk < K && gn < N)
-                    v = __ldg(reinterpret_cast<const float4 *>(B + (size_t)gk * N + gn));
+                if (gk < K && gn < N) v = __ldg(reinterpret_cast<const float4 *>(B + off));
                 rb[i][0] = v.x; rb[i][1] = v.y; rb[i][2] = v.z; rb[i][3] = v.w;
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    rb[i][j] = (gk < K && gn + j < N) ? to_f32(B[(size_t)gk * N + gn + j]) : 0.f;
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = TB ? (gk + j < K && gn < N) : (gk < K && gn + j < N);
+                    rb[i][j] = in ? to_f32(B[off + j]) : 0.f;
+                }
             }
         }
     };
@@ -128,16 +166,26 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 #pragma unroll
         for (int i = 0; i < LA; ++i) {
             const int idx = tid + i * THREADS;
-            const int row = idx / QA, kq = (idx % QA) * 4;
+            if (TA) {
+                const int kr = idx / (MT / 4), mq = (idx % (MT / 4)) * 4;
+                *reinterpret_cast<float4 *>(&As[buf][kr][mq]) = make_float4(ra[i][0], ra[i][1], ra[i][2], ra[i][3]);
+            } else {
+                const int row = idx / QA, kq = (idx % QA) * 4;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) As[buf][kq + j][row] = ra[i][j];
+                for (int j = 0; j < 4; ++j) As[buf][kq + j][row] = ra[i][j];
+            }
         }
 #pragma unroll
         for (int i = 0; i < LB; ++i) {
             const int idx = tid + i * THREADS;
-            const int kr = idx >> 5, nq = (idx & 31) * 4;
-            *reinterpret_cast<float4 *>(&Bs[buf][kr][nq]) =
-                make_float4(rb[i][0], rb[i][1], rb[i][2], rb[i][3]);
+            if (TB) {
+                const int col = idx / QA, kq = (idx % QA) * 4;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) Bs[buf][kq + j][col] = rb[i][j];
+            } else {
+                const int kr = idx >> 5, nq = (idx & 31) * 4;
+                *reinterpret_cast<float4 *>(&Bs[buf][kr][nq]) = make_float4(rb[i][0], rb[i][1], rb[i][2], rb[i][3]);
+            }
         }
     };
 
@@ -180,7 +228,9 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
         __syncthreads();
     }
 
-    // Epilogue: each thread writes its 4*RG rows x (2 x 4) columns.
+    // Epilogue: each thread writes its 4*RG rows x (2 x 4) columns; the general
+    // form scales by alpha and, when beta != 0, adds beta times the old C.
+    const bool use_beta = EX && ex.beta != 0.0f;
 #pragma unroll
     for (int i = 0; i < 4 * RG; ++i) {
         const int gm = m0 + a_off + 16 * (i >> 2) + (i & 3);
@@ -188,14 +238,27 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int gn = n0 + b_off + h * 32;
-            TOut *dst = C + (size_t)gm * N + gn;
+            TOut *dst = C + (size_t)gm * ldc + gn;
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = EX ? ex.alpha * acc[i][4 * h + j] : acc[i][4 * h + j];
             if (VEC && gn + 3 < N) {
-                *reinterpret_cast<float4 *>(dst) =
-                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+                if (use_beta) {
+                    const float4 o = *reinterpret_cast<const float4 *>(dst);
+                    v[0] = fmaf(ex.beta, o.x, v[0]);
+                    v[1] = fmaf(ex.beta, o.y, v[1]);
+                    v[2] = fmaf(ex.beta, o.z, v[2]);
+                    v[3] = fmaf(ex.beta, o.w, v[3]);
+                }
+                *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (gn + j < N) dst[j] = from_f32<TOut>(acc[i][4 * h + j]);
+                for (int j = 0; j < 4; ++j) {
+                    if (gn + j < N) {
+                        const float w = use_beta ? fmaf(ex.beta, to_f32(dst[j]), v[j]) : v[j];
+                        dst[j] = from_f32<TOut>(w);
+                    }
+                }
             }
         }
     }
@@ -226,17 +289,56 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     const long long whole = tiles - split;
     if (whole > 0) {
         simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 128><<<(unsigned)whole, THREADS, 0, s>>>(
-            A, B, C, p.M, p.N, p.K, 0);
+            A, B, C, p.M, p.N, p.K, 0, SimtEx{});
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (split > 0) {
         simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 64><<<(unsigned)(2 * split), THREADS, 0, s>>>(
-            A, B, C, p.M, p.N, p.K, (int)whole);
+            A, B, C, p.M, p.N, p.K, (int)whole, SimtEx{});
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// The general form: one launch per chunk of at most 65535 batch entries
+// (blockIdx.y), whole 128 x 128 tiles.
+template <typename TIn, bool VEC, bool TA, bool TB>
+cudaError_t launch_ex_typed(const ProblemEx &p, cudaStream_t s) {
+    const long long tiles = (long long)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const SimtEx ex = {p.lda, p.ldb, p.ldc, p.sa, p.sb, p.sc, p.alpha, p.beta};
+    for (long long b0 = 0; b0 < p.batch; b0 += 65535) {
+        const long long nb = std::min<long long>(65535, p.batch - b0);
+        const TIn *A = static_cast<const TIn *>(p.A) + b0 * p.sa;
+        const TIn *B = static_cast<const TIn *>(p.B) + b0 * p.sb;
+        TIn *C = static_cast<TIn *>(p.C) + b0 * p.sc;
+        simt_gemm_kernel<TIn, TIn, VEC, SIMT_BK, SIMT_MINB, 128, true, TA, TB>
+            <<<dim3((unsigned)tiles, (unsigned)nb, 1), THREADS, 0, s>>>(A, B, C, p.M, p.N, p.K, 0, ex);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <typename TIn, bool VEC>
+cudaError_t launch_ex_ops(const ProblemEx &p, cudaStream_t s) {
+    if (p.a_t) return p.b_t ? launch_ex_typed<TIn, VEC, true, true>(p, s) : launch_ex_typed<TIn, VEC, true, false>(p, s);
+    return p.b_t ? launch_ex_typed<TIn, VEC, false, true>(p, s) : launch_ex_typed<TIn, VEC, false, false>(p, s);
+}
+
+bool aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
+
+// float4 loads and stores: every base 16-byte aligned, every leading dimension
+// and used batch stride a multiple of 4, and the contiguous extent of each
+// operand a multiple of 4 (a quad is then wholly inside or outside).
+bool ex_vec_ok(const ProblemEx &p) {
+    if (p.elt != Elt::F32) return false;
+    if (!aligned16(p.A) || !aligned16(p.B) || !aligned16(p.C)) return false;
+    if (p.lda % 4 || p.ldb % 4 || p.ldc % 4 || p.sa % 4 || p.sb % 4 || p.sc % 4) return false;
+    if ((p.a_t ? p.M : p.K) % 4 || (p.b_t ? p.K : p.N) % 4) return false;
+    return true;
 }
 
 }  // namespace
@@ -250,6 +352,20 @@ cudaError_t launch_simt(const Problem &p, bool vec4, int num_sms, cudaStream_t s
         return launch_typed<__half, __half, false>(p, num_sms, s);
     case Elt::BF16:
         return launch_typed<__nv_bfloat16, __nv_bfloat16, false>(p, num_sms, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool simt_ex_vec(const ProblemEx &p) { return ex_vec_ok(p); }
+
+cudaError_t launch_simt_ex(const ProblemEx &p, cudaStream_t s) {
+    switch (p.elt) {
+    case Elt::F32:
+        return ex_vec_ok(p) ? launch_ex_ops<float, true>(p, s) : launch_ex_ops<float, false>(p, s);
+    case Elt::F16:
+        return launch_ex_ops<__half, false>(p, s);
+    case Elt::BF16:
+        return launch_ex_ops<__nv_bfloat16, false>(p, s);
     }
     return cudaErrorInvalidValue;
 }

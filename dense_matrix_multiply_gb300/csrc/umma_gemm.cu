@@ -298,13 +298,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor for kind::f16: FP32 accumulator, A and B of the same
-// 16-bit type (0 = f16, 1 = bf16), A K-major, B MN-major, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m = BM, uint32_t n = BN) {
-    return (1u << 4)              // D: FP32
-           | (ab_format << 7)     // A type
-           | (ab_format << 10)    // B type
-           | (0u << 15)           // A K-major
-           | (1u << 16)           // B MN-major
+// 16-bit type (0 = f16, 1 = bf16); by default A K-major, B MN-major, M = 128,
+// N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m = BM, uint32_t n = BN,
+                                                  bool a_mn = false, bool b_mn = true) {
+    return (1u << 4)                      // D: FP32
+           | (ab_format << 7)             // A type
+           | (ab_format << 10)            // B type
+           | ((a_mn ? 1u : 0u) << 15)     // A major: 0 = K, 1 = MN
+           | ((b_mn ? 1u : 0u) << 16)     // B major
            | ((n >> 3) << 17)     // N / 8
            | ((m >> 4) << 24);    // M / 16
 }
@@ -594,13 +596,13 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ CTA pairs
-// The same product on 256 x 256 tiles computed by a cluster of two CTAs on
-// two SMs (tcgen05 cta_group::2).  CTA r of the pair holds rows r*128..+127 of
-// the A tile and columns r*128..+127 of the B tile in its own shared memory;
-// the leader's (rank 0) single MMA thread issues M=256, N=256, K=16 steps
-// that read both CTAs' shared memory and write each CTA's 128 accumulator
-// rows into that CTA's tensor memory.  Per CTA a stage is 32 KiB (half the B
-// bytes of the single-CTA tile), so six stages fit.
+// The product on 256 x 256 tiles computed by a cluster of two CTAs on two SMs
+// (tcgen05 cta_group::2).  CTA r of the pair holds rows r*128..+127 of the A
+// tile and columns r*128..+127 of the B tile in its own shared memory; the
+// leader's (rank 0) single MMA thread issues M=256, N=256, K=16 steps that
+// read both CTAs' shared memory and write each CTA's 128 accumulator rows into
+// that CTA's tensor memory.  Per CTA a stage is 32 KiB (half the B bytes of
+// the single-CTA tile), so six stages fit beside the epilogue's staging boxes.
 //   * Both producers load their halves; every load completes on the LEADER's
 //     full[s] (the leader arms it with the bytes of both CTAs).
 //   * The leader's commit after a stage arrives on empty[s] of both CTAs
@@ -608,47 +610,106 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 //   * acc_full[b] of both CTAs is committed the same way; each CTA's 128
 //     epilogue threads read their own tensor memory and arrive on the
 //     leader's acc_empty[b] (256 arrivals).
+//   * The epilogue stages each warp's 32 x 64 output boxes in 128-byte-
+//     swizzled shared memory and writes them with TMA stores (full-line writes,
+//     clipped at the matrix edge by the tensor map).
 // No TMA multicast is used: each CTA fetches only its own operand halves.
+//
+// The kernel also computes the general form ("SGEMM measured and the three
+// ledgers", section 2, the library call with operation flags and leading
+// dimensions; section 3, kernel K1, alpha * acc + beta * C):
+//     C_b = alpha * op(A_b) * op(B_b) + beta * C_b,   b < batch,
+// row-major, with any leading dimensions and batch strides that TMA can
+// describe.  All tensor maps are 3-D (inner, outer, batch).  op(A) = A^T (A
+// stored [K, M]) makes the A tile MN-major: two 64 x 64 boxes per CTA and
+// stage, described like the MN-major B tile.  op(B) = B^T (B stored [N, K])
+// makes the B tile K-major: one 64 x 128 box per CTA and stage, described like
+// the K-major A tile.  The instruction descriptor's major bits follow.
 namespace pairk {
 constexpr int PBM = 256, PBN = 256;
 constexpr int P_A_STAGE = 128 * BK * 2;                        // 16 KiB per CTA
-constexpr int P_B_STAGE = 128 * BK * 2;                        // 16 KiB per CTA (two 64-column boxes)
+constexpr int P_B_STAGE = 128 * BK * 2;                        // 16 KiB per CTA
+constexpr int P_BOX64 = 64 * BK * 2;                           // one 64 x 64 box: 8 KiB
 constexpr uint32_t P_STAGE_TX = 2u * (P_A_STAGE + P_B_STAGE);  // bytes per stage, both CTAs
 constexpr int P_STG_BOX = 32 * 64 * 2;                         // one 32-row x 64-column output box
 constexpr int P_GROUP_M = 8;                                   // pair tiles per raster group
-// Shared memory: NST operand stages, then (TMA-store epilogue) two staging
-// boxes per epilogue warp, then the barriers.
+constexpr int P_STAGES = 6;
+// Shared memory: the operand stages, two staging boxes per epilogue warp, the
+// barriers.
 __host__ __device__ constexpr int smem_tiles(int nst) { return nst * (P_A_STAGE + P_B_STAGE); }
-__host__ __device__ constexpr int smem_staging(bool tma_store) { return tma_store ? 4 * 2 * P_STG_BOX : 0; }
-__host__ __device__ constexpr int smem_bytes(int nst, bool tma_store) {
-    return 1024 + smem_tiles(nst) + smem_staging(tma_store) + 256;
-}
-static_assert(smem_bytes(7, false) <= 232448 && smem_bytes(6, true) <= 232448, "shared memory budget");
+constexpr int SMEM_STAGING = 4 * 2 * P_STG_BOX;
+__host__ __device__ constexpr int smem_bytes(int nst) { return 1024 + smem_tiles(nst) + SMEM_STAGING + 256; }
+static_assert(smem_bytes(P_STAGES) <= 232448, "shared memory budget");
 }  // namespace pairk
 
-// bn: the tile's N extent, a multiple of 32 in [128, 256], chosen per problem
+// Scalar arguments of the pair kernel.
+struct PairArgs {
+    void *C;                  // C (read only when beta != 0; written through tmC)
+    long long ldc, stride_c;  // elements
+    int M, N, K, batch;
+    int bn;                   // the tile's N extent (128, 192 or 256)
+    int a_t;                  // A stored [K, M] (M contiguous) instead of [M, K]
+    int b_t;                  // B stored [N, K] (K contiguous) instead of [K, N]
+    int a_bcast, b_bcast;     // batch stride 0: every b reads matrix 0
+    float alpha, beta;
+    int *status;
+};
+
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
+                                                 int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&o)[8], const __nv_bfloat16 *) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&o)[8], const __half *) {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(h[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float load1(const __half *p) { return __half2float(*p); }
+
+// bn: the tile's N extent, a multiple of 64 in [128, 256], chosen per problem
 // to fill the last wave (each CTA still loads 128 columns of B per stage and
 // the MMA reads bn/2 of them; accumulator buffers stay 256 columns apart).
-// PSTAGES: operand stages.  TMA_ST: the epilogue stages each warp's 32 x 64
-// output boxes in 128-byte-swizzled shared memory and writes them with TMA
-// stores (full-line writes) instead of per-thread 16-byte stores; bn must then
-// be a multiple of 64.
 // DUAL (the FFN gate/up projection, "Chapter 5 Operators and Runtime",
-// section 5.3.1): two weight matrices, tmB = W_g and tmB2 = W_u.  A tile is
-// 256 x 128 of Z.  Per K step CTA r loads columns [64r, 64r + 64) of the tile
-// from W_g into its first B box and the same columns of W_u into its second,
-// so ONE N = 256 MMA (each CTA supplying 128 B columns) yields G and U side by
-// side: accumulator columns 128r + [0, 64) hold G and 128r + [64, 128) hold U
-// for Z columns 64r + [0, 64).  The epilogue keeps the unfused chain's
-// rounding points: G and U rounded to the output type, T = round(SiLU(G)),
-// Z = round(T * U).  G, U and T never leave the SM.
-template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool TMA_ST, bool DUAL = false>
+// section 5.3.1): two weight matrices, tmB = W_g and tmB2 = W_u, both stored
+// [K, N].  A tile is 256 x 128 of Z.  Per K step CTA r loads columns
+// [64r, 64r + 64) of the tile from W_g into its first B box and the same
+// columns of W_u into its second, so ONE N = 256 MMA (each CTA supplying 128 B
+// columns) yields G and U side by side: accumulator columns 128r + [0, 64)
+// hold G and 128r + [64, 128) hold U for Z columns 64r + [0, 64).  The
+// epilogue keeps the unfused chain's rounding points: G and U rounded to the
+// output type, T = round(SiLU(G)), Z = round(T * U).  G, U and T never leave
+// the SM.
+template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool DUAL = false>
 __global__ void __launch_bounds__(THREADS, 1)
 umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmC, T *__restrict__ C, int M, int N, int K, int *status,
-                 int bn, const __grid_constant__ CUtensorMap tmB2)
+                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
+                 const PairArgs args)
 {
-    static_assert(!DUAL || TMA_ST, "the fused gate/up epilogue writes through TMA stores");
     using namespace pairk;
     using PBars = BarsT<PSTAGES>;
     static_assert(sizeof(PBars) <= 256, "barrier block");
@@ -658,15 +719,18 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint8_t *a_tiles = smem;
     uint8_t *b_tiles = smem + PSTAGES * P_A_STAGE;
     uint8_t *staging = smem + smem_tiles(PSTAGES);
-    PBars *bars = reinterpret_cast<PBars *>(smem + smem_tiles(PSTAGES) + smem_staging(TMA_ST));
+    PBars *bars = reinterpret_cast<PBars *>(smem + smem_tiles(PSTAGES) + SMEM_STAGING);
     volatile int *abort_flag = &bars->abort;
 
+    const int M = args.M, N = args.N, K = args.K, bn = args.bn;
+    int *status = args.status;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int cluster = (int)cluster_id_x(), nclusters = (int)cluster_count_x();
     const int tiles_m = (M + PBM - 1) / PBM, tiles_n = (N + bn - 1) / bn;
-    const int num_tiles = tiles_m * tiles_n;
+    const int tiles_per_batch = tiles_m * tiles_n;
+    const int num_tiles = tiles_per_batch * args.batch;
     const int num_kb = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -683,7 +747,8 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (TMA_ST) tma_prefetch_desc(&tmC);
+        tma_prefetch_desc(&tmC);
+        if (DUAL) tma_prefetch_desc(&tmB2);
     }
     if (warp == 1) {
         tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
@@ -694,12 +759,15 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
 
-    auto coords = [&](int t, int &tm, int &tn) {
+    // Tile t -> (batch index, row tile, column tile); M-grouped raster inside a batch.
+    auto coords = [&](int t, int &bt, int &tm, int &tn) {
+        bt = t / tiles_per_batch;
+        const int r0 = t - bt * tiles_per_batch;
         const int per_group = P_GROUP_M * tiles_n;
-        const int group = t / per_group;
+        const int group = r0 / per_group;
         const int first_m = group * P_GROUP_M;
         const int gsize = min(tiles_m - first_m, P_GROUP_M);
-        const int r = t - group * per_group;
+        const int r = r0 - group * per_group;
         tm = first_m + r % gsize;
         tn = r / gsize;
     };
@@ -711,8 +779,9 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         long long issued = 0;
         bool ok = true;
         for (int t = cluster; t < num_tiles && ok; t += nclusters) {
-            int tm, tn;
-            coords(t, tm, tn);
+            int bt, tm, tn;
+            coords(t, bt, tm, tn);
+            const int za = args.a_bcast ? 0 : bt, zb = args.b_bcast ? 0 : bt;
             const int row0 = tm * PBM + (int)rank * 128;
             const int col0 = tn * bn + (int)rank * (bn >> 1);
             for (int kb = 0; kb < num_kb; ++kb) {
@@ -721,14 +790,22 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (leader) mbar_arrive_expect_tx(&bars->full[stage], P_STAGE_TX);
                 uint8_t *a_dst = a_tiles + stage * P_A_STAGE;
                 uint8_t *b_dst = b_tiles + stage * P_B_STAGE;
-                tma_load_2d_pair(a_dst, &tmA, full_leader, kb * BK, row0);
+                const int k0 = kb * BK;
+                if (!args.a_t) {
+                    tma_load_3d_pair(a_dst, &tmA, full_leader, k0, row0, za);
+                } else {
+                    tma_load_3d_pair(a_dst, &tmA, full_leader, row0, k0, za);
+                    tma_load_3d_pair(a_dst + P_BOX64, &tmA, full_leader, row0 + 64, k0, za);
+                }
                 if (DUAL) {
                     // same 64 columns of W_g and of W_u
-                    tma_load_2d_pair(b_dst, &tmB, full_leader, col0, kb * BK);
-                    tma_load_2d_pair(b_dst + B_BOX, &tmB2, full_leader, col0, kb * BK);
+                    tma_load_3d_pair(b_dst, &tmB, full_leader, col0, k0, 0);
+                    tma_load_3d_pair(b_dst + P_BOX64, &tmB2, full_leader, col0, k0, 0);
+                } else if (!args.b_t) {
+                    tma_load_3d_pair(b_dst, &tmB, full_leader, col0, k0, zb);
+                    tma_load_3d_pair(b_dst + P_BOX64, &tmB, full_leader, col0 + 64, k0, zb);
                 } else {
-                    tma_load_2d_pair(b_dst, &tmB, full_leader, col0, kb * BK);
-                    tma_load_2d_pair(b_dst + B_BOX, &tmB, full_leader, col0 + 64, kb * BK);
+                    tma_load_3d_pair(b_dst, &tmB, full_leader, k0, col0, zb);
                 }
                 ++issued;
                 if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
@@ -756,12 +833,21 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer (leader)
-        const uint32_t idesc = make_idesc(AB_FORMAT, PBM, DUAL ? 256u : (uint32_t)bn);
+        const bool a_mn = args.a_t != 0, b_mn = DUAL || args.b_t == 0;
+        const uint32_t idesc = make_idesc(AB_FORMAT, PBM, DUAL ? 256u : (uint32_t)bn, a_mn, b_mn);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
         bool ok = true;
-        const uint32_t a_base = smem_u32(a_tiles), b_base = smem_u32(b_tiles);
+        // Descriptors of stage 0, K step 0; a stage or K step only moves the
+        // start address (bits 0-13, in 16-byte units).  K-major tile: a K step
+        // of 16 elements is 32 bytes inside the 128-byte swizzle row, 8-row
+        // groups are 1024 bytes apart.  MN-major tile: a K step is 16 rows of
+        // 128 bytes (2048 bytes), 64-element MN chunks (boxes) are P_BOX64
+        // bytes apart.
+        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(a_tiles), a_mn ? P_BOX64 : 16, 1024);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_tiles), b_mn ? P_BOX64 : 16, 1024);
+        const uint32_t a_kstep = (a_mn ? 2048u : 32u) >> 4, b_kstep = (b_mn ? 2048u : 32u) >> 4;
         for (int t = cluster; t < num_tiles && ok; t += nclusters, ++it) {
             const int buf = it & 1;
             const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
@@ -771,14 +857,11 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!mbar_wait_cluster(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a_addr = a_base + stage * P_A_STAGE;
-                const uint32_t b_addr = b_base + stage * P_B_STAGE;
+                const uint64_t ad = a_desc0 + (uint64_t)((stage * P_A_STAGE) >> 4);
+                const uint64_t bd = b_desc0 + (uint64_t)((stage * P_B_STAGE) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < BK / UMMA_K; ++ks) {
-                    const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(b_addr + ks * 2048, B_BOX, 1024);
-                    umma_pair(d_tmem, ad, bd, idesc, (kb | ks) != 0);
-                }
+                for (int ks = 0; ks < BK / UMMA_K; ++ks)
+                    umma_pair(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, (kb | ks) != 0);
                 umma_commit_pair_multicast(&bars->empty[stage], 0x3);
                 if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
             }
@@ -794,24 +877,24 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
-        const int row_in_tile = (int)rank * 128 + quarter * 32 + lane;
         uint8_t *my_stg = staging + quarter * 2 * P_STG_BOX;  // this warp's two staging boxes
+        const float alpha = args.alpha, beta = args.beta;
+        const bool use_beta = !DUAL && beta != 0.0f;
         int sb = 0;
         int it = 0;
         bool ok = true;
         for (int t = cluster; t < num_tiles; t += nclusters, ++it) {
-            int tm, tn;
-            coords(t, tm, tn);
+            int bt, tm, tn;
+            coords(t, bt, tm, tn);
             const int buf = it & 1;
             const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
             if (!mbar_wait_cluster(&bars->acc_full[buf], acc_par, abort_flag, true)) { ok = false; break; }
             tc_fence_after();
             __syncwarp();
-            const int row = tm * PBM + row_in_tile;
             const int n0 = tn * bn;
+            const int box_row0 = tm * PBM + (int)rank * 128 + quarter * 32;  // warp-uniform
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * PBN);
             if constexpr (DUAL) {
-                const int box_row0 = tm * PBM + (int)rank * 128 + quarter * 32;  // warp-uniform
 #pragma unroll 1
                 for (int g = 0; g < 2; ++g) {
                     const int c0 = n0 + g * 64;
@@ -842,18 +925,16 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
-                    if (lane == 0 && box_row0 < M) {
-                        asm volatile(
-                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                                reinterpret_cast<uint64_t>(&tmC)),
-                            "r"(c0), "r"(box_row0), "r"(smem_u32(my_stg + sb * P_STG_BOX))
-                            : "memory");
-                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    }
+                    if (lane == 0 && box_row0 < M) tma_store_3d(&tmC, my_stg + sb * P_STG_BOX, c0, box_row0, 0);
                     sb ^= 1;
                 }
-            } else if constexpr (TMA_ST) {
-                const int box_row0 = tm * PBM + (int)rank * 128 + quarter * 32;  // warp-uniform
+            } else {
+                const int row = box_row0 + lane;
+                // This thread's row of C in batch bt, read only when beta != 0.
+                const T *c_old = (use_beta && row < M)
+                                     ? static_cast<const T *>(args.C) + (long long)bt * args.stride_c +
+                                           (long long)row * args.ldc
+                                     : nullptr;
 #pragma unroll 1
                 for (int g = 0; g < (bn >> 6); ++g) {
                     const int c0 = n0 + g * 64;
@@ -861,6 +942,22 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     uint32_t r0[32], r1[32];
                     tmem_ld_32cols(t_row + (uint32_t)(g * 64), r0);
                     tmem_ld_32cols(t_row + (uint32_t)(g * 64 + 32), r1);
+                    uint4 old[8];
+                    if (use_beta) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int cc = c0 + 8 * c;
+                            old[c] = make_uint4(0u, 0u, 0u, 0u);
+                            if (c_old != nullptr && cc + 8 <= N) {
+                                old[c] = *reinterpret_cast<const uint4 *>(c_old + cc);
+                            } else if (c_old != nullptr) {
+                                T tmp[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) tmp[e] = cc + e < N ? c_old[cc + e] : T(0.0f);
+                                memcpy(&old[c], tmp, 16);
+                            }
+                        }
+                    }
                     tmem_ld_wait();
                     // The store issued two boxes ago read this staging box.
                     if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -869,58 +966,32 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const uint32_t *src = c < 4 ? &r0[8 * c] : &r1[8 * (c - 4)];
-                        uint4 v;
-                        v.x = pack2(__uint_as_float(src[0]), __uint_as_float(src[1]), (T *)nullptr);
-                        v.y = pack2(__uint_as_float(src[2]), __uint_as_float(src[3]), (T *)nullptr);
-                        v.z = pack2(__uint_as_float(src[4]), __uint_as_float(src[5]), (T *)nullptr);
-                        v.w = pack2(__uint_as_float(src[6]), __uint_as_float(src[7]), (T *)nullptr);
-                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (lane & 7)) << 4)) = v;
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = alpha * __uint_as_float(src[e]);
+                        if (use_beta) {
+                            float o[8];
+                            unpack8(old[c], o, (const T *)nullptr);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = fmaf(beta, o[e], v[e]);
+                        }
+                        uint4 w;
+                        w.x = pack2(v[0], v[1], (T *)nullptr);
+                        w.y = pack2(v[2], v[3], (T *)nullptr);
+                        w.z = pack2(v[4], v[5], (T *)nullptr);
+                        w.w = pack2(v[6], v[7], (T *)nullptr);
+                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (lane & 7)) << 4)) = w;
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
-                    if (lane == 0 && box_row0 < M) {
-                        asm volatile(
-                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                                reinterpret_cast<uint64_t>(&tmC)),
-                            "r"(c0), "r"(box_row0), "r"(smem_u32(my_stg + sb * P_STG_BOX))
-                            : "memory");
-                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    }
+                    if (lane == 0 && box_row0 < M) tma_store_3d(&tmC, my_stg + sb * P_STG_BOX, c0, box_row0, bt);
                     sb ^= 1;
-                }
-            } else {
-                T *crow = C + (size_t)row * N;
-#pragma unroll 1
-                for (int chunk = 0; chunk < (bn >> 5); ++chunk) {
-                    const int c0 = n0 + chunk * 32;
-                    if (c0 >= N) break;  // warp-uniform
-                    uint32_t r[32];
-                    tmem_ld_32cols(t_row + (uint32_t)(chunk * 32), r);
-                    tmem_ld_wait();
-                    if (row < M) {
-                        if (c0 + 32 <= N) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(crow + c0);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                uint4 v;
-                                v.x = pack2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]), (T *)nullptr);
-                                v.y = pack2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]), (T *)nullptr);
-                                v.z = pack2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]), (T *)nullptr);
-                                v.w = pack2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]), (T *)nullptr);
-                                dst[q] = v;
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (c0 + j < N) store1(crow + c0 + j, __uint_as_float(r[j]));
-                        }
-                    }
                 }
             }
             tc_fence_before();
             mbar_arrive_cluster(map_to_rank(&bars->acc_empty[buf], 0));
         }
-        if (TMA_ST && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         if (!ok) {
             atomicOr(status, ST_EPILOGUE);
             *abort_flag = 1;
@@ -1000,13 +1071,23 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     return cudaGetLastError();
 }
 
-// Pair-kernel configuration: 128-byte TMA-store epilogue with six operand
-// stages (the staging boxes take the seventh stage's shared memory).
-#ifndef PAIR_TMA_STORE
-#define PAIR_TMA_STORE 1
-#endif
-constexpr bool kPairTmaStore = PAIR_TMA_STORE != 0;
-constexpr int kPairStages = kPairTmaStore ? 6 : 7;
+// 3-D tensor map of `batch` matrices of [outer, inner] 16-bit elements: row
+// stride ld elements, matrix stride `stride` elements; box [box_outer,
+// box_inner], 128-byte swizzle, zero fill out of bounds.  batch == 1 ignores
+// stride.
+bool make_map3(CUtensorMap *map, const void *base, CUtensorMapDataType dt, long long inner, long long outer,
+               long long batch, long long ld, long long stride, int box_inner, int box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    if (batch <= 1) stride = ld * outer;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)(batch > 1 ? batch : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)stride * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // Largest number of co-resident two-CTA clusters of the pair kernel, per device
 // (0: the pair kernel cannot be launched).
@@ -1015,8 +1096,8 @@ int pair_clusters_max(int dev) {
     static std::atomic<int> cached[64];
     static std::once_flag once[64];
     std::call_once(once[dev & 63], [&] {
-        auto kern = umma_pair_kernel<T, F, kPairStages, kPairTmaStore, DUAL>;
-        const int smem = pairk::smem_bytes(kPairStages, kPairTmaStore);
+        auto kern = umma_pair_kernel<T, F, pairk::P_STAGES, DUAL>;
+        const int smem = pairk::smem_bytes(pairk::P_STAGES);
         int n = 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess) {
@@ -1039,40 +1120,13 @@ int pair_clusters_max(int dev) {
     return cached[dev & 63].load();
 }
 
-// lda: row stride of A in elements (0: K).
-template <typename T, uint32_t F>
-cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, cudaStream_t s,
-                              long long lda = 0) {
-    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap ta, tb, tc;
-    if (!make_map(&ta, p.A, dt, p.M, p.K, 128, BK, lda)) return cudaErrorInvalidValue;
-    if (!make_map(&tb, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
-    if (kPairTmaStore) {
-        if (!make_map(&tc, p.C, dt, p.M, p.N, 32, 64)) return cudaErrorInvalidValue;
-    } else {
-        tc = tb;  // unused by the kernel
-    }
-    // N extent of a tile: the one of 256, 192, 128 (TMA-store boxes are 64
-    // columns wide) with the fewest waves of tiles over the clusters, widest on
-    // ties: per-tile time is set mostly by the operand feed, which does not
-    // shrink with the tile's N.
-    const long long tiles_m = (p.M + pairk::PBM - 1) / pairk::PBM;
-    int bn = 256;
-    long long best = -1;
-    const int step = kPairTmaStore ? 64 : 32;
-    for (int cand = 256; cand >= 128; cand -= step) {
-        const long long t = tiles_m * ((p.N + cand - 1) / cand);
-        const long long waves = (t + clusters_max - 1) / clusters_max;
-        const long long cost = waves * (cand > 224 ? cand : 224);
-        if (best < 0 || cost < best) { best = cost; bn = cand; }
-    }
-    const long long tiles = tiles_m * ((p.N + bn - 1) / bn);
-    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
+template <typename T, uint32_t F, bool DUAL>
+cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                            const CUtensorMap &tb2, const PairArgs &args, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pairk::smem_bytes(kPairStages, kPairTmaStore);
+    cfg.dynamicSmemBytes = pairk::smem_bytes(pairk::P_STAGES);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1081,8 +1135,55 @@ cudaError_t launch_pair_typed(const Problem &p, int clusters_max, int *status, c
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, kPairStages, kPairTmaStore>, ta, tb, tc,
-                              static_cast<T *>(p.C), p.M, p.N, p.K, status, bn, tb);
+    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL>, ta, tb, tc, tb2, args);
+}
+
+// The general problem on CTA pairs.  Returns cudaErrorNotSupported, before any
+// launch, when a tensor map cannot describe an operand.
+template <typename T, uint32_t F>
+cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status, cudaStream_t s) {
+    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const long long ba = p.sa == 0 ? 1 : p.batch, bb = p.sb == 0 ? 1 : p.batch;
+    CUtensorMap ta, tb, tc;
+    const bool ok_a = p.a_t ? make_map3(&ta, p.A, dt, p.M, p.K, ba, p.lda, p.sa, 64, BK)
+                            : make_map3(&ta, p.A, dt, p.K, p.M, ba, p.lda, p.sa, BK, 128);
+    const bool ok_b = p.b_t ? make_map3(&tb, p.B, dt, p.K, p.N, bb, p.ldb, p.sb, BK, 128)
+                            : make_map3(&tb, p.B, dt, p.N, p.K, bb, p.ldb, p.sb, 64, BK);
+    const bool ok_c = make_map3(&tc, p.C, dt, p.N, p.M, p.batch, p.ldc, p.sc, 64, 32);
+    if (!ok_a || !ok_b || !ok_c) return cudaErrorNotSupported;
+    // N extent of a tile: the one of 256, 192, 128 (TMA-store boxes are 64
+    // columns wide) with the fewest waves of tiles over the clusters, widest on
+    // ties: per-tile time is set mostly by the operand feed, which does not
+    // shrink with the tile's N.
+    const long long tiles_mb = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * p.batch;
+    int bn = 256;
+    long long best = -1;
+    for (int cand = 256; cand >= 128; cand -= 64) {
+        const long long t = tiles_mb * ((p.N + cand - 1) / cand);
+        const long long waves = (t + clusters_max - 1) / clusters_max;
+        const long long cost = waves * (cand > 224 ? cand : 224);
+        if (best < 0 || cost < best) { best = cost; bn = cand; }
+    }
+    const long long tiles = tiles_mb * ((p.N + bn - 1) / bn);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
+    PairArgs args = {};
+    args.C = p.C;
+    args.ldc = p.ldc;
+    args.stride_c = p.sc;
+    args.M = p.M;
+    args.N = p.N;
+    args.K = p.K;
+    args.batch = p.batch;
+    args.bn = bn;
+    args.a_t = p.a_t;
+    args.b_t = p.b_t;
+    args.a_bcast = p.sa == 0;
+    args.b_bcast = p.sb == 0;
+    args.alpha = p.alpha;
+    args.beta = p.beta;
+    args.status = status;
+    return launch_pair_cfg<T, F, false>(ta, tb, tc, tb, args, clusters, s);
 }
 
 // Z = SiLU(X W_g) * (X W_u): p.A = X [M,K], p.B = W_g [K,N], p.C = Z [M,N];
@@ -1092,28 +1193,45 @@ cudaError_t launch_pair_silu_mul_typed(const Problem &p, const void *w_u, int cl
                                        cudaStream_t s) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tg, tu, tc;
-    if (!make_map(&ta, p.A, dt, p.M, p.K, 128, BK)) return cudaErrorInvalidValue;
-    if (!make_map(&tg, p.B, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
-    if (!make_map(&tu, w_u, dt, p.K, p.N, BK, 64)) return cudaErrorInvalidValue;
-    if (!make_map(&tc, p.C, dt, p.M, p.N, 32, 64)) return cudaErrorInvalidValue;
+    if (!make_map3(&ta, p.A, dt, p.K, p.M, 1, p.K, 0, BK, 128)) return cudaErrorInvalidValue;
+    if (!make_map3(&tg, p.B, dt, p.N, p.K, 1, p.N, 0, 64, BK)) return cudaErrorInvalidValue;
+    if (!make_map3(&tu, w_u, dt, p.N, p.K, 1, p.N, 0, 64, BK)) return cudaErrorInvalidValue;
+    if (!make_map3(&tc, p.C, dt, p.N, p.M, 1, p.N, 0, 64, 32)) return cudaErrorInvalidValue;
     const int bn = 128;
     const long long tiles = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * ((p.N + bn - 1) / bn);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pairk::smem_bytes(kPairStages, kPairTmaStore);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, kPairStages, kPairTmaStore, true>, ta, tg, tc,
-                              static_cast<T *>(p.C), p.M, p.N, p.K, status, bn, tu);
+    PairArgs args = {};
+    args.C = p.C;
+    args.ldc = p.N;
+    args.M = p.M;
+    args.N = p.N;
+    args.K = p.K;
+    args.batch = 1;
+    args.bn = bn;
+    args.alpha = 1.0f;
+    args.status = status;
+    return launch_pair_cfg<T, F, true>(ta, tg, tc, tu, args, clusters, s);
+}
+
+// The tight problem of the plain entry points as a general one; lda: row
+// stride of A in elements (0: K).
+ProblemEx plain_ex(const Problem &p, long long lda = 0) {
+    ProblemEx q = {};
+    q.A = p.A;
+    q.B = p.B;
+    q.C = p.C;
+    q.M = p.M;
+    q.N = p.N;
+    q.K = p.K;
+    q.batch = 1;
+    q.lda = lda > 0 ? lda : p.K;
+    q.ldb = p.N;
+    q.ldc = p.N;
+    q.alpha = 1.0f;
+    q.beta = 0.0f;
+    q.elt = p.elt;
+    return q;
 }
 
 }  // namespace
@@ -1172,8 +1290,9 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
                 if (e == cudaSuccess) {
                     Problem q = p;
                     q.A = ap;
-                    e = p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(q, cmax, status, s, lda)
-                                           : launch_pair_typed<__half, 0>(q, cmax, status, s, lda);
+                    const ProblemEx qe = plain_ex(q, lda);
+                    e = p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(qe, cmax, status, s)
+                                           : launch_pair_typed<__half, 0>(qe, cmax, status, s);
                 }
                 const cudaError_t f = cudaFreeAsync(ap, s);
                 return e != cudaSuccess ? e : f;
@@ -1191,8 +1310,9 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
         const int cmax = p.elt == Elt::BF16 ? pair_clusters_max<__nv_bfloat16, 1>(dev)
                                             : pair_clusters_max<__half, 0>(dev);
         if (cmax > 0) {
-            return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(p, cmax, status, s)
-                                      : launch_pair_typed<__half, 0>(p, cmax, status, s);
+            const ProblemEx q = plain_ex(p);
+            return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(q, cmax, status, s)
+                                      : launch_pair_typed<__half, 0>(q, cmax, status, s);
         }
     }
     if (p.elt == Elt::BF16) return launch_typed<__nv_bfloat16, 1, false>(p, num_sms, status, s);
@@ -1239,7 +1359,7 @@ cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s) {
 }
 
 bool umma_silu_mul_supported(const Problem &p, const void *w_u) {
-    if (p.elt != Elt::BF16 || !kPairTmaStore) return false;
+    if (p.elt != Elt::BF16) return false;
     return aligned(p.A, 16) && aligned(p.B, 16) && aligned(w_u, 16) && aligned(p.C, 16) && (p.K % 8) == 0 &&
            (p.N % 8) == 0;
 }
@@ -1252,6 +1372,30 @@ cudaError_t launch_umma_silu_mul(const Problem &p, const void *w_u, int *status,
     const int cmax = pair_clusters_max<__nv_bfloat16, 1, true>(dev);
     if (cmax <= 0) return cudaErrorNotSupported;
     return launch_pair_silu_mul_typed<__nv_bfloat16, 1>(p, w_u, cmax, status, s);
+}
+
+bool umma_ex_supported(const ProblemEx &p) {
+    if (p.elt == Elt::F32) return false;
+    if (!aligned(p.A, 16) || !aligned(p.B, 16) || !aligned(p.C, 16)) return false;
+    if (p.lda % 8 || p.ldb % 8 || p.ldc % 8) return false;
+    if (p.batch > 1 && (p.sa % 8 || p.sb % 8 || p.sc % 8)) return false;
+    // TMA moves the contiguous dimension in 16-byte pieces: each stored
+    // matrix's contiguous extent must be a whole number of them, or a store
+    // would touch elements past the end of a row of C.
+    if ((p.a_t ? p.M : p.K) % 8 || (p.b_t ? p.K : p.N) % 8 || p.N % 8) return false;
+    return true;
+}
+
+cudaError_t launch_umma_ex(const ProblemEx &p, int *status, cudaStream_t s) {
+    if (!umma_ex_supported(p)) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int cmax = p.elt == Elt::BF16 ? pair_clusters_max<__nv_bfloat16, 1>(dev)
+                                        : pair_clusters_max<__half, 0>(dev);
+    if (cmax <= 0) return cudaErrorNotSupported;
+    return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(p, cmax, status, s)
+                              : launch_pair_typed<__half, 0>(p, cmax, status, s);
 }
 
 cudaError_t launch_umma_stall_test(const Problem &p, int num_sms, int *status, cudaStream_t s) {

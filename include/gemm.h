@@ -139,6 +139,57 @@ GEMM_API gemm_status_t gemm_bf16_rm_silu_mul(const uint16_t *X, const uint16_t *
 GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B, uint16_t *C,
                                             int M, int N, int K);
 
+/* General form ("SGEMM measured and the three ledgers", section 2: the
+ * library call with operation flags and leading dimensions, and the row- and
+ * column-major readings of the same bytes; section 3, kernel K1:
+ * alpha * acc + beta * C).  For b = 0 .. batch-1:
+ *
+ *     C_b <- alpha * op(A_b) * op(B_b) + beta * C_b
+ *
+ * op(X) is X (GEMM_OP_N) or its transpose (GEMM_OP_T); op(A) is M x K, op(B)
+ * is K x N, C is M x N.  dtype gives the element type of A, B and C (float, or
+ * IEEE half / bf16 bit patterns); alpha and beta are float.  The products are
+ * accumulated in FP32; alpha * acc + beta * c is formed in FP32 and rounded
+ * once to the output type.
+ *
+ * Storage.  A stored matrix of R x Cn elements with leading dimension ld holds
+ * element (r, c) at r*ld + c (GEMM_ROW_MAJOR) or r + c*ld (GEMM_COL_MAJOR).
+ * A is stored M x K for GEMM_OP_N and K x M for GEMM_OP_T; B is stored K x N or
+ * N x K; C is stored M x N.  Each leading dimension must be at least the stored
+ * matrix's contiguous extent (and at least 1).  Matrix b of A starts stride_a
+ * elements after matrix b-1 (likewise B and C); stride_a or stride_b may be 0
+ * (one matrix serves every b); stride_c must keep the C matrices apart when
+ * batch > 1.  Leading dimensions and strides are in elements, int64.
+ * All pointers are device pointers owned by the caller.
+ *
+ * Reads.  C is not read when beta == 0 (a NaN in C does not reach the result).
+ * A and B are not read when alpha == 0 or K == 0; C is then scaled by beta
+ * (or set to zero).
+ *
+ * Errors.  GEMM_ERR_INVALID_VALUE: an unknown enum value; a negative size or
+ * stride; a leading dimension below the contiguous extent; overlapping C
+ * matrices; a null pointer that would be read or written; sizes whose element
+ * span overflows; a forced kernel family that cannot run the problem
+ * ("simt" and "umma" are accepted here, the others are not).
+ * GEMM_ERR_ALIAS: C's span overlaps A's or B's span.  Otherwise as the entry
+ * points above.  M, N or batch == 0 is a no-op.
+ *
+ * Kernels.  16-bit problems whose A, B, C are 16-byte aligned and whose
+ * leading dimensions (and, for batch > 1, nonzero batch strides) and stored
+ * contiguous extents (K or M for A, N or K for B, N for C in row-major terms)
+ * are multiples of 8 elements run on the tensor-core CTA pairs; everything
+ * else, and every FP32 problem, on the SIMT kernel (float4 loads where
+ * alignment allows). */
+typedef enum gemm_dtype_t { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2 } gemm_dtype_t;
+typedef enum gemm_layout_t { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+typedef enum gemm_op_t { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
+
+GEMM_API gemm_status_t gemm_ex(gemm_dtype_t dtype, gemm_layout_t layout, gemm_op_t op_a, gemm_op_t op_b,
+                               int M, int N, int K, float alpha,
+                               const void *A, int64_t lda, int64_t stride_a,
+                               const void *B, int64_t ldb, int64_t stride_b,
+                               float beta, void *C, int64_t ldc, int64_t stride_c, int batch);
+
 /* Stream for the calling host thread's subsequent calls: a cudaStream_t passed
  * as void*.  NULL selects the legacy default stream.  The stream stays owned by
  * the caller and must outlive the calls issued on it. */

@@ -99,3 +99,32 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(g, "_lib", None)
     with pytest.raises(RuntimeError, match="CUDA extension missing"):
         g.load()
+
+
+def test_general_form_host_side_errors(built):
+    """gemm_ex rejects bad arguments before touching a device."""
+    lib = built
+    buf = ctypes.create_string_buffer(1 << 16)
+    p = ctypes.addressof(buf)
+    A, B, C = p, p + 16384, p + 32768
+
+    def ex(dtype=0, layout=0, oa=0, ob=0, M=4, N=4, K=4, alpha=1.0, a=A, lda=4, sa=0, b=B, ldb=4, sb=0,
+           beta=0.0, c=C, ldc=4, sc=16, batch=1):
+        return lib.gemm_ex(dtype, layout, oa, ob, M, N, K, alpha, a, lda, sa, b, ldb, sb, beta, c, ldc, sc, batch)
+
+    assert ex(dtype=3) == 1 and ex(layout=2) == 1 and ex(oa=2) == 1 and ex(ob=-1) == 1
+    assert ex(M=-1) == 1 and ex(K=-1) == 1 and ex(batch=-1) == 1 and ex(sa=-4) == 1
+    assert ex(lda=3) == 1                     # row-major A [4,4] needs lda >= 4
+    assert ex(M=6, oa=1, lda=5) == 1          # A stored [K,M] = [4,6] needs lda >= 6
+    assert ex(N=6, ob=1, ldb=3) == 1          # B stored [N,K] = [6,4] needs ldb >= 4
+    assert ex(ldc=3) == 1
+    assert ex(layout=1, M=6, lda=4) == 1      # column-major A [6,4] needs lda >= 6
+    assert ex(batch=2, sc=8) == 1             # the two C matrices would overlap
+    assert ex(c=None) == 1 and ex(a=None) == 1
+    assert ex(M=0) == 0 and lib.gemm_last_kernel() == b"noop"
+    assert ex(batch=0) == 0 and ex(N=0) == 0
+    assert ex(c=A + 8) == 2                   # C overlaps A
+    assert ex(b=C + 32, ldb=4) == 2           # C overlaps B
+    # B's third matrix (stride 4096 floats = 16384 bytes) starts exactly at C
+    assert ex(batch=3, sc=16, sb=4096, b=C - 2 * 16384) == 2
+    assert ex(lda=1 << 61, batch=1) == 1      # span overflows
