@@ -61,3 +61,22 @@ def wave_efficiency(tiles: int, slots: int) -> float:
     if tiles == 0:
         return 1.0
     return tiles / (math.ceil(tiles / slots) * slots)
+
+
+def fp8_rowscale_traffic(M: int, K: int, N: int, tile_n: int, in_elt: int = 2, q_elt: int = 1,
+                         w_elt: int = 1, out_elt: int = 2, tile_m: int = 128) -> dict:
+    """Bytes moved by a row-scaled FP8 projection when every output tile reads
+    its operands independently ("Chapter 5 Operators and Runtime", example 5-8).
+    Both schemes first read the whole input once to find each row's scale.
+    separate: write the FP8 input once, then every column block re-reads it.
+    fused: every column block re-reads the 16-bit input and quantises locally.
+    Both: every row block reads the whole weight matrix; the output is written
+    once."""
+    col_blocks = -(-N // tile_n)
+    row_blocks = -(-M // tile_m)
+    a_in, a_q = M * K * in_elt, M * K * q_elt
+    separate_in = a_in + a_q + col_blocks * a_q
+    fused_in = a_in + col_blocks * a_in
+    w_out = row_blocks * K * N * w_elt + M * N * out_elt
+    return {"separate_input": separate_in, "fused_input": fused_in, "weights_output": w_out,
+            "separate_total": separate_in + w_out, "fused_total": fused_in + w_out}

@@ -66,6 +66,12 @@ def _load():
             lib.oracle_gemm_ex.argtypes = [ctypes.c_int] * 4 + [i64, i64, i64, d,
                                            vp, i64, i64, vp, i64, i64, d, vp, i64, i64, i64,
                                            dp, dp, dp, dp]
+            lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+            lib.oracle_decode_e4m3.restype = ctypes.c_double
+            lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_encode_e4m3.restype = ctypes.c_uint8
+            lib.oracle_quantize_rows_e4m3.argtypes = [vp, i64, i64, vp, vp]
+            lib.oracle_gemm_e4m3_rowscale.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, dp, dp]
             lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
             lib.oracle_decode_f16.restype = ctypes.c_double
             lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
@@ -197,6 +203,53 @@ def gemm_ex(dtype: str, layout: str, op_a: str, op_b: str, M: int, N: int, K: in
     if rc:
         raise RuntimeError(f"oracle_gemm_ex failed ({rc})")
     return {k: v.reshape(batch, M, N) for k, v in out.items()}
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """The oracle's decoder of E4M3FN codes, as float64."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([lib.oracle_decode_e4m3(int(v)) for v in c], dtype=np.float64)
+
+
+def encode_e4m3(x) -> np.ndarray:
+    """Nearest E4M3FN codes (ties to even, clamped to +-448) of float32 values."""
+    lib = _load()
+    v = np.asarray(x, dtype=np.float32).reshape(-1)
+    return np.array([lib.oracle_encode_e4m3(float(t)) for t in v], dtype=np.uint8)
+
+
+def quantize_rows_e4m3(A, M: int, K: int):
+    """Row-wise E4M3 quantisation of a half [M,K] row-major matrix ("Chapter 5
+    Operators and Runtime", example 5-7): returns (Q uint8 [M,K], scale float32
+    [M]) with q_ik = E4M3(a_ik * 448/amax_i) and scale_i = amax_i / 448."""
+    lib = _load()
+    a = _buf(A, "f16", M * K)
+    Q = np.empty(M * K, dtype=np.uint8)
+    sc = np.empty(M, dtype=np.float32)
+    if lib.oracle_quantize_rows_e4m3(_ptr(a), M, K, _ptr(Q), _ptr(sc)):
+        raise RuntimeError("oracle_quantize_rows_e4m3 failed")
+    return Q.reshape(M, K), sc
+
+
+def gemm_e4m3_rowscale(Q, scale, Wt, M: int, N: int, K: int, rows=None):
+    """C[i,j] = scale_i * sum_k q_ik w_kj with Q [M,K] and the weights given as
+    Wt [N,K] (example 5-8).  Returns (C, S) float64 of shape [M or len(rows), N]."""
+    lib = _load()
+    q = np.ascontiguousarray(Q, dtype=np.uint8).reshape(-1)
+    w = np.ascontiguousarray(Wt, dtype=np.uint8).reshape(-1)
+    sc = np.ascontiguousarray(scale, dtype=np.float32).reshape(-1)
+    if q.size != M * K or w.size != N * K or sc.size != M:
+        raise ValueError("buffer sizes do not match M, N, K")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n = M if r is None else r.size
+    C = np.empty(n * N, dtype=np.float64)
+    S = np.empty(n * N, dtype=np.float64)
+    rc = lib.oracle_gemm_e4m3_rowscale(_ptr(q), _ptr(sc), _ptr(w), M, N, K,
+                                       None if r is None else _ptr(r), n, _ptr(C), _ptr(S))
+    if rc:
+        raise RuntimeError("oracle_gemm_e4m3_rowscale failed")
+    return C.reshape(n, N), S.reshape(n, N)
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:

@@ -278,6 +278,125 @@ int oracle_gemm_ex(int dtype, int layout, int op_a, int op_b,
     return 0;
 }
 
+/*
+ * FP8 E4M3FN ("Chapter 5 Operators and Runtime", section 5.4.3, example 5-7):
+ * 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; largest finite value
+ * 448; no infinities; S.1111.111 is NaN.  Subnormals (exponent field 0) are
+ * f/8 * 2^-6.
+ */
+double oracle_decode_e4m3(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int f = c & 0x7;
+    double v;
+    if (e == 15 && f == 7) {
+        v = NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f, -9);             /* f/8 * 2^-6 */
+    } else {
+        v = ldexp((double)(8 + f), e - 10);   /* (1 + f/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3FN value to x (ties to the even fraction), clamped to +-448 when
+ * |x| exceeds it; NaN stays NaN.  Returns the code. */
+uint8_t oracle_encode_e4m3(float x)
+{
+    if (x != x) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                      /* a = m * 2^e, 0.5 <= m < 1: binade exponent e-1 */
+    int be = e - 1;
+    if (be < -6) be = -6;              /* subnormal range shares the spacing of binade -6 */
+    double step = ldexp(1.0, be - 3);  /* 3 fraction bits */
+    double q = nearbyint(a / step);    /* exact division by a power of two; ties to even */
+    double v = q * step;
+    if (v >= 448.0) return sign | 0x7E;
+    if (v < ldexp(1.0, -6)) return sign | (uint8_t)q;           /* subnormal (or a rounded-up 8 -> normal below) */
+    frexp(v, &e);
+    be = e - 1;
+    uint8_t frac = (uint8_t)(ldexp(v, 3 - be) - 8.0);
+    return sign | (uint8_t)((be + 7) << 3) | frac;
+}
+
+/*
+ * Row-wise quantisation of a half matrix A [M,K] (row-major) to E4M3FN with one
+ * scale per row (example 5-7: the scale follows from the whole row's largest
+ * magnitude, so the row is read completely before any element is quantised):
+ *     amax_i  = max_k |a_ik|
+ *     q_ik    = E4M3(a_ik * (448 / amax_i))     (448 / amax_i and the product in FP32)
+ *     scale_i = amax_i / 448                    (FP32)
+ * so that a_ik ~ q_ik * scale_i.  A row of zeros gives q = 0 and scale 0.
+ * The two FP32 operations are written out so that the quantised codes, an
+ * integer result decided by floating point, are decided in FP32 exactly as the
+ * device does.
+ */
+int oracle_quantize_rows_e4m3(const uint16_t *A, int64_t M, int64_t K, uint8_t *Q, float *scale)
+{
+    if (M < 0 || K < 0) return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = (float)oracle_decode_f16(A[i * K + k]);
+            if (fabsf(a) > amax) amax = fabsf(a);
+        }
+        if (amax == 0.0f) {
+            for (int64_t k = 0; k < K; ++k) Q[i * K + k] = 0;
+            scale[i] = 0.0f;
+            continue;
+        }
+        volatile float inv = 448.0f / amax;
+        for (int64_t k = 0; k < K; ++k) {
+            volatile float x = (float)oracle_decode_f16(A[i * K + k]) * inv;
+            Q[i * K + k] = oracle_encode_e4m3(x);
+        }
+        volatile float sc = amax / 448.0f;
+        scale[i] = sc;
+    }
+    return 0;
+}
+
+/*
+ * Product of the row-quantised input with E4M3 weights (example 5-8: FP8 input
+ * times FP8 weights, FP16 output):
+ *     C[i,j] = scale_i * sum_k q_ik * w_kj
+ * Q is [M,K] row-major; the weights are given transposed, Wt [N,K] row-major
+ * (Wt[j*K + k] = w_kj).  Products and sums in double (each product of two E4M3
+ * values is exact); the scale multiplies the finished sum.  S[i,j] =
+ * |scale_i| * sum_k |q_ik w_kj|.  C and S are [M,N] row-major; rows select
+ * output rows (NULL: all M).
+ */
+int oracle_gemm_e4m3_rowscale(const uint8_t *Q, const float *scale, const uint8_t *Wt,
+                              int64_t M, int64_t N, int64_t K,
+                              const int64_t *rows, int64_t nrows, double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0) return 1;
+    if (!rows) nrows = M;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows && (rows[r] < 0 || rows[r] >= M)) return 1;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0, sab = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = oracle_decode_e4m3(Q[i * K + k]) * oracle_decode_e4m3(Wt[j * K + k]);
+                acc += p;
+                sab += fabs(p);
+            }
+            C[r * N + j] = (double)scale[i] * acc;
+            S[r * N + j] = fabs((double)scale[i]) * sab;
+        }
+    }
+    return 0;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

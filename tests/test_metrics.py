@@ -50,3 +50,13 @@ def test_wave_accounting():
     assert metrics.wave_count(1024, 46) == pytest.approx(22.26, abs=0.01)
     assert metrics.wave_efficiency(1024, 46) == pytest.approx(1024 / (23 * 46))
     assert metrics.wave_efficiency(0, 10) == 1.0
+
+
+def test_fp8_quantisation_traffic_example_5_8():
+    g = golden()
+    t = metrics.fp8_rowscale_traffic(4096, 4096, 1536, 128)
+    assert t["separate_input"] == g["fp8_separate_input_mib"] * MIB
+    assert t["fused_input"] == g["fp8_fused_input_mib"] * MIB
+    assert t["weights_output"] == g["fp8_weights_output_mib"] * MIB
+    assert t["separate_total"] == g["fp8_separate_total_mib"] * MIB
+    assert t["fused_total"] == g["fp8_fused_total_mib"] * MIB
