@@ -40,6 +40,8 @@ SIGNATURES = {
     "gemm_ex": ([_I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _VP, ctypes.c_int64, ctypes.c_int64,
                  _VP, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, _VP, ctypes.c_int64, ctypes.c_int64,
                  _I], _I),
+    "gemm_quantize_rows_e4m3": ([_VP, _VP, _VP, _I, _I], _I),
+    "gemm_e4m3_rowscale": ([_VP, _VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_set_stream": ([_VP], _I),
     "gemm_get_stream": ([], _VP),
     "gemm_synchronize": ([], _I),
@@ -140,6 +142,25 @@ def gemm_bf16_rm_silu_mul(X, W_g, W_u, Z, M: int, N: int, K: int) -> None:
     st = lib.gemm_bf16_rm_silu_mul(_addr(X), _addr(W_g), _addr(W_u), _addr(Z), int(M), int(N), int(K))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_bf16_rm_silu_mul", lib.gemm_last_error().decode())
+
+
+def gemm_quantize_rows_e4m3(A, Q, scale, M: int, K: int) -> None:
+    """Row-wise E4M3 quantisation of a half [M,K] matrix: Q [M,K] codes (uint8),
+    scale [M] float32, a_ik ~ Q[i,k] * scale_i."""
+    lib = load()
+    _bind_torch_stream(A, Q, scale)
+    st = lib.gemm_quantize_rows_e4m3(_addr(A), _addr(Q), _addr(scale), int(M), int(K))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_quantize_rows_e4m3", lib.gemm_last_error().decode())
+
+
+def gemm_e4m3_rowscale(Q, scale, Wt, C, M: int, N: int, K: int) -> None:
+    """C[M,N] (half) = diag(scale) Q[M,K] W[K,N], with the E4M3 weights given as Wt [N,K]."""
+    lib = load()
+    _bind_torch_stream(Q, scale, Wt, C)
+    st = lib.gemm_e4m3_rowscale(_addr(Q), _addr(scale), _addr(Wt), _addr(C), int(M), int(N), int(K))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_e4m3_rowscale", lib.gemm_last_error().decode())
 
 
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}

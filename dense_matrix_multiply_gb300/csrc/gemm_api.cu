@@ -453,6 +453,61 @@ GEMM_API gemm_status_t gemm_bf16_rm_silu_mul(const uint16_t *X, const uint16_t *
     return finish(launch_umma_silu_mul(p, Wu, dev->status, s), "umma_bf16_silu_mul");
 }
 
+GEMM_API gemm_status_t gemm_quantize_rows_e4m3(const uint16_t *A, uint8_t *Q, float *scale, int M, int K) {
+    if (M < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0) { t_last_kernel = "noop"; return GEMM_OK; }
+    if (!scale || (K > 0 && (!A || !Q))) return GEMM_ERR_INVALID_VALUE;
+    const size_t a_bytes = (size_t)M * K * 2, q_bytes = (size_t)M * K, s_bytes = (size_t)M * 4;
+    if (overlaps(Q, q_bytes, A, a_bytes) || overlaps(scale, s_bytes, A, a_bytes) ||
+        overlaps(scale, s_bytes, Q, q_bytes))
+        return GEMM_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    gemm_status_t st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = t_stream;
+    if (K == 0) {  // every row is empty: amax = 0, scale 0
+        const cudaError_t e = cudaMemsetAsync(scale, 0, s_bytes, s);
+        return finish(e, "zero_fill");
+    }
+    return finish(launch_quantize_rows_e4m3(A, Q, scale, M, K, s),
+                  quantize_rows_vec_ok(A, Q, K) ? "quantize_e4m3_vec" : "quantize_e4m3_scalar");
+}
+
+GEMM_API gemm_status_t gemm_e4m3_rowscale(const uint8_t *Q, const float *scale, const uint8_t *Wt, uint16_t *C,
+                                          int M, int N, int K) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) { t_last_kernel = "noop"; return GEMM_OK; }
+    if (!C || (K > 0 && (!Q || !scale || !Wt))) return GEMM_ERR_INVALID_VALUE;
+    const size_t c_bytes = (size_t)M * N * 2;
+    if (overlaps(C, c_bytes, Q, (size_t)M * K) || overlaps(C, c_bytes, Wt, (size_t)N * K) ||
+        overlaps(C, c_bytes, scale, (size_t)M * 4))
+        return GEMM_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    gemm_status_t st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = t_stream;
+    if (K == 0) {
+        const unsigned grid = (unsigned)(dev->num_sms * 4);
+        if (aligned16(C)) {
+            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)C, c_bytes / 16, (uint8_t *)C + (c_bytes & ~(size_t)15),
+                                                  c_bytes & 15);
+        } else {
+            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)C, c_bytes);
+        }
+        return finish(cudaGetLastError(), "zero_fill");
+    }
+    if (!umma_e4m3_supported(Q, Wt, C, N, K)) {
+        record_message("gemm_e4m3_rowscale: needs Q, Wt, C 16-byte aligned, K % 16 == 0 and N % 8 == 0");
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    const cudaError_t e = launch_umma_e4m3_rowscale(Q, scale, Wt, C, M, N, K, dev->status, s);
+    if (e == cudaErrorNotSupported) {
+        record_message("gemm_e4m3_rowscale: the tensor-core kernel cannot describe these operands");
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    return finish(e, "umma_e4m3_rowscale");
+}
+
 GEMM_API gemm_status_t gemm_set_stream(void *cuda_stream) {
     t_stream = static_cast<cudaStream_t>(cuda_stream);
     return GEMM_OK;

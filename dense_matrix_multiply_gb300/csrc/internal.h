@@ -73,6 +73,19 @@ bool umma_supported(const Problem &p);
 bool umma_ex_supported(const ProblemEx &p);
 cudaError_t launch_umma_ex(const ProblemEx &p, int *status, cudaStream_t s);
 
+// Row-wise E4M3 quantisation of a half [M,K] row-major matrix: Q [M,K] codes,
+// scale [M] (see quant_e4m3.cu).  M, K >= 1.
+bool quantize_rows_vec_ok(const void *A, const void *Q, int K);
+cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int M, int K, cudaStream_t s);
+
+// Row-scaled FP8 product on the tensor-core CTA pairs: C [M,N] half =
+// diag(scale) * Q [M,K] * Wt^T with Q and Wt [N,K] E4M3 codes, row-major.
+// Needs Q, Wt, C 16-byte aligned, K % 16 == 0, N % 8 == 0; returns
+// cudaErrorNotSupported, before any launch, otherwise.
+bool umma_e4m3_supported(const void *Q, const void *Wt, const void *C, int N, int K);
+cudaError_t launch_umma_e4m3_rowscale(const void *Q, const float *scale, const void *Wt, void *C, int M, int N,
+                                      int K, int *status, cudaStream_t s);
+
 // Test of the bounded pipeline waits: the single-CTA tensor-core kernel with a
 // producer that issues no load, so every CTA takes its timeout path (~2 s) and
 // records a code in *status.  Returns the launch status.

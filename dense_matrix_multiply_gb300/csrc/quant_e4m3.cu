@@ -1,0 +1,108 @@
+// Row-wise FP8 (E4M3FN) quantisation of a half matrix ("Chapter 5 Operators
+// and Runtime", section 5.4.3, example 5-7): the scale of a row comes from the
+// whole row's largest magnitude, so a row is read completely before any of its
+// elements is quantised.
+//     amax_i  = max_k |a_ik|
+//     q_ik    = E4M3(a_ik * (448 / amax_i))   nearest, ties to even, clamped to +-448
+//     scale_i = amax_i / 448
+// 448 / amax_i, the product and amax_i / 448 are single FP32 operations (IEEE
+// division: the library is built without fast math), so the codes are the
+// ones an FP32 evaluation of these steps gives.  A row of zeros gives q = 0 and
+// scale 0.
+//
+// Bound: HBM (read 2 bytes, write 1 byte per element).  One warp per row: a
+// first pass of 16-byte loads finds amax (warp shuffle reduction), a second
+// pass re-reads the row -- from L1/L2, the row was just read -- and writes 8
+// codes per 8-byte store.  Rows that are not 16-byte aligned use scalar loads.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+
+namespace gemm_gb300 {
+namespace {
+
+constexpr int WARPS = 8;
+
+__device__ __forceinline__ uint16_t cvt2(float lo, float hi) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(WARPS * 32)
+quantize_rows_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, float *__restrict__ scale, int M,
+                     int K) {
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (row >= M) return;
+    const __half *a = A + row * K;
+    uint8_t *q = Q + row * K;
+
+    float amax = 0.0f;
+    if (VEC) {
+        for (int k = lane * 8; k < K; k += 32 * 8) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a + k));
+            const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(h[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    } else {
+        for (int k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(__half2float(a[k])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+
+    if (amax == 0.0f) {
+        if (VEC) {
+            for (int k = lane * 8; k < K; k += 32 * 8) *reinterpret_cast<uint2 *>(q + k) = make_uint2(0u, 0u);
+        } else {
+            for (int k = lane; k < K; k += 32) q[k] = 0;
+        }
+        if (lane == 0) scale[row] = 0.0f;
+        return;
+    }
+    const float inv = 448.0f / amax;
+    if (VEC) {
+        for (int k = lane * 8; k < K; k += 32 * 8) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a + k));
+            const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+            uint32_t w[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float2 f0 = __half22float2(h[2 * i]);
+                const float2 f1 = __half22float2(h[2 * i + 1]);
+                w[i] = (uint32_t)cvt2(f0.x * inv, f0.y * inv) | ((uint32_t)cvt2(f1.x * inv, f1.y * inv) << 16);
+            }
+            *reinterpret_cast<uint2 *>(q + k) = make_uint2(w[0], w[1]);
+        }
+    } else {
+        for (int k = lane; k < K; k += 32)
+            q[k] = (uint8_t)__nv_cvt_float_to_fp8(__half2float(a[k]) * inv, __NV_SATFINITE, __NV_E4M3);
+    }
+    if (lane == 0) scale[row] = amax / 448.0f;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+bool quantize_rows_vec_ok(const void *A, const void *Q, int K) {
+    return aligned(A, 16) && aligned(Q, 8) && (K % 8) == 0;
+}
+
+cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int M, int K, cudaStream_t s) {
+    const long long blocks = ((long long)M + WARPS - 1) / WARPS;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (quantize_rows_vec_ok(A, Q, K))
+        quantize_rows_kernel<true><<<(unsigned)blocks, WARPS * 32, 0, s>>>(
+            static_cast<const __half *>(A), static_cast<uint8_t *>(Q), scale, M, K);
+    else
+        quantize_rows_kernel<false><<<(unsigned)blocks, WARPS * 32, 0, s>>>(
+            static_cast<const __half *>(A), static_cast<uint8_t *>(Q), scale, M, K);
+    return cudaGetLastError();
+}
+
+}  // namespace gemm_gb300

@@ -238,16 +238,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     if (mbar_try_wait_cluster(bar, parity)) return true;
     return mbar_wait_cluster_slow(bar, parity, abort, check_abort);
 }
-// TMA load into this CTA's shared memory, completion counted on an mbarrier
-// that may live in the peer CTA (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
-                                                 int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
-        : "memory");
-}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t cols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
                  "r"(cols)
@@ -343,12 +333,6 @@ __device__ __forceinline__ float silu_mul(float g, float u, __nv_bfloat16 *) {
     const float gb = __bfloat162float(__float2bfloat16_rn(g));
     const float ub = __bfloat162float(__float2bfloat16_rn(u));
     const float t = __bfloat162float(__float2bfloat16_rn(silu_f32(gb)));
-    return t * ub;
-}
-__device__ __forceinline__ float silu_mul(float g, float u, __half *) {
-    const float gb = __half2float(__float2half_rn(g));
-    const float ub = __half2float(__float2half_rn(u));
-    const float t = __half2float(__float2half_rn(silu_f32(gb)));
     return t * ub;
 }
 
@@ -652,6 +636,7 @@ struct PairArgs {
     int b_t;                  // B stored [N, K] (K contiguous) instead of [K, N]
     int a_bcast, b_bcast;     // batch stride 0: every b reads matrix 0
     float alpha, beta;
+    const float *row_scale;   // FP8 products: per-row scale of the output
     int *status;
 };
 
@@ -688,8 +673,16 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&o)[8], const __h
         o[2 * i + 1] = f.y;
     }
 }
-__device__ __forceinline__ float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
-__device__ __forceinline__ float load1(const __half *p) { return __half2float(*p); }
+// One M=256 N=bn K=32 step on 8-bit E4M3 operands (kind::f8f6f4), FP32 accumulator.
+__device__ __forceinline__ void umma_pair_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 
 // bn: the tile's N extent, a multiple of 64 in [128, 256], chosen per problem
 // to fill the last wave (each CTA still loads 128 columns of B per stage and
@@ -704,7 +697,13 @@ __device__ __forceinline__ float load1(const __half *p) { return __half2float(*p
 // epilogue keeps the unfused chain's rounding points: G and U rounded to the
 // output type, T = round(SiLU(G)), Z = round(T * U).  G, U and T never leave
 // the SM.
-template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool DUAL = false>
+// F8 (the row-scaled FP8 projection, "Chapter 5 Operators and Runtime",
+// example 5-8): A = Q [M,K] and B = Wt [N,K], E4M3 codes, both K-major; a K
+// block is 128 codes (one 128-byte swizzle row, the same bytes as 64 16-bit
+// elements) and one kind::f8f6f4 MMA consumes K = 32 (32 bytes, as a 16-bit
+// K = 16 step).  The epilogue multiplies row i by row_scale[i] and rounds to
+// T (half).
+template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool DUAL = false, bool F8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
 umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
@@ -731,7 +730,8 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int tiles_m = (M + PBM - 1) / PBM, tiles_n = (N + bn - 1) / bn;
     const int tiles_per_batch = tiles_m * tiles_n;
     const int num_tiles = tiles_per_batch * args.batch;
-    const int num_kb = (K + BK - 1) / BK;
+    constexpr int KB = F8 ? 128 : BK;  // K elements per stage (128 bytes per row)
+    const int num_kb = (K + KB - 1) / KB;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PSTAGES; ++s) {
@@ -790,7 +790,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (leader) mbar_arrive_expect_tx(&bars->full[stage], P_STAGE_TX);
                 uint8_t *a_dst = a_tiles + stage * P_A_STAGE;
                 uint8_t *b_dst = b_tiles + stage * P_B_STAGE;
-                const int k0 = kb * BK;
+                const int k0 = kb * KB;
                 if (!args.a_t) {
                     tma_load_3d_pair(a_dst, &tmA, full_leader, k0, row0, za);
                 } else {
@@ -860,8 +860,12 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const uint64_t ad = a_desc0 + (uint64_t)((stage * P_A_STAGE) >> 4);
                 const uint64_t bd = b_desc0 + (uint64_t)((stage * P_B_STAGE) >> 4);
 #pragma unroll
-                for (int ks = 0; ks < BK / UMMA_K; ++ks)
-                    umma_pair(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, (kb | ks) != 0);
+                for (int ks = 0; ks < BK / UMMA_K; ++ks) {
+                    if constexpr (F8)
+                        umma_pair_f8(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, (kb | ks) != 0);
+                    else
+                        umma_pair(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, (kb | ks) != 0);
+                }
                 umma_commit_pair_multicast(&bars->empty[stage], 0x3);
                 if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
             }
@@ -879,7 +883,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int quarter = warp & 3;
         uint8_t *my_stg = staging + quarter * 2 * P_STG_BOX;  // this warp's two staging boxes
         const float alpha = args.alpha, beta = args.beta;
-        const bool use_beta = !DUAL && beta != 0.0f;
+        const bool use_beta = !DUAL && !F8 && beta != 0.0f;
         int sb = 0;
         int it = 0;
         bool ok = true;
@@ -930,6 +934,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
             } else {
                 const int row = box_row0 + lane;
+                const float scale_v = F8 ? (row < M ? args.row_scale[row] : 0.0f) : alpha;
                 // This thread's row of C in batch bt, read only when beta != 0.
                 const T *c_old = (use_beta && row < M)
                                      ? static_cast<const T *>(args.C) + (long long)bt * args.stride_c +
@@ -968,7 +973,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         const uint32_t *src = c < 4 ? &r0[8 * c] : &r1[8 * (c - 4)];
                         float v[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = alpha * __uint_as_float(src[e]);
+                        for (int e = 0; e < 8; ++e) v[e] = scale_v * __uint_as_float(src[e]);
                         if (use_beta) {
                             float o[8];
                             unpack8(old[c], o, (const T *)nullptr);
@@ -1076,12 +1081,12 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
 // box_inner], 128-byte swizzle, zero fill out of bounds.  batch == 1 ignores
 // stride.
 bool make_map3(CUtensorMap *map, const void *base, CUtensorMapDataType dt, long long inner, long long outer,
-               long long batch, long long ld, long long stride, int box_inner, int box_outer) {
+               long long batch, long long ld, long long stride, int box_inner, int box_outer, int esize = 2) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     if (batch <= 1) stride = ld * outer;
     const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)(batch > 1 ? batch : 1)};
-    const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)stride * 2};
+    const cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(stride * esize)};
     const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1091,12 +1096,12 @@ bool make_map3(CUtensorMap *map, const void *base, CUtensorMapDataType dt, long 
 
 // Largest number of co-resident two-CTA clusters of the pair kernel, per device
 // (0: the pair kernel cannot be launched).
-template <typename T, uint32_t F, bool DUAL = false>
+template <typename T, uint32_t F, bool DUAL = false, bool F8 = false>
 int pair_clusters_max(int dev) {
     static std::atomic<int> cached[64];
     static std::once_flag once[64];
     std::call_once(once[dev & 63], [&] {
-        auto kern = umma_pair_kernel<T, F, pairk::P_STAGES, DUAL>;
+        auto kern = umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>;
         const int smem = pairk::smem_bytes(pairk::P_STAGES);
         int n = 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
@@ -1120,7 +1125,7 @@ int pair_clusters_max(int dev) {
     return cached[dev & 63].load();
 }
 
-template <typename T, uint32_t F, bool DUAL>
+template <typename T, uint32_t F, bool DUAL, bool F8 = false>
 cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                             const CUtensorMap &tb2, const PairArgs &args, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
@@ -1135,7 +1140,7 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL>, ta, tb, tc, tb2, args);
+    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>, ta, tb, tc, tb2, args);
 }
 
 // The general problem on CTA pairs.  Returns cudaErrorNotSupported, before any
@@ -1212,6 +1217,41 @@ cudaError_t launch_pair_silu_mul_typed(const Problem &p, const void *w_u, int cl
     args.alpha = 1.0f;
     args.status = status;
     return launch_pair_cfg<T, F, true>(ta, tg, tc, tu, args, clusters, s);
+}
+
+// C [M,N] half = diag(scale) Q Wt^T on CTA pairs, Q [M,K] and Wt [N,K] E4M3.
+cudaError_t launch_pair_e4m3(const void *Q, const float *scale, const void *Wt, void *C, int M, int N, int K,
+                             int clusters_max, int *status, cudaStream_t s) {
+    CUtensorMap ta, tb, tc;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!make_map3(&ta, Q, u8, K, M, 1, K, 0, 128, 128, 1) || !make_map3(&tb, Wt, u8, K, N, 1, K, 0, 128, 128, 1) ||
+        !make_map3(&tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, N, M, 1, N, 0, 64, 32))
+        return cudaErrorNotSupported;
+    const long long tiles_m = (M + pairk::PBM - 1) / pairk::PBM;
+    int bn = 256;
+    long long best = -1;
+    for (int cand = 256; cand >= 128; cand -= 64) {
+        const long long t = tiles_m * ((N + cand - 1) / cand);
+        const long long waves = (t + clusters_max - 1) / clusters_max;
+        const long long cost = waves * (cand > 224 ? cand : 224);
+        if (best < 0 || cost < best) { best = cost; bn = cand; }
+    }
+    const long long tiles = tiles_m * ((N + bn - 1) / bn);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
+    PairArgs args = {};
+    args.C = C;
+    args.ldc = N;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.batch = 1;
+    args.bn = bn;
+    args.b_t = 1;
+    args.alpha = 1.0f;
+    args.row_scale = scale;
+    args.status = status;
+    return launch_pair_cfg<__half, 0, false, true>(ta, tb, tc, tb, args, clusters, s);
 }
 
 // The tight problem of the plain entry points as a general one; lda: row
@@ -1396,6 +1436,21 @@ cudaError_t launch_umma_ex(const ProblemEx &p, int *status, cudaStream_t s) {
     if (cmax <= 0) return cudaErrorNotSupported;
     return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(p, cmax, status, s)
                               : launch_pair_typed<__half, 0>(p, cmax, status, s);
+}
+
+bool umma_e4m3_supported(const void *Q, const void *Wt, const void *C, int N, int K) {
+    return aligned(Q, 16) && aligned(Wt, 16) && aligned(C, 16) && (K % 16) == 0 && (N % 8) == 0;
+}
+
+cudaError_t launch_umma_e4m3_rowscale(const void *Q, const float *scale, const void *Wt, void *C, int M, int N,
+                                      int K, int *status, cudaStream_t s) {
+    if (!umma_e4m3_supported(Q, Wt, C, N, K)) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int cmax = pair_clusters_max<__half, 0, false, true>(dev);
+    if (cmax <= 0) return cudaErrorNotSupported;
+    return launch_pair_e4m3(Q, scale, Wt, C, M, N, K, cmax, status, s);
 }
 
 cudaError_t launch_umma_stall_test(const Problem &p, int num_sms, int *status, cudaStream_t s) {

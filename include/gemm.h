@@ -190,6 +190,36 @@ GEMM_API gemm_status_t gemm_ex(gemm_dtype_t dtype, gemm_layout_t layout, gemm_op
                                const void *B, int64_t ldb, int64_t stride_b,
                                float beta, void *C, int64_t ldc, int64_t stride_c, int batch);
 
+/* Row-wise FP8 quantisation ("Chapter 5 Operators and Runtime", section 5.4.3,
+ * example 5-7).  A is [M,K] row-major IEEE half; for every row i:
+ *     amax_i  = max_k |a_ik|
+ *     Q[i,k]  = E4M3FN(a_ik * (448 / amax_i))   nearest, ties to even, clamped to +-448
+ *     scale_i = amax_i / 448
+ * with 448 / amax_i, the product and amax_i / 448 each one FP32 operation, so
+ * a_ik ~ Q[i,k] * scale_i.  A row of zeros gives Q = 0 and scale 0.  The whole
+ * row is read before any of its codes is written (the scale depends on it).
+ * E4M3FN: 1 sign, 4 exponent (bias 7), 3 fraction bits, largest finite 448,
+ * no infinities.  Q [M,K] row-major bytes, scale [M] float, device pointers
+ * owned by the caller.  Any alignment (16-byte aligned A and 8-byte aligned Q
+ * with K % 8 == 0 use vector loads).  NaN or infinite inputs are outside the
+ * contract.  K = 0 sets every scale to 0.  Errors: GEMM_ERR_INVALID_VALUE for a
+ * negative size or a null pointer; GEMM_ERR_ALIAS if Q, scale and A overlap. */
+GEMM_API gemm_status_t gemm_quantize_rows_e4m3(const uint16_t *A, uint8_t *Q, float *scale, int M, int K);
+
+/* Row-scaled FP8 projection ("Chapter 5 Operators and Runtime", section 5.4.4,
+ * example 5-8: FP8 input times FP8 weights, FP16 output):
+ *     C[i,j] = scale_i * sum_k Q[i,k] * W[k,j]
+ * on the tensor cores (E4M3 x E4M3 products, FP32 accumulation), the row scale
+ * applied to the FP32 sum, one rounding to half.  Q [M,K] row-major E4M3FN codes
+ * and scale [M] as written by gemm_quantize_rows_e4m3; the weights W [K,N] are
+ * given transposed, Wt [N,K] row-major (each output column's K codes
+ * contiguous, the layout of a linear layer's weight); C [M,N] row-major half.
+ * Needs Q, Wt, C 16-byte aligned, K % 16 == 0 and N % 8 == 0
+ * (GEMM_ERR_INVALID_VALUE otherwise, with a message in gemm_last_error).
+ * K = 0 gives C = 0.  GEMM_ERR_ALIAS if C overlaps Q, Wt or scale. */
+GEMM_API gemm_status_t gemm_e4m3_rowscale(const uint8_t *Q, const float *scale, const uint8_t *Wt, uint16_t *C,
+                                          int M, int N, int K);
+
 /* Stream for the calling host thread's subsequent calls: a cudaStream_t passed
  * as void*.  NULL selects the legacy default stream.  The stream stays owned by
  * the caller and must outlive the calls issued on it. */

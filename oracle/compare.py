@@ -162,3 +162,28 @@ def check_ex(variant: str, C: np.ndarray, ref: dict, K: int, alpha: float) -> di
         "max_err_over_tol": float(np.nanmax(ratio)) if C.size else 0.0,
         "ok": bool(not bad.any()),
     }
+
+
+def tol_e4m3(C_ref: np.ndarray, S: np.ndarray) -> np.ndarray:
+    """Tolerance of the row-scaled FP8 product (half output) against
+    ``oracle.gemm_e4m3_rowscale``: the codes and the FP32 row scale are the same
+    on both sides, every E4M3 x E4M3 product is exact in FP32, so what remains is
+    the FP32 accumulation allowance 1e-5 * S (S = |scale| sum_k |q w|), the FP32
+    rounding of scale * acc (2^-23 |C|, with slack) and the final rounding to
+    half (one half ulp at |C|)."""
+    C_ref = np.asarray(C_ref, dtype=np.float64)
+    return 1e-5 * np.asarray(S, dtype=np.float64) + 2.0 ** -23 * np.abs(C_ref) + ulp_out("f16", C_ref)
+
+
+def check_e4m3(C: np.ndarray, C_ref: np.ndarray, S: np.ndarray) -> dict:
+    C = np.asarray(C, dtype=np.float64)
+    C_ref = np.asarray(C_ref, dtype=np.float64)
+    if C.shape != C_ref.shape:
+        raise ValueError(f"shape {C.shape} != reference shape {C_ref.shape}")
+    tol = tol_e4m3(C_ref, S)
+    err = np.abs(C - C_ref)
+    bad = ~(err <= tol)
+    return {"n": int(C.size), "n_bad": int(bad.sum()),
+            "max_abs_err": float(np.nanmax(err)) if C.size else 0.0,
+            "max_err_over_tol": float(np.nanmax(err / tol)) if C.size else 0.0,
+            "ok": bool(not bad.any())}

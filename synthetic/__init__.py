@@ -119,6 +119,21 @@ def matrix(dtype: str, rows: int, cols: int, seed: int, dist: str = "uniform",
 # The five workloads, by what they are. Each entry: (config id, list of
 # problems); a problem is (variant, M, N, K, distribution of A, sigma A,
 # distribution of B, sigma B).
+def e4m3_codes(rows: int, cols: int, seed: int, exp_lo: int = 4, exp_hi: int = 10) -> np.ndarray:
+    """Random FP8 E4M3FN codes built bit by bit (no rounding involved): a random
+    sign, an exponent field uniform in [exp_lo, exp_hi] and a random 3-bit
+    fraction, i.e. values of magnitude 2^(exp_lo-7) .. 1.875 * 2^(exp_hi-7).
+    exp_hi <= 14 keeps every code finite (field 15 holds 448 and NaN)."""
+    if not (1 <= exp_lo <= exp_hi <= 14):
+        raise ValueError("exponent fields must lie in 1..14")
+    x = splitmix64(seed, rows * cols)
+    sign = (x >> np.uint64(63)).astype(np.uint8)
+    frac = ((x >> np.uint64(32)) & np.uint64(7)).astype(np.uint8)
+    span = np.uint64(exp_hi - exp_lo + 1)
+    expo = (((x & np.uint64(0xFFFFFFFF)) % span) + np.uint64(exp_lo)).astype(np.uint8)
+    return ((sign << 7) | (expo << 3) | frac).astype(np.uint8)
+
+
 WORKLOADS = {
     "sgemm_f32_rm_256": (0, [("f32_rm", 256, 256, 256, "uniform", 1.0, "uniform", 1.0)]),
     "sgemm_f32_rm_4096": (1, [("f32_rm", 4096, 4096, 4096, "uniform", 1.0, "uniform", 1.0)]),

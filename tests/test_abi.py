@@ -128,3 +128,22 @@ def test_general_form_host_side_errors(built):
     # B's third matrix (stride 4096 floats = 16384 bytes) starts exactly at C
     assert ex(batch=3, sc=16, sb=4096, b=C - 2 * 16384) == 2
     assert ex(lda=1 << 61, batch=1) == 1      # span overflows
+
+
+def test_fp8_host_side_errors(built):
+    lib = built
+    buf = ctypes.create_string_buffer(1 << 16)
+    p = ctypes.addressof(buf)
+    A, Q, S, W, C = p, p + 8192, p + 16384, p + 24576, p + 32768
+    q = lib.gemm_quantize_rows_e4m3
+    assert q(A, Q, S, -1, 4) == 1 and q(A, Q, S, 4, -1) == 1
+    assert q(A, Q, S, 0, 4) == 0 and lib.gemm_last_kernel() == b"noop"
+    assert q(None, Q, S, 4, 4) == 1 and q(A, Q, None, 4, 4) == 1
+    assert q(A, A + 8, S, 4, 4) == 2          # Q overlaps A
+    assert q(A, Q, Q + 4, 4, 4) == 2          # scale overlaps Q
+    r = lib.gemm_e4m3_rowscale
+    assert r(Q, S, W, C, -1, 4, 16) == 1 and r(Q, S, W, C, 4, 4, -16) == 1
+    assert r(Q, S, W, C, 0, 4, 16) == 0 and r(Q, S, W, C, 4, 0, 16) == 0
+    assert r(Q, S, W, None, 4, 4, 16) == 1 and r(None, S, W, C, 4, 4, 16) == 1
+    assert r(Q, S, W, Q + 8, 4, 4, 16) == 2   # C overlaps Q
+    assert r(Q, S, W, S, 4, 4, 16) == 2       # C overlaps scale

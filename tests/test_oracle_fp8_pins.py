@@ -133,3 +133,22 @@ def test_rowscale_gemm_brute_force():
     rows = np.array([3, 0])
     Cr, _ = oracle.gemm_e4m3_rowscale(Q, scale, W, M, N, K, rows=rows)
     assert np.array_equal(Cr, C[rows])
+
+
+def test_e4m3_code_generator_stays_finite_and_in_range():
+    import synthetic
+    c = synthetic.e4m3_codes(64, 64, 123, 4, 10)
+    v = np.abs(oracle.decode_e4m3(c))
+    assert np.isfinite(v).all()
+    assert v.min() >= 2.0 ** -3 and v.max() <= 1.875 * 2.0 ** 3
+    assert np.array_equal(c, synthetic.e4m3_codes(64, 64, 123, 4, 10))
+
+
+def test_e4m3_tolerance_admits_rounding_and_rejects_a_step():
+    from oracle import compare
+    C_ref = np.array([1.0, 100.0, -3.5, 1000.0])
+    S = np.abs(C_ref) * 10
+    exact = C_ref.astype(np.float16).astype(np.float64)
+    assert compare.check_e4m3(exact, C_ref, S)["ok"]
+    moved = C_ref + 4 * compare.ulp_out("f16", C_ref) + 1e-4 * S
+    assert not compare.check_e4m3(moved, C_ref, S)["ok"]
