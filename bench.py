@@ -82,6 +82,10 @@ def all_workloads():
     # the FFN gate/up projection with its SiLU * U epilogue fused (two GEMMs)
     out["ffn_gate_up_bf16_silu_mul_1024x12288x4096"] = (3, ("bf16_silu_mul", 1024, 12288, 4096, "normal", 1.0,
                                                              "normal", 1.0 / 64.0))
+    # the row-scaled FP8 projection of example 5-8: A [4096,4096] half quantised
+    # row-wise to E4M3, times E4M3 weights [4096,1536], half output
+    out["fp8_rowscale_e4m3_4096x1536x4096"] = (5, ("e4m3_rowscale", 4096, 1536, 4096, "normal", 1.0,
+                                                    "uniform", 1.0))
     # the general form (gemm_ex): a linear layer's X W^T with W stored [N, K],
     # a strided batch, and FP32 with a transposed B on the SIMT kernel
     for dtype, ops, batch, (M, N, K) in (("bf16", "NT", 1, (8192, 8192, 8192)),
@@ -206,6 +210,9 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
     if variant == "bf16_silu_mul":  # two products, X read once: X, W_g, W_u, Z
         flops = 2 * metrics.gemm_flops(M, N, K)
         algo_bytes = es * (M * K + 2 * K * N + M * N)
+    elif variant == "e4m3_rowscale":  # the product kernel: Q, W codes, the row scales, half C
+        flops = metrics.gemm_flops(M, N, K)
+        algo_bytes = M * K + K * N + 4 * M + 2 * M * N
     elif variant.startswith("ex:"):  # batch independent products, beta = 0 (C not read)
         batch = ex_parse(variant)[4]
         flops = batch * metrics.gemm_flops(M, N, K)
@@ -223,6 +230,13 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
         return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "algorithmic_bytes": algo_bytes, "peak_source": peaks_src}
     achieved = flops / seconds_per_launch / 1e12
+    if kind == "umma" and variant == "e4m3_rowscale":
+        # dense FP8 rate = 2 x the dense BF16 rate (4.5 vs 2.25 PFLOP/s nominal)
+        peak = 2.0 * float(peaks["bf16_tflops"])
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "algorithmic_flops": flops,
+                "algorithmic_bytes": algo_bytes,
+                "peak_source": f"{peaks_src} cuBLAS bf16 burst x 2 (nominal FP8/BF16 dense ratio)"}
     if kind == "umma":
         peak = float(peaks["bf16_tflops"])
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -266,12 +280,44 @@ def time_device(fn, steps: int, warmup: int, stream):
     return start.elapsed_time(end)
 
 
+def host_inputs(variant, cfg, M, N, K, da, sa, db, sb):
+    """Seeded host buffers of a workload: (A, B, extra)."""
+    if variant == "bf16_silu_mul":
+        A = synthetic.matrix("bf16", M, K, synthetic.seed_for(cfg, 1), da, sa)
+        B = synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 2), db, sb)
+        return A, B, (synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 3), db, sb),)
+    if variant == "e4m3_rowscale":
+        A = synthetic.matrix("f16", M, K, synthetic.seed_for(cfg, 1), da, sa)
+        return A, synthetic.e4m3_codes(N, K, synthetic.seed_for(cfg, 2)), ()
+    if variant.startswith("ex:"):
+        dtype, _, _, _, batch = ex_parse(variant)
+        A = synthetic.matrix(dtype, batch * M, K, synthetic.seed_for(cfg, 5), da, sa)
+        B = synthetic.matrix(dtype, batch * K, N, synthetic.seed_for(cfg, 6), db, sb)
+        return A, B, ()
+    A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
+    return A, B, ()
+
+
 def oracle_rows(variant, A, B, M, N, K, rows, extra=()):
-    """The oracle on output rows `rows`; returns the FLOPs that took."""
+    """The oracle on output rows `rows` (for a batched workload: rows 0..len-1
+    of the first batch entry); returns the FLOPs that took."""
     import oracle
     if variant == "bf16_silu_mul":
         oracle.silu_mul(A, B, extra[0], M, N, K, rows=rows)
         return 4.0 * len(rows) * N * K
+    if variant == "e4m3_rowscale":  # quantise the rows, then their products
+        a = np.ascontiguousarray(A.reshape(M, K)[rows])
+        Q, S = oracle.quantize_rows_e4m3(a, len(rows), K)
+        oracle.gemm_e4m3_rowscale(Q, S, B, len(rows), N, K)
+        return 2.0 * len(rows) * N * K
+    if variant.startswith("ex:"):
+        dtype, layout, op_a, op_b, _ = ex_parse(variant)
+        m = len(rows)
+        lda = M if op_a == "T" else K
+        ldb = K if op_b == "T" else N
+        oracle.gemm_ex(dtype, layout, op_a, op_b, m, N, K, 1.0, A[:M * K], lda, 0, B[:K * N], ldb, 0, 0.0,
+                       None, N, 0, 1)
+        return 2.0 * m * N * K
     oracle.gemm_rows(variant, A, B, M, N, K, rows)
     return 2.0 * len(rows) * N * K
 
@@ -335,11 +381,29 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
 
         def call():
             return fn(pa, pb, pu, pc, M, N, K)
+    elif variant == "e4m3_rowscale":
+        # one step: quantise A row-wise (E4M3 codes + row scales), then the FP8 product
+        A, B, _ = host_inputs(variant, cfg, M, N, K, da, sa, db, sb)
+        dA = torch.from_numpy(A.view(np.int16)).cuda()
+        dB = torch.from_numpy(B).cuda()
+        dQ = torch.empty(M * K, dtype=torch.uint8, device="cuda")
+        dS = torch.empty(M, dtype=torch.float32, device="cuda")
+        dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+        lib = g.load()
+        pa, pb, pq, ps, pc = dA.data_ptr(), dB.data_ptr(), dQ.data_ptr(), dS.data_ptr(), dC.data_ptr()
+
+        def quantize():
+            return lib.gemm_quantize_rows_e4m3(pa, pq, ps, M, K)
+
+        def product():
+            return lib.gemm_e4m3_rowscale(pq, ps, pb, pc, M, N, K)
+
+        def call():
+            return quantize() or product()
     elif variant.startswith("ex:"):
         # tight strides: A stored [M,K] or [K,M], B [K,N] or [N,K], batch matrices back to back
         dtype, layout, op_a, op_b, batch = ex_parse(variant)
-        A = synthetic.matrix(dtype, batch * M, K, synthetic.seed_for(cfg, 5), da, sa)
-        B = synthetic.matrix(dtype, batch * K, N, synthetic.seed_for(cfg, 6), db, sb)
+        A, B, _ = host_inputs(variant, cfg, M, N, K, da, sa, db, sb)
         dA, dB, dC = device_inputs(dtype + "_rm", A, B, batch * M, N)
         lda = M if op_a == "T" else K
         ldb = K if op_b == "T" else N
@@ -367,6 +431,13 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     g.gemm_synchronize()
     kernel = g.gemm_last_kernel()
     kind = kernel_kind(kernel)
+    split = {}
+    if variant == "e4m3_rowscale":
+        # each kernel of the step timed on its own: the product is the dominant
+        # (tensor-bound) kernel, the quantisation is HBM-bound
+        for nm, fn1 in (("quantize", quantize), ("product", product)):
+            ms1 = time_device(fn1, steps, 3, stream)
+            split[nm] = ms1 / steps
 
     sampler = ClockSampler(sampler_uuid) if clocks else None
     for _ in range(warmup):
@@ -386,16 +457,25 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     flops = metrics.gemm_flops(M, N, K) * (2 if variant == "bf16_silu_mul" else
                                            ex_parse(variant)[4] if variant.startswith("ex:") else 1)
     s_per = ms / 1e3 / steps
+    s_kernel = split["product"] / 1e3 if split else s_per
     res = {
         "workload": name, "variant": variant, "M": M, "N": N, "K": K, "kernel": kernel, "flops_per_step": flops,
         "ms_per_step": ms / steps, "tflops": flops / s_per / 1e12, "steps": steps, "ms_total": ms,
-        "roofline": roofline_for(kind, variant, M, N, K, s_per, peaks, peaks_src,
+        "roofline": roofline_for(kind, variant, M, N, K, s_kernel, peaks, peaks_src,
                                  clk["sm_mhz"] if clk else None, sms, name, prop_mhz),
         "clocks": clk, "footprint_bytes": int(dA.numel() * dA.element_size() + dB.numel() * dB.element_size()
                                               + dC.numel() * dC.element_size()),
     }
 
-    if e2e:
+    if split:
+        q_bytes = 2 * M * K + M * K + 4 * M  # read A once, write the codes and the scales
+        res["kernels"] = {
+            "quantize_e4m3": {"ms": split["quantize"], "GB/s": q_bytes / (split["quantize"] / 1e3) / 1e9,
+                              "frac_hbm": q_bytes / (split["quantize"] / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                              "algorithmic_bytes": q_bytes},
+            "umma_e4m3_rowscale": {"ms": split["product"], "TFLOP/s": flops / (split["product"] / 1e3) / 1e12},
+        }
+    if e2e and variant != "e4m3_rowscale":
         hA = torch.from_numpy(A.view(np.int16) if A.dtype != np.float32 else A).pin_memory()
         hB = torch.from_numpy(B.view(np.int16) if B.dtype != np.float32 else B).pin_memory()
         hC = torch.empty_like(dC, device="cpu").pin_memory()
@@ -471,7 +551,7 @@ def run_ours(args):
             r = measure_workload(wl, max(5, args.path_steps), 3, peaks, peaks_src, sms, stream,
                                  sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True, prop_mhz=prop_mhz)
             paths.append({k: r[k] for k in ("workload", "kernel", "M", "N", "K", "ms_per_step", "tflops",
-                                            "roofline", "clocks")})
+                                            "roofline", "clocks", "kernels") if k in r})
 
     if rank == 0:
         M, N, K = res["M"], res["N"], res["K"]
@@ -516,13 +596,7 @@ def run_reference(args):
         return
     import oracle
     cfg, (variant, M, N, K, da, sa, db, sb) = all_workloads()[args.workload]
-    extra = ()
-    if variant == "bf16_silu_mul":
-        A = synthetic.matrix("bf16", M, K, synthetic.seed_for(cfg, 1), da, sa)
-        B = synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 2), db, sb)
-        extra = (synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 3), db, sb),)
-    else:
-        A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
+    A, B, extra = host_inputs(variant, cfg, M, N, K, da, sa, db, sb)
     threads = oracle.num_threads()
     # size each step so that warmup + steps take about args.ref_seconds in total
     rows = np.arange(min(threads, M), dtype=np.int64)
@@ -569,7 +643,8 @@ def main(argv=None):
                                                    "ffn_gate_up_bf16_silu_mul_1024x12288x4096",
                                                    "gemm_ex_bf16_rm_NT_8192x8192x8192",
                                                    "gemm_ex_f16_rm_NN_batch32_1024x1024x1024",
-                                                   "gemm_ex_f32_rm_NT_4096x4096x4096"])
+                                                   "gemm_ex_f32_rm_NT_4096x4096x4096",
+                                                   "fp8_rowscale_e4m3_4096x1536x4096"])
     p.add_argument("--path-steps", type=int, default=50)
     p.add_argument("--no-paths", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
