@@ -346,6 +346,102 @@ def cpu_sample(variant, A, B, M, N, K, budget_s: float, extra=()):
     return fl / dt, nrows, dt, threads
 
 
+# ------------------------------------------------------------------ cuBLAS column
+class Cublas:
+    """cuBLAS, timed beside the library as a reference column (outside the
+    library, never on its path): FP32 SGEMM in pedantic math (no TF32, as the
+    pages' cuBLAS baseline), half and bf16 through cublasGemmEx with FP32
+    compute and default math.  Row-major problems use the identity C^T = B^T A^T
+    ("SGEMM measured and the three ledgers", section 2)."""
+
+    OP_N, R_32F, R_16F, R_16BF, COMPUTE_32F, GEMM_DEFAULT = 0, 0, 2, 14, 68, -1
+    DEFAULT_MATH, PEDANTIC_MATH = 0, 2
+
+    def __init__(self):
+        import ctypes
+        import glob
+        self.ct = ctypes
+        cands = glob.glob("/usr/local/cuda/lib64/libcublas.so*")
+        try:
+            import nvidia
+            for d in nvidia.__path__:
+                cands += glob.glob(os.path.join(d, "cublas", "lib", "libcublas.so*"))
+        except ImportError:
+            pass
+        self.lib, err = None, "libcublas not found"
+        for c in sorted(cands, key=len):
+            try:
+                self.lib = ctypes.CDLL(c)
+                break
+            except OSError as e:
+                err = str(e)
+        if self.lib is None:
+            raise RuntimeError(err)
+        self.handle = ctypes.c_void_p()
+        if self.lib.cublasCreate_v2(ctypes.byref(self.handle)) != 0:
+            raise RuntimeError("cublasCreate failed")
+        vp, i, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+        self.lib.cublasSgemm_v2.argtypes = [vp, i, i, i, i, i, vp, vp, i, vp, i, vp, vp, i]
+        self.lib.cublasGemmEx.argtypes = [vp, i, i, i, i, i, vp, vp, i, i, vp, i, i, vp, vp, i, i, i, i]
+        self.lib.cublasSetStream_v2.argtypes = [vp, vp]
+        self.lib.cublasSetMathMode.argtypes = [vp, i]
+        self.one = ctypes.c_float(1.0)
+        self.zero = ctypes.c_float(0.0)
+
+    def call(self, variant, M, N, K, pa, pb, pc):
+        ct, lib, h = self.ct, self.lib, self.handle
+        one, zero = ct.byref(self.one), ct.byref(self.zero)
+        if variant == "f32_rm":
+            lib.cublasSetMathMode(h, self.PEDANTIC_MATH)
+            return lib.cublasSgemm_v2(h, self.OP_N, self.OP_N, N, M, K, one, pb, N, pa, K, zero, pc, N)
+        lib.cublasSetMathMode(h, self.DEFAULT_MATH)
+        if variant == "f16_cm":
+            return lib.cublasGemmEx(h, self.OP_N, self.OP_N, M, N, K, one, pa, self.R_16F, M, pb, self.R_16F, K,
+                                    zero, pc, self.R_16F, M, self.COMPUTE_32F, self.GEMM_DEFAULT)
+        # bf16 row-major
+        return lib.cublasGemmEx(h, self.OP_N, self.OP_N, N, M, K, one, pb, self.R_16BF, N, pa, self.R_16BF, K,
+                                zero, pc, self.R_16BF, N, self.COMPUTE_32F, self.GEMM_DEFAULT)
+
+    def measure(self, variant, M, N, K, dA, dB, dC_like, stream, steps):
+        """{"tflops", "ms_per_step", "mode", "max_abs_diff_vs_library"}: cuBLAS on the
+        same device inputs, timed like the library (CUDA events, same stream)."""
+        import torch
+        self.lib.cublasSetStream_v2(self.handle, self.ct.c_void_p(stream.cuda_stream))
+        out = torch.empty_like(dC_like)
+        pa, pb, pc = dA.data_ptr(), dB.data_ptr(), out.data_ptr()
+
+        def step():
+            st = self.call(variant, M, N, K, pa, pb, pc)
+            if st != 0:
+                raise RuntimeError(f"cuBLAS status {st}")
+
+        ms = time_device(step, steps, 3, stream)
+        torch.cuda.synchronize()
+        if variant == "f32_rm":
+            diff = (out - dC_like).abs().max().item()
+        else:
+            dt = torch.float16 if variant.startswith("f16") else torch.bfloat16
+            diff = (out.view(dt).float() - dC_like.view(dt).float()).abs().max().item()
+        mode = "FP32, CUBLAS_PEDANTIC_MATH" if variant == "f32_rm" else "cublasGemmEx, FP32 compute, default math"
+        return {"tflops": metrics.gemm_flops(M, N, K) / (ms / 1e3 / steps) / 1e12, "ms_per_step": ms / steps,
+                "mode": mode, "max_abs_diff_vs_library": diff}
+
+
+_CUBLAS = None
+
+
+def cublas_column(variant, M, N, K, dA, dB, dC, stream, steps):
+    global _CUBLAS
+    if variant not in ("f32_rm", "f16_cm", "bf16_rm"):
+        return None
+    try:
+        if _CUBLAS is None:
+            _CUBLAS = Cublas()
+        return _CUBLAS.measure(variant, M, N, K, dA, dB, dC, stream, steps)
+    except Exception as e:  # a reference column only: report why it is missing
+        return {"unavailable": str(e)[:200]}
+
+
 # ------------------------------------------------------------------ replicas
 def slowest_rank_ms(ms: float, world: int, device: str = "cpu") -> float:
     """The timed region's length on the slowest rank (every rank gets it)."""
@@ -366,7 +462,7 @@ def replica_throughput(flops_per_step: float, steps: int, world: int, ms_slowest
 
 # ------------------------------------------------------------------ our arm
 def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler_uuid=None, e2e=True,
-                     cpu_budget=0.0, clocks=True, prop_mhz=None):
+                     cpu_budget=0.0, clocks=True, prop_mhz=None, cublas=True):
     import torch
     import dense_matrix_multiply_gb300 as g
 
@@ -471,6 +567,8 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
                                               + dC.numel() * dC.element_size()),
     }
 
+    if cublas and variant in ("f32_rm", "f16_cm", "bf16_rm"):
+        res["cublas"] = cublas_column(variant, M, N, K, dA, dB, dC, stream, steps)
     if split:
         q_bytes = 2 * M * K + M * K + 4 * M  # read A once, write the codes and the scales
         res["kernels"] = {
@@ -555,7 +653,7 @@ def run_ours(args):
             r = measure_workload(wl, max(5, args.path_steps), 3, peaks, peaks_src, sms, stream,
                                  sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True, prop_mhz=prop_mhz)
             paths.append({k: r[k] for k in ("workload", "kernel", "M", "N", "K", "ms_per_step", "tflops",
-                                            "roofline", "clocks", "kernels") if k in r})
+                                            "roofline", "clocks", "kernels", "cublas") if k in r})
 
     if rank == 0:
         M, N, K = res["M"], res["N"], res["K"]
@@ -576,7 +674,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "kernel": res["kernel"],
             "roofline": res["roofline"],
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if res["variant"] == "e4m3_rowscale" else 1),
             "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
                        "reasons": clk.get("reasons", []), "samples": clk.get("samples", 0)},
         }
@@ -584,6 +682,8 @@ def run_ours(args):
             line["e2e"] = res["e2e"]
         if "cpu_baseline" in res:
             line["cpu_baseline"] = res["cpu_baseline"]
+        if res.get("cublas"):
+            line["cublas"] = res["cublas"]
         if paths:
             line["paths"] = paths
         print(json.dumps(line), flush=True)
