@@ -24,8 +24,8 @@
 // The same template with 16-bit inputs (converted to FP32 when staged) and
 // 16-bit outputs (rounded to nearest even once) serves as the tensor path's
 // fallback for strides TMA cannot describe.  FP32 problems with float4-able
-// operands that fill the GPU run on simt_ffma2_kernel instead: the same tile
-// and order of operations, issued as packed two-lane FMAs (see below).
+// operands run on simt_ffma2_kernel instead: the same order of operations on
+// 128 x 64 tiles, issued as packed two-lane FMAs (see below).
 //
 // EX: the general form ("SGEMM measured and the three ledgers", section 2,
 // operation flags and leading dimensions; section 3, kernel K1,
@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 
@@ -49,7 +50,7 @@ constexpr int A_LD = BM + 4;  // padded row of the k-major A tile (floats)
 constexpr int B_LD = BN;      // row of the B tile (floats)
 constexpr int GROUP_M = 8;
 
-// Whether FP32 problems that fill the GPU issue packed two-lane FMAs.
+// Whether FP32 problems with float4-able operands use the packed-FMA kernel.
 #ifndef SIMT_FFMA2
 #define SIMT_FFMA2 1
 #endif
@@ -272,79 +273,96 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
     }
 }
 
-// ------------------------------------------------------ packed-FMA variant
-// The FP32 kernel for problems that fill the GPU.  Same 128 x 128 tile and
-// 16 x 8 outputs per thread, with the FFMA stream issued as packed two-lane
-// FMAs (fma.rn.f32x2 through __ffma2_rn): one instruction updates two
-// accumulators, so the FMA pipe rather than instruction issue bounds the loop,
-// and loads, stores and address work fit in the issue slots the pipe leaves.
-//   * Accumulators are pairs of horizontally adjacent outputs (columns c, c+1
-//     of one row): B's fragment supplies (b_c, b_c+1) as it lies, A's value is
-//     paired with itself, (a_r, a_r).
-//   * B quads go to shared memory with 16-byte cp.async; A quads pass through
-//     registers to be transposed into the padded k-major tile.
-//   * A ring of F2_STAGES stages; one barrier per K step.  B is requested
-//     F2_STAGES - 1 steps ahead; A is loaded into registers one step before
-//     its store, so each load has a whole compute step to arrive.
-// Measured on GB300 at 4096^3: 57.6 TFLOP/s against 54.4 for the scalar-FFMA
-// kernel below it (FMA pipe 76 % vs 71 %, 1.39 G instead of 2.45 G issued
-// instructions).  A version that stored A duplicated in shared memory to form
-// (a_r, a_r) by a 128-bit load ran at 51.8: twice the A loads and 250
-// registers.  FP32 with float4-able operands only.  Every product and sum is
-// the scalar kernel's, in the same order, so the results are bit-identical.
-constexpr int F2_STAGES = 3;
-constexpr int F2_BK = 8;
-constexpr int F2_ALD = A_LD;  // floats per k-row of the k-major A tile
-
+// ------------------------------------------------------ packed-FMA FP32 kernel
+// The FP32 kernel for float4-able operands.  The FFMA stream is issued as
+// packed two-lane FMAs (fma.rn.f32x2 through __ffma2_rn): one instruction
+// updates two accumulators, so the FMA pipe rather than instruction issue
+// bounds the loop, and loads, stores and address work fit in the issue slots
+// the pipe leaves free.
+//   * CTA tile 128 x 64, 128 threads (2 x 2 warps of 64 x 32), 8 x 8 outputs
+//     per thread held as 32 pairs of horizontally adjacent outputs (columns
+//     c, c+1 of one row): B's fragment supplies (b_c, b_c+1) as it lies, A's
+//     value is paired with itself, (a_r, a_r).  A lane (lm, ln) of the 8 x 4
+//     lane grid owns rows {4lm..4lm+3} + {0, 32} and columns {4ln..4ln+3} +
+//     {0, 16} of its warp's sub-tile: per k two LDS.128 of A (the 8 row groups
+//     of a warp read 128 contiguous bytes), two of B, 32 packed FMAs.
+//   * K step 16; B quads go to shared memory with 16-byte cp.async, A quads
+//     pass through registers to be transposed into the padded k-major tile.
+//   * A ring of three stages, one barrier per K step.  B is requested two steps
+//     ahead; A is loaded into registers one step before its store, so each load
+//     has a whole compute step to arrive.  160 registers: three CTAs per SM.
+//   * Grouped rasterisation along M, predicated loads (zero fill) and stores.
+// Every product and sum is the scalar kernel's, in the same order, so the
+// results are bit-identical to it.  Measured on GB300 (CUDA events):
+// 60.2 TFLOP/s at 4096^3 against 54.4 for the scalar-FFMA 128 x 128 kernel,
+// 36.2 against 24.3 at 1000^3; 128 x 128 tiles with 16 x 8 packed outputs per
+// thread reached 57.6 (242 registers, two CTAs per SM); K steps 8 and 32, four
+// stages and four CTAs per SM were slower.
+constexpr int G_BM = 128, G_BN = 64, G_BK = 16, G_STAGES = 3;
+constexpr int G_ALD = G_BM + 4;
 struct F2Shared {
-    float As[F2_STAGES][F2_BK][F2_ALD];
-    float Bs[F2_STAGES][F2_BK][B_LD];
+    float As[G_STAGES][G_BK][G_ALD];
+    float Bs[G_STAGES][G_BK][G_BN];
 };
 
 __global__ void __launch_bounds__(THREADS, 2)
-simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ C, int M, int N,
-                  int K)
+simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ C, int M,
+                     int N, int K)
 {
-    __shared__ __align__(16) F2Shared sm;
+    extern __shared__ __align__(16) uint8_t f2_smem[];
+    F2Shared &sm = *reinterpret_cast<F2Shared *>(f2_smem);
+    constexpr int QA = G_BK / 4;                     // quads of k per A row
+    constexpr int LA = G_BM * QA / THREADS;          // 4 A quads per thread and step
+    constexpr int QB = G_BN / 4;                     // quads of n per B row
+    constexpr int LB = G_BK * QB / THREADS;          // 2 B quads per thread and step
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 1, wn = warp & 1;
-    const int lm = lane >> 3, ln = lane & 7;
+    const int lm = lane >> 2, ln = lane & 3;
+    // Linear CTA index -> tile, grouped along M.
+    const int tiles_m = (M + G_BM - 1) / G_BM, tiles_n = (N + G_BN - 1) / G_BN;
     int tm, tn;
-    raster((int)blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
-    const int ktiles = (K + F2_BK - 1) / F2_BK;
+    {
+        const int pid = (int)blockIdx.x;
+        const int per_group = GROUP_M * tiles_n;
+        const int group = pid / per_group;
+        const int first_m = group * GROUP_M;
+        const int gsize = min(tiles_m - first_m, GROUP_M);
+        const int r = pid - group * per_group;
+        tm = first_m + r % gsize;
+        tn = r / gsize;
+    }
+    const int m0 = tm * G_BM, n0 = tn * G_BN;
+    const int ktiles = (K + G_BK - 1) / G_BK;
 
-    // A: 128 rows x 2 quads of k per step, two quads per thread.
-    float4 ra[2];
+    float4 ra[LA];
     auto load_a = [&](int t) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LA; ++i) {
             const int idx = tid + i * THREADS;
-            const int row = idx >> 1, kq = (idx & 1) * 4;
-            const int gm = m0 + row, gk = t * F2_BK + kq;
+            const int row = idx / QA, kq = (idx % QA) * 4;
+            const int gm = m0 + row, gk = t * G_BK + kq;
             ra[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (gm < M && gk < K) ra[i] = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gm * K + gk));
         }
     };
     auto store_a = [&](int stage) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LA; ++i) {
             const int idx = tid + i * THREADS;
-            const int row = idx >> 1, kq = (idx & 1) * 4;
+            const int row = idx / QA, kq = (idx % QA) * 4;
             sm.As[stage][kq + 0][row] = ra[i].x;
             sm.As[stage][kq + 1][row] = ra[i].y;
             sm.As[stage][kq + 2][row] = ra[i].z;
             sm.As[stage][kq + 3][row] = ra[i].w;
         }
     };
-    // B: 8 k-rows x 32 quads of n per step, two quads per thread, by cp.async.
     auto copy_b = [&](int t, int stage) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LB; ++i) {
             const int idx = tid + i * THREADS;
-            const int kr = idx >> 5, nq = (idx & 31) * 4;
-            const int gk = t * F2_BK + kr, gn = n0 + nq;
+            const int kr = idx / QB, nq = (idx % QB) * 4;
+            const int gk = t * G_BK + kr, gn = n0 + nq;
             const bool in = gk < K && gn < N;
             const float *src = in ? B + (size_t)gk * N + gn : B;
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
@@ -354,9 +372,8 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
         }
     };
 
-    // Prologue: steps 0 .. F2_STAGES-2 filled, A of step F2_STAGES-1 in registers.
 #pragma unroll
-    for (int t = 0; t < F2_STAGES - 1; ++t) {
+    for (int t = 0; t < G_STAGES - 1; ++t) {
         if (t < ktiles) {
             copy_b(t, t);
             load_a(t);
@@ -364,62 +381,60 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    if (F2_STAGES - 1 < ktiles) load_a(F2_STAGES - 1);
+    if (G_STAGES - 1 < ktiles) load_a(G_STAGES - 1);
 
-    float2 acc[16][4];  // [row][column pair]
+    float2 acc[8][4];  // [row][column pair]
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-    const int a_off = wm * 64 + lm * 4;  // rows a_off + 16q + {0..3}
-    const int b_off = wn * 64 + ln * 4;  // columns b_off + {0..3} + {0, 32}
+    const int a_off = wm * 64 + lm * 4;  // rows a_off + {0..3} + {0, 32}
+    const int b_off = wn * 32 + ln * 4;  // columns b_off + {0..3} + {0, 16}
 
     for (int t = 0; t < ktiles; ++t) {
-        const int stage = t % F2_STAGES;
-        // this thread's copies of step t have landed; after the barrier every
-        // thread's have, and every thread has finished step t-1
-        asm volatile("cp.async.wait_group %0;" ::"n"(F2_STAGES - 2) : "memory");
+        const int stage = t % G_STAGES;
+        asm volatile("cp.async.wait_group %0;" ::"n"(G_STAGES - 2) : "memory");
         __syncthreads();
-        const int tn_ = t + F2_STAGES - 1;  // step to request now, into the stage step t-1 used
-        if (tn_ < ktiles) {
-            const int st = tn_ % F2_STAGES;
-            copy_b(tn_, st);
+        const int tr = t + G_STAGES - 1;
+        if (tr < ktiles) {
+            const int st = tr % G_STAGES;
+            copy_b(tr, st);
             store_a(st);
-            if (tn_ + 1 < ktiles) load_a(tn_ + 1);
+            if (tr + 1 < ktiles) load_a(tr + 1);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
 #pragma unroll
-        for (int kk = 0; kk < F2_BK; ++kk) {
-            float a[16];
+        for (int kk = 0; kk < G_BK; ++kk) {
+            float a[8];
             float2 b[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = *reinterpret_cast<const float4 *>(&sm.As[stage][kk][a_off + 16 * q]);
+            for (int q = 0; q < 2; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(&sm.As[stage][kk][a_off + 32 * q]);
                 a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const float4 v = *reinterpret_cast<const float4 *>(&sm.Bs[stage][kk][b_off + 32 * h]);
+                const float4 v = *reinterpret_cast<const float4 *>(&sm.Bs[stage][kk][b_off + 16 * h]);
                 b[2 * h] = make_float2(v.x, v.y);
                 b[2 * h + 1] = make_float2(v.z, v.w);
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(make_float2(a[i], a[i]), b[j], acc[i][j]);
         }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 
-    // row i: a_off + 16 (i >> 2) + (i & 3); column pair j: b_off + 32 (j >> 1) + 2 (j & 1)
+    // row i: a_off + 32 (i >> 2) + (i & 3); column pair j: b_off + 16 (j >> 1) + 2 (j & 1)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int gm = m0 + a_off + 16 * (i >> 2) + (i & 3);
+    for (int i = 0; i < 8; ++i) {
+        const int gm = m0 + a_off + 32 * (i >> 2) + (i & 3);
         if (gm >= M) continue;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int gn = n0 + b_off + 32 * h;
+            const int gn = n0 + b_off + 16 * h;
             float *dst = C + (size_t)gm * N + gn;
             const float2 lo = acc[i][2 * h], hi = acc[i][2 * h + 1];
             if (gn + 3 < N) {
@@ -433,6 +448,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
         }
     }
 }
+
 
 // Tile configuration of the SIMT kernel: K step and CTAs per SM.
 #ifndef SIMT_BK
@@ -450,11 +466,14 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     const TIn *B = static_cast<const TIn *>(p.B);
     TOut *C = static_cast<TOut *>(p.C);
     if constexpr (VEC && sizeof(TIn) == 4) {
-        // FP32 problems that fill half a round of resident CTAs: packed FMAs.
-        if (g_simt_ffma2 && 2 * tiles > (long long)num_sms * SIMT_MINB) {
-            simt_ffma2_kernel<<<(unsigned)tiles, THREADS, 0, s>>>(static_cast<const float *>(p.A),
-                                                                 static_cast<const float *>(p.B),
-                                                                 static_cast<float *>(p.C), p.M, p.N, p.K);
+        if (g_simt_ffma2) {
+            const long long tiles2 = (long long)((p.M + G_BM - 1) / G_BM) * ((p.N + G_BN - 1) / G_BN);
+            if (tiles2 > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+            constexpr int smem = (int)sizeof(F2Shared);
+            static_assert(smem <= 48 * 1024, "static launch without the large-shared-memory attribute");
+            simt_ffma2_kernel<<<(unsigned)tiles2, THREADS, smem, s>>>(static_cast<const float *>(p.A),
+                                                                     static_cast<const float *>(p.B),
+                                                                     static_cast<float *>(p.C), p.M, p.N, p.K);
             return cudaGetLastError();
         }
     }
