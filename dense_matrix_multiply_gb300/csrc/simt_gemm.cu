@@ -300,21 +300,35 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 // stages and four CTAs per SM were slower.
 constexpr int G_BM = 128, G_BN = 64, G_BK = 16, G_STAGES = 3;
 constexpr int G_ALD = G_BM + 4;
+template <bool TB>
 struct F2Shared {
     float As[G_STAGES][G_BK][G_ALD];
-    float Bs[G_STAGES][G_BK][G_BN];
+    float Bs[G_STAGES][G_BK][TB ? G_BN + 4 : G_BN];
 };
 
+// EX: the general form (blockIdx.y the batch index, leading dimensions,
+// alpha and beta), TA: A stored [K, M] -- its tile is already k-major and goes
+// to shared memory by cp.async; TB: B stored [N, K] -- its tile passes through
+// registers to be transposed, into rows padded by four floats.
+template <bool EX, bool TA, bool TB>
 __global__ void __launch_bounds__(THREADS, 2)
 simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ C, int M,
-                     int N, int K)
+                  int N, int K, SimtEx ex)
 {
+    static_assert(EX || (!TA && !TB), "transposed operands need the general form");
     extern __shared__ __align__(16) uint8_t f2_smem[];
-    F2Shared &sm = *reinterpret_cast<F2Shared *>(f2_smem);
-    constexpr int QA = G_BK / 4;                     // quads of k per A row
+    F2Shared<TB> &sm = *reinterpret_cast<F2Shared<TB> *>(f2_smem);
+    constexpr int QA = G_BK / 4;                     // quads of k per A row ([M,K] storage)
     constexpr int LA = G_BM * QA / THREADS;          // 4 A quads per thread and step
-    constexpr int QB = G_BN / 4;                     // quads of n per B row
+    constexpr int QB = G_BN / 4;                     // quads of n per B row ([K,N] storage)
     constexpr int LB = G_BK * QB / THREADS;          // 2 B quads per thread and step
+    static_assert(LA == 4 && LB == 2, "tile/thread mapping");
+    const long long lda = EX ? ex.lda : K, ldb = EX ? ex.ldb : N, ldc = EX ? ex.ldc : N;
+    if (EX) {
+        A += (long long)blockIdx.y * ex.sa;
+        B += (long long)blockIdx.y * ex.sb;
+        C += (long long)blockIdx.y * ex.sc;
+    }
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 1, wn = warp & 1;
@@ -335,53 +349,107 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     const int m0 = tm * G_BM, n0 = tn * G_BN;
     const int ktiles = (K + G_BK - 1) / G_BK;
 
-    float4 ra[LA];
+    auto cp16 = [&](float *dst, const float *src, bool in) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                     "l"(in ? src : A), "r"(in ? 16 : 0)
+                     : "memory");
+    };
+    // A stored [M,K]: 128 rows x 4 quads of k per step through registers.
+    float4 ra[TA ? 1 : LA];
     auto load_a = [&](int t) {
+        if constexpr (!TA) {
 #pragma unroll
-        for (int i = 0; i < LA; ++i) {
-            const int idx = tid + i * THREADS;
-            const int row = idx / QA, kq = (idx % QA) * 4;
-            const int gm = m0 + row, gk = t * G_BK + kq;
-            ra[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (gm < M && gk < K) ra[i] = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gm * K + gk));
+            for (int i = 0; i < LA; ++i) {
+                const int idx = tid + i * THREADS;
+                const int row = idx / QA, kq = (idx % QA) * 4;
+                const int gm = m0 + row, gk = t * G_BK + kq;
+                ra[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gm < M && gk < K) ra[i] = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gm * lda + gk));
+            }
         }
     };
     auto store_a = [&](int stage) {
+        if constexpr (!TA) {
 #pragma unroll
-        for (int i = 0; i < LA; ++i) {
-            const int idx = tid + i * THREADS;
-            const int row = idx / QA, kq = (idx % QA) * 4;
-            sm.As[stage][kq + 0][row] = ra[i].x;
-            sm.As[stage][kq + 1][row] = ra[i].y;
-            sm.As[stage][kq + 2][row] = ra[i].z;
-            sm.As[stage][kq + 3][row] = ra[i].w;
+            for (int i = 0; i < LA; ++i) {
+                const int idx = tid + i * THREADS;
+                const int row = idx / QA, kq = (idx % QA) * 4;
+                sm.As[stage][kq + 0][row] = ra[i].x;
+                sm.As[stage][kq + 1][row] = ra[i].y;
+                sm.As[stage][kq + 2][row] = ra[i].z;
+                sm.As[stage][kq + 3][row] = ra[i].w;
+            }
         }
     };
-    auto copy_b = [&](int t, int stage) {
+    // A stored [K,M]: 16 k-rows x 32 quads of m per step by cp.async.
+    auto copy_a = [&](int t, int stage) {
+        if constexpr (TA) {
 #pragma unroll
-        for (int i = 0; i < LB; ++i) {
-            const int idx = tid + i * THREADS;
-            const int kr = idx / QB, nq = (idx % QB) * 4;
-            const int gk = t * G_BK + kr, gn = n0 + nq;
-            const bool in = gk < K && gn < N;
-            const float *src = in ? B + (size_t)gk * N + gn : B;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                             static_cast<uint32_t>(__cvta_generic_to_shared(&sm.Bs[stage][kr][nq]))),
-                         "l"(src), "r"(in ? 16 : 0)
-                         : "memory");
+            for (int i = 0; i < LA; ++i) {
+                const int idx = tid + i * THREADS;
+                const int kr = idx >> 5, mq = (idx & 31) * 4;
+                const int gk = t * G_BK + kr, gm = m0 + mq;
+                cp16(&sm.As[stage][kr][mq], A + (size_t)gk * lda + gm, gk < K && gm < M);
+            }
+        }
+    };
+    // B stored [K,N]: 16 k-rows x 16 quads of n per step by cp.async.
+    auto copy_b = [&](int t, int stage) {
+        if constexpr (!TB) {
+#pragma unroll
+            for (int i = 0; i < LB; ++i) {
+                const int idx = tid + i * THREADS;
+                const int kr = idx / QB, nq = (idx % QB) * 4;
+                const int gk = t * G_BK + kr, gn = n0 + nq;
+                cp16(&sm.Bs[stage][kr][nq], B + (size_t)gk * ldb + gn, gk < K && gn < N);
+            }
+        }
+    };
+    // B stored [N,K]: 64 columns x 4 quads of k per step through registers.
+    float4 rb[TB ? LB : 1];
+    auto load_b = [&](int t) {
+        if constexpr (TB) {
+#pragma unroll
+            for (int i = 0; i < LB; ++i) {
+                const int idx = tid + i * THREADS;
+                const int col = idx / QA, kq = (idx % QA) * 4;
+                const int gn = n0 + col, gk = t * G_BK + kq;
+                rb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (gn < N && gk < K) rb[i] = __ldg(reinterpret_cast<const float4 *>(B + (size_t)gn * ldb + gk));
+            }
+        }
+    };
+    auto store_b = [&](int stage) {
+        if constexpr (TB) {
+#pragma unroll
+            for (int i = 0; i < LB; ++i) {
+                const int idx = tid + i * THREADS;
+                const int col = idx / QA, kq = (idx % QA) * 4;
+                sm.Bs[stage][kq + 0][col] = rb[i].x;
+                sm.Bs[stage][kq + 1][col] = rb[i].y;
+                sm.Bs[stage][kq + 2][col] = rb[i].z;
+                sm.Bs[stage][kq + 3][col] = rb[i].w;
+            }
         }
     };
 
 #pragma unroll
     for (int t = 0; t < G_STAGES - 1; ++t) {
         if (t < ktiles) {
+            copy_a(t, t);
             copy_b(t, t);
             load_a(t);
             store_a(t);
+            load_b(t);
+            store_b(t);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    if (G_STAGES - 1 < ktiles) load_a(G_STAGES - 1);
+    if (G_STAGES - 1 < ktiles) {
+        load_a(G_STAGES - 1);
+        load_b(G_STAGES - 1);
+    }
 
     float2 acc[8][4];  // [row][column pair]
 #pragma unroll
@@ -399,9 +467,14 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
         const int tr = t + G_STAGES - 1;
         if (tr < ktiles) {
             const int st = tr % G_STAGES;
+            copy_a(tr, st);
             copy_b(tr, st);
             store_a(st);
-            if (tr + 1 < ktiles) load_a(tr + 1);
+            store_b(st);
+            if (tr + 1 < ktiles) {
+                load_a(tr + 1);
+                load_b(tr + 1);
+            }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
 #pragma unroll
@@ -427,7 +500,9 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 
-    // row i: a_off + 32 (i >> 2) + (i & 3); column pair j: b_off + 16 (j >> 1) + 2 (j & 1)
+    // row i: a_off + 32 (i >> 2) + (i & 3); column pair j: b_off + 16 (j >> 1) + 2 (j & 1).
+    // The general form scales by alpha and, when beta != 0, adds beta * old C.
+    const bool use_beta = EX && ex.beta != 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int gm = m0 + a_off + 32 * (i >> 2) + (i & 3);
@@ -435,20 +510,42 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int gn = n0 + b_off + 16 * h;
-            float *dst = C + (size_t)gm * N + gn;
+            float *dst = C + (size_t)gm * ldc + gn;
             const float2 lo = acc[i][2 * h], hi = acc[i][2 * h + 1];
+            float v[4] = {lo.x, lo.y, hi.x, hi.y};
+            if (EX) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] *= ex.alpha;
+            }
             if (gn + 3 < N) {
-                *reinterpret_cast<float4 *>(dst) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                if (use_beta) {
+                    const float4 o = *reinterpret_cast<const float4 *>(dst);
+                    v[0] = fmaf(ex.beta, o.x, v[0]);
+                    v[1] = fmaf(ex.beta, o.y, v[1]);
+                    v[2] = fmaf(ex.beta, o.z, v[2]);
+                    v[3] = fmaf(ex.beta, o.w, v[3]);
+                }
+                *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
-                const float v[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (gn + j < N) dst[j] = v[j];
+                    if (gn + j < N) dst[j] = use_beta ? fmaf(ex.beta, dst[j], v[j]) : v[j];
             }
         }
     }
 }
 
+// Launch of the packed-FMA kernel over `batches` batch entries (grid.y).
+template <bool EX, bool TA, bool TB>
+cudaError_t launch_ffma2(const float *A, const float *B, float *C, int M, int N, int K, const SimtEx &ex,
+                         unsigned batches, cudaStream_t s) {
+    const long long tiles = (long long)((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    constexpr int smem = (int)sizeof(F2Shared<TB>);
+    static_assert(smem <= 48 * 1024, "launched without the large-shared-memory attribute");
+    simt_ffma2_kernel<EX, TA, TB><<<dim3((unsigned)tiles, batches, 1), THREADS, smem, s>>>(A, B, C, M, N, K, ex);
+    return cudaGetLastError();
+}
 
 // Tile configuration of the SIMT kernel: K step and CTAs per SM.
 #ifndef SIMT_BK
@@ -466,16 +563,10 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     const TIn *B = static_cast<const TIn *>(p.B);
     TOut *C = static_cast<TOut *>(p.C);
     if constexpr (VEC && sizeof(TIn) == 4) {
-        if (g_simt_ffma2) {
-            const long long tiles2 = (long long)((p.M + G_BM - 1) / G_BM) * ((p.N + G_BN - 1) / G_BN);
-            if (tiles2 > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-            constexpr int smem = (int)sizeof(F2Shared);
-            static_assert(smem <= 48 * 1024, "static launch without the large-shared-memory attribute");
-            simt_ffma2_kernel<<<(unsigned)tiles2, THREADS, smem, s>>>(static_cast<const float *>(p.A),
-                                                                     static_cast<const float *>(p.B),
-                                                                     static_cast<float *>(p.C), p.M, p.N, p.K);
-            return cudaGetLastError();
-        }
+        if (g_simt_ffma2)
+            return launch_ffma2<false, false, false>(static_cast<const float *>(p.A),
+                                                     static_cast<const float *>(p.B), static_cast<float *>(p.C),
+                                                     p.M, p.N, p.K, SimtEx{}, 1, s);
     }
     // A problem too small to fill half of one round of resident CTAs runs as
     // half tiles: twice the CTAs, half the rows each.  (Splitting only the last
@@ -512,9 +603,15 @@ cudaError_t launch_ex_typed(const ProblemEx &p, cudaStream_t s) {
         const TIn *A = static_cast<const TIn *>(p.A) + b0 * p.sa;
         const TIn *B = static_cast<const TIn *>(p.B) + b0 * p.sb;
         TIn *C = static_cast<TIn *>(p.C) + b0 * p.sc;
-        simt_gemm_kernel<TIn, TIn, VEC, SIMT_BK, SIMT_MINB, 128, true, TA, TB>
-            <<<dim3((unsigned)tiles, (unsigned)nb, 1), THREADS, 0, s>>>(A, B, C, p.M, p.N, p.K, 0, ex);
-        const cudaError_t e = cudaGetLastError();
+        cudaError_t e;
+        if constexpr (VEC && sizeof(TIn) == 4) {
+            // float4-able FP32: the packed-FMA kernel
+            e = launch_ffma2<true, TA, TB>(A, B, C, p.M, p.N, p.K, ex, (unsigned)nb, s);
+        } else {
+            simt_gemm_kernel<TIn, TIn, VEC, SIMT_BK, SIMT_MINB, 128, true, TA, TB>
+                <<<dim3((unsigned)tiles, (unsigned)nb, 1), THREADS, 0, s>>>(A, B, C, p.M, p.N, p.K, 0, ex);
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
