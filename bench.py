@@ -59,7 +59,7 @@ L2_BYTES = 129e6
 # ncu capture, keyed by workload; valid only while the kernel's source is the one
 # captured (sha256 prefix of the .cu file), else reported as null.
 TRAFFIC = {
-    "sgemm_f32_rm_4096": {"bytes": 333249792 + 56564480, "source": "11300e4037de"},
+    "sgemm_f32_rm_4096": {"bytes": 332759808 + 56879616, "source": "95b29bce66b1"},
     "hgemm_f16_cm_8192": {"bytes": 1029527000 + 125773056, "source": "4a7c0f78937a"},
     "ffn_bf16_rm_1024x12288x4096": {"bytes": 110070272 + 12095744, "source": "4a7c0f78937a"},
     "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211739648 + 19507968, "source": "4a7c0f78937a"},

@@ -287,29 +287,41 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 //     {0, 16} of its warp's sub-tile: per k two LDS.128 of A (the 8 row groups
 //     of a warp read 128 contiguous bytes), two of B, 32 packed FMAs.
 //   * K step 16; B quads go to shared memory with 16-byte cp.async, A quads
-//     pass through registers to be transposed into the padded k-major tile.
+//     pass through registers to be transposed into the k-major tile, whose
+//     16-byte chunks are XOR-swizzled by k so that the transposing stores of
+//     a warp hit 32 distinct banks (a padded tile left them 2-way conflicted:
+//     61.1 against 62.5 TFLOP/s at 4096^3).
 //   * A ring of three stages, one barrier per K step.  B is requested two steps
 //     ahead; A is loaded into registers one step before its store, so each load
 //     has a whole compute step to arrive.  160 registers: three CTAs per SM.
 //   * Grouped rasterisation along M, predicated loads (zero fill) and stores.
 // Every product and sum is the scalar kernel's, in the same order, so the
 // results are bit-identical to it.  Measured on GB300 (CUDA events):
-// 60.2 TFLOP/s at 4096^3 against 54.4 for the scalar-FFMA 128 x 128 kernel,
-// 36.2 against 24.3 at 1000^3; 128 x 128 tiles with 16 x 8 packed outputs per
+// 62.5 TFLOP/s at 4096^3 against 54.4 for the scalar-FFMA 128 x 128 kernel,
+// 38.9 against 24.3 at 1000^3; 128 x 128 tiles with 16 x 8 packed outputs per
 // thread reached 57.6 (242 registers, two CTAs per SM); K steps 8 and 32, four
 // stages and four CTAs per SM were slower.
 constexpr int G_BM = 128, G_BN = 64, G_BK = 16, G_STAGES = 3;
-constexpr int G_ALD = G_BM + 4;
+constexpr int G_ALD = G_BM;
+// 16-byte chunk c of k-row k of the A tile lives at chunk c ^ a_swz(k): the
+// four k-rows one transposing store instruction writes land in different
+// banks, and the eight chunks of a fragment load stay within one 128-byte row
+// segment.
+__device__ __forceinline__ int a_swz(int k) { return 2 * ((k >> 2) & 3); }
+__device__ __forceinline__ int a_col(int k, int row) { return ((((row >> 2) ^ a_swz(k))) << 2) | (row & 3); }
+// The B tile uses the same swizzle when it is transposed through registers
+// (B stored [N, K]); filled by cp.async it lies unswizzled.
 template <bool TB>
+__device__ __forceinline__ int b_col(int k, int col) { return TB ? a_col(k, col) : col; }
 struct F2Shared {
     float As[G_STAGES][G_BK][G_ALD];
-    float Bs[G_STAGES][G_BK][TB ? G_BN + 4 : G_BN];
+    float Bs[G_STAGES][G_BK][G_BN];
 };
 
 // EX: the general form (blockIdx.y the batch index, leading dimensions,
 // alpha and beta), TA: A stored [K, M] -- its tile is already k-major and goes
 // to shared memory by cp.async; TB: B stored [N, K] -- its tile passes through
-// registers to be transposed, into rows padded by four floats.
+// registers to be transposed into the swizzled layout.
 template <bool EX, bool TA, bool TB>
 __global__ void __launch_bounds__(THREADS, 2)
 simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ C, int M,
@@ -317,7 +329,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
 {
     static_assert(EX || (!TA && !TB), "transposed operands need the general form");
     extern __shared__ __align__(16) uint8_t f2_smem[];
-    F2Shared<TB> &sm = *reinterpret_cast<F2Shared<TB> *>(f2_smem);
+    F2Shared &sm = *reinterpret_cast<F2Shared *>(f2_smem);
     constexpr int QA = G_BK / 4;                     // quads of k per A row ([M,K] storage)
     constexpr int LA = G_BM * QA / THREADS;          // 4 A quads per thread and step
     constexpr int QB = G_BN / 4;                     // quads of n per B row ([K,N] storage)
@@ -375,10 +387,10 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             for (int i = 0; i < LA; ++i) {
                 const int idx = tid + i * THREADS;
                 const int row = idx / QA, kq = (idx % QA) * 4;
-                sm.As[stage][kq + 0][row] = ra[i].x;
-                sm.As[stage][kq + 1][row] = ra[i].y;
-                sm.As[stage][kq + 2][row] = ra[i].z;
-                sm.As[stage][kq + 3][row] = ra[i].w;
+                sm.As[stage][kq + 0][a_col(kq + 0, row)] = ra[i].x;
+                sm.As[stage][kq + 1][a_col(kq + 1, row)] = ra[i].y;
+                sm.As[stage][kq + 2][a_col(kq + 2, row)] = ra[i].z;
+                sm.As[stage][kq + 3][a_col(kq + 3, row)] = ra[i].w;
             }
         }
     };
@@ -390,7 +402,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
                 const int idx = tid + i * THREADS;
                 const int kr = idx >> 5, mq = (idx & 31) * 4;
                 const int gk = t * G_BK + kr, gm = m0 + mq;
-                cp16(&sm.As[stage][kr][mq], A + (size_t)gk * lda + gm, gk < K && gm < M);
+                cp16(&sm.As[stage][kr][a_col(kr, mq)], A + (size_t)gk * lda + gm, gk < K && gm < M);
             }
         }
     };
@@ -426,10 +438,10 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             for (int i = 0; i < LB; ++i) {
                 const int idx = tid + i * THREADS;
                 const int col = idx / QA, kq = (idx % QA) * 4;
-                sm.Bs[stage][kq + 0][col] = rb[i].x;
-                sm.Bs[stage][kq + 1][col] = rb[i].y;
-                sm.Bs[stage][kq + 2][col] = rb[i].z;
-                sm.Bs[stage][kq + 3][col] = rb[i].w;
+                sm.Bs[stage][kq + 0][b_col<TB>(kq + 0, col)] = rb[i].x;
+                sm.Bs[stage][kq + 1][b_col<TB>(kq + 1, col)] = rb[i].y;
+                sm.Bs[stage][kq + 2][b_col<TB>(kq + 2, col)] = rb[i].z;
+                sm.Bs[stage][kq + 3][b_col<TB>(kq + 3, col)] = rb[i].w;
             }
         }
     };
@@ -483,12 +495,12 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             float2 b[4];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const float4 v = *reinterpret_cast<const float4 *>(&sm.As[stage][kk][a_off + 32 * q]);
+                const float4 v = *reinterpret_cast<const float4 *>(&sm.As[stage][kk][a_col(kk, a_off + 32 * q)]);
                 a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const float4 v = *reinterpret_cast<const float4 *>(&sm.Bs[stage][kk][b_off + 16 * h]);
+                const float4 v = *reinterpret_cast<const float4 *>(&sm.Bs[stage][kk][b_col<TB>(kk, b_off + 16 * h)]);
                 b[2 * h] = make_float2(v.x, v.y);
                 b[2 * h + 1] = make_float2(v.z, v.w);
             }
@@ -541,7 +553,7 @@ cudaError_t launch_ffma2(const float *A, const float *B, float *C, int M, int N,
                          unsigned batches, cudaStream_t s) {
     const long long tiles = (long long)((M + G_BM - 1) / G_BM) * ((N + G_BN - 1) / G_BN);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    constexpr int smem = (int)sizeof(F2Shared<TB>);
+    constexpr int smem = (int)sizeof(F2Shared);
     static_assert(smem <= 48 * 1024, "launched without the large-shared-memory attribute");
     simt_ffma2_kernel<EX, TA, TB><<<dim3((unsigned)tiles, batches, 1), THREADS, smem, s>>>(A, B, C, M, N, K, ex);
     return cudaGetLastError();
