@@ -46,6 +46,18 @@ __global__ void zero_fill_bytes_kernel(uint8_t *p, size_t n) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0;
 }
 
+// Zeros `bytes` bytes at p on stream s (16-byte stores when p is aligned).
+cudaError_t zero_fill(void *p, size_t bytes, int num_sms, cudaStream_t s) {
+    const unsigned grid = (unsigned)(num_sms * 4);
+    if (((uintptr_t)p & 15u) == 0) {
+        zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)p, bytes / 16, (uint8_t *)p + (bytes & ~(size_t)15),
+                                              bytes & 15);
+    } else {
+        zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)p, bytes);
+    }
+    return cudaGetLastError();
+}
+
 __device__ __forceinline__ float elt_to_f32(float x) { return x; }
 __device__ __forceinline__ float elt_to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float elt_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -147,14 +159,7 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
 
     if (K == 0) {
         if (t_force != Family::Auto) return GEMM_ERR_INVALID_VALUE;
-        const unsigned grid = (unsigned)(dev->num_sms * 4);
-        if (aligned16(C)) {
-            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)C, c_bytes / 16, (uint8_t *)C + (c_bytes & ~(size_t)15),
-                                                  c_bytes & 15);
-        } else {
-            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)C, c_bytes);
-        }
-        return finish(cudaGetLastError(), "zero_fill");
+        return finish(zero_fill(C, c_bytes, dev->num_sms, s), "zero_fill");
     }
 
     Problem p{A, B, C, M, N, K, elt};
@@ -400,14 +405,7 @@ GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B
     if (st != GEMM_OK) return st;
     cudaStream_t s = t_stream;
     if (K == 0) {
-        const unsigned grid = (unsigned)(dev->num_sms * 4);
-        if (aligned16(C)) {
-            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)C, c_bytes / 16, (uint8_t *)C + (c_bytes & ~(size_t)15),
-                                                  c_bytes & 15);
-        } else {
-            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)C, c_bytes);
-        }
-        return finish(cudaGetLastError(), "zero_fill");
+        return finish(zero_fill(C, c_bytes, dev->num_sms, s), "zero_fill");
     }
     Problem p{A, B, C, M, N, K, Elt::BF16};
     if (!umma_supported(p)) {
@@ -436,14 +434,7 @@ GEMM_API gemm_status_t gemm_bf16_rm_silu_mul(const uint16_t *X, const uint16_t *
     if (st != GEMM_OK) return st;
     cudaStream_t s = t_stream;
     if (K == 0) {  // G = U = 0, SiLU(0) * 0 = 0
-        const unsigned grid = (unsigned)(dev->num_sms * 4);
-        if (aligned16(Z)) {
-            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)Z, z_bytes / 16, (uint8_t *)Z + (z_bytes & ~(size_t)15),
-                                                  z_bytes & 15);
-        } else {
-            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)Z, z_bytes);
-        }
-        return finish(cudaGetLastError(), "zero_fill");
+        return finish(zero_fill(Z, z_bytes, dev->num_sms, s), "zero_fill");
     }
     Problem p{X, Wg, Z, M, N, K, Elt::BF16};
     if (!umma_silu_mul_supported(p, Wu)) {
@@ -487,14 +478,7 @@ GEMM_API gemm_status_t gemm_e4m3_rowscale(const uint8_t *Q, const float *scale, 
     if (st != GEMM_OK) return st;
     cudaStream_t s = t_stream;
     if (K == 0) {
-        const unsigned grid = (unsigned)(dev->num_sms * 4);
-        if (aligned16(C)) {
-            zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)C, c_bytes / 16, (uint8_t *)C + (c_bytes & ~(size_t)15),
-                                                  c_bytes & 15);
-        } else {
-            zero_fill_bytes_kernel<<<grid, 256, 0, s>>>((uint8_t *)C, c_bytes);
-        }
-        return finish(cudaGetLastError(), "zero_fill");
+        return finish(zero_fill(C, c_bytes, dev->num_sms, s), "zero_fill");
     }
     if (!umma_e4m3_supported(Q, Wt, C, N, K)) {
         record_message("gemm_e4m3_rowscale: needs Q, Wt, C 16-byte aligned, K % 16 == 0 and N % 8 == 0");
