@@ -283,6 +283,33 @@ def time_device(fn, steps: int, warmup: int, stream):
     return start.elapsed_time(end)
 
 
+_FLUSH = None
+
+
+def time_device_flushed(fn, steps: int, warmup: int, stream):
+    """CUDA-event time of `steps` calls on `stream`, each timed on its own with
+    the L2 flushed before it (a read of a 512 MiB buffer, four times the L2,
+    leaving clean lines so that the timed call pays no write-backs): ms total,
+    launch latency of every call included.  For problems that fit in L2."""
+    import torch
+    global _FLUSH
+    if _FLUSH is None:
+        _FLUSH = (torch.ones(512 * 1024 * 1024 // 4, device="cuda"), torch.empty(1, device="cuda"))
+    buf, sink = _FLUSH
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        with torch.cuda.stream(stream):
+            torch.sum(buf, dim=0, out=sink)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
 def host_inputs(variant, cfg, M, N, K, da, sa, db, sb):
     """Seeded host buffers of a workload: (A, B, extra)."""
     if variant == "bf16_silu_mul":
@@ -449,20 +476,24 @@ class Cublas:
         return lib.cublasGemmEx(h, self.OP_N, self.OP_N, N, M, K, one, pb, self.R_16BF, N, pa, self.R_16BF, K,
                                 zero, pc, self.R_16BF, N, self.COMPUTE_32F, self.GEMM_DEFAULT)
 
-    def measure(self, variant, M, N, K, dA, dB, dC_like, stream, steps):
+    def measure(self, variant, M, N, K, dA, dB, dC_like, stream, steps, flushed=False, sets=None):
         """{"tflops", "ms_per_step", "mode", "max_abs_diff_vs_library"}: cuBLAS on the
         same device inputs, timed like the library (CUDA events, same stream)."""
         import torch
         self.lib.cublasSetStream_v2(self.handle, self.ct.c_void_p(stream.cuda_stream))
         out = torch.empty_like(dC_like)
-        pa, pb, pc = dA.data_ptr(), dB.data_ptr(), out.data_ptr()
+        pc = out.data_ptr()
+        ab = sets or [(dA.data_ptr(), dB.data_ptr())]   # rotated like the library's calls
+        i = [0]
 
         def step():
+            pa, pb = ab[i[0] % len(ab)]
+            i[0] += 1
             st = self.call(variant, M, N, K, pa, pb, pc)
             if st != 0:
                 raise RuntimeError(f"cuBLAS status {st}")
 
-        ms = time_device(step, steps, 3, stream)
+        ms = (time_device_flushed if flushed else time_device)(step, steps, 3, stream)
         torch.cuda.synchronize()
         if variant == "f32_rm":
             diff = (out - dC_like).abs().max().item()
@@ -477,14 +508,14 @@ class Cublas:
 _CUBLAS = None
 
 
-def cublas_column(variant, M, N, K, dA, dB, dC, stream, steps):
+def cublas_column(variant, M, N, K, dA, dB, dC, stream, steps, flushed=False, sets=None):
     global _CUBLAS
     if variant not in ("f32_rm", "f16_cm", "bf16_rm"):
         return None
     try:
         if _CUBLAS is None:
             _CUBLAS = Cublas()
-        return _CUBLAS.measure(variant, M, N, K, dA, dB, dC, stream, steps)
+        return _CUBLAS.measure(variant, M, N, K, dA, dB, dC, stream, steps, flushed, sets)
     except Exception as e:  # a reference column only: report why it is missing
         return {"unavailable": str(e)[:200]}
 
@@ -539,11 +570,18 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         lib = g.load()
         pa, pb, pq, ps, pc = dA.data_ptr(), dB.data_ptr(), dQ.data_ptr(), dS.data_ptr(), dC.data_ptr()
 
+        e4_sets = [(pa, pb, pq, ps, pc)]
+        e4_i = [0, 0]  # rotation counters of quantize() and product()
+
         def quantize():
-            return lib.gemm_quantize_rows_e4m3(pa, pq, ps, M, K)
+            a, _, q, sc, _ = e4_sets[e4_i[0] % len(e4_sets)]
+            e4_i[0] += 1
+            return lib.gemm_quantize_rows_e4m3(a, q, sc, M, K)
 
         def product():
-            return lib.gemm_e4m3_rowscale(pq, ps, pb, pc, M, N, K)
+            _, b, q, sc, c = e4_sets[e4_i[1] % len(e4_sets)]
+            e4_i[1] += 1
+            return lib.gemm_e4m3_rowscale(q, sc, b, c, M, N, K)
 
         def call():
             return quantize() or product()
@@ -564,10 +602,13 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         A, B = synthetic.problem_inputs(variant, M, N, K, cfg, da, sa, db, sb)
         dA, dB, dC = device_inputs(variant, A, B, M, N)
         fn = getattr(g.load(), ENTRY[variant])
-        pa, pb, pc = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
+        plain_sets = [(dA.data_ptr(), dB.data_ptr(), dC.data_ptr())]
+        plain_i = [0]
 
         def call():
-            return fn(pa, pb, pc, M, N, K)
+            pa_, pb_, pc_ = plain_sets[plain_i[0] % len(plain_sets)]
+            plain_i[0] += 1
+            return fn(pa_, pb_, pc_, M, N, K)
 
     def step():
         st = call()
@@ -578,21 +619,42 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     g.gemm_synchronize()
     kernel = g.gemm_last_kernel()
     kind = kernel_kind(kernel)
+
+    footprint = sum(t.numel() * t.element_size() for t in [dA, dB, dC] + ([dWu] if extra else [])
+                    + ([dQ, dS] if variant == "e4m3_rowscale" else []))
+    # Operands that fit in L2 would stay there between calls.  Then the calls
+    # rotate over R copies of them, R x footprint > 3 x L2, so that every call
+    # reads its operands from DRAM (as consecutive layers of a model would),
+    # timed back to back.
+    rotated = 1
+    keep = []
+    if footprint <= L2_BYTES and (variant in ENTRY or variant == "e4m3_rowscale"):
+        rotated = int(min(512, -(-3 * int(L2_BYTES) // max(1, footprint))))
+        for _ in range(rotated - 1):
+            if variant in ENTRY:
+                a2, b2, c2 = dA.clone(), dB.clone(), torch.empty_like(dC)
+                keep += [a2, b2, c2]
+                plain_sets.append((a2.data_ptr(), b2.data_ptr(), c2.data_ptr()))
+            else:
+                a2, b2, q2, s2, c2 = dA.clone(), dB.clone(), torch.empty_like(dQ), torch.empty_like(dS), \
+                    torch.empty_like(dC)
+                keep += [a2, b2, q2, s2, c2]
+                e4_sets.append((a2.data_ptr(), b2.data_ptr(), q2.data_ptr(), s2.data_ptr(), c2.data_ptr()))
+    flushed = footprint <= L2_BYTES and rotated == 1
     split = {}
     if variant == "e4m3_rowscale":
         # each kernel of the step timed on its own: the product is the dominant
         # (tensor-bound) kernel, the quantisation is HBM-bound
         for nm, fn1 in (("quantize", quantize), ("product", product)):
-            ms1 = time_device(fn1, steps, 3, stream)
+            ms1 = (time_device_flushed if flushed else time_device)(fn1, steps, 3, stream)
             split[nm] = ms1 / steps
-
     sampler = ClockSampler(sampler_uuid) if clocks else None
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     time.sleep(0.2 if clocks else 0)
     t_host0 = time.time()
-    ms = time_device(step, steps, 0, stream)
+    ms = (time_device_flushed if flushed else time_device)(step, steps, 0, stream)
     t_host1 = time.time()
     g.gemm_synchronize()
     clk = None
@@ -610,12 +672,18 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         "ms_per_step": ms / steps, "tflops": flops / s_per / 1e12, "steps": steps, "ms_total": ms,
         "roofline": roofline_for(kind, variant, M, N, K, s_kernel, peaks, peaks_src,
                                  clk["sm_mhz"] if clk else None, sms, name, prop_mhz),
-        "clocks": clk, "footprint_bytes": int(dA.numel() * dA.element_size() + dB.numel() * dB.element_size()
-                                              + dC.numel() * dC.element_size()),
+        "clocks": clk, "footprint_bytes": int(footprint),
+        "l2": (f"{footprint / 2**20:.1f} MiB of operands fit in the 129 MB L2: calls rotate over {rotated} "
+               f"copies ({rotated * footprint / 2**20:.0f} MiB), each read from DRAM, back to back"
+               if rotated > 1 else
+               f"flushed before every timed call (read of a 512 MiB buffer): {footprint / 2**20:.0f} MiB of "
+               f"operands fit in the 129 MB L2" if flushed else
+               f"no flush: {footprint / 2**20:.0f} MiB of operands > 129 MB L2"),
     }
 
     if cublas and variant in ("f32_rm", "f16_cm", "bf16_rm"):
-        res["cublas"] = cublas_column(variant, M, N, K, dA, dB, dC, stream, steps)
+        res["cublas"] = cublas_column(variant, M, N, K, dA, dB, dC, stream, steps, flushed,
+                                      [(p_[0], p_[1]) for p_ in plain_sets] if variant in ENTRY else None)
     if split:
         q_bytes = 2 * M * K + M * K + 4 * M  # read A once, write the codes and the scales
         res["kernels"] = {
@@ -662,7 +730,7 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         res["cpu_baseline"] = {"value": fps / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                "sample": f"{nrows} of {M} output rows ({nrows}x{N}x{K} FMAs, FP64 oracle) "
                                          f"in {dt:.1f} s"}
-    del dA, dB, dC
+    del dA, dB, dC, keep
     torch.cuda.empty_cache()
     return res
 
@@ -709,7 +777,7 @@ def run_ours(args):
             r = measure_workload(wl, max(5, args.path_steps), 3, peaks, peaks_src, sms, stream,
                                  sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True, prop_mhz=prop_mhz)
             paths.append({k: r[k] for k in ("workload", "kernel", "M", "N", "K", "ms_per_step", "tflops",
-                                            "roofline", "clocks", "kernels", "cublas") if k in r})
+                                            "roofline", "clocks", "kernels", "cublas", "l2") if k in r})
 
     if rank == 0:
         M, N, K = res["M"], res["N"], res["K"]
@@ -725,8 +793,7 @@ def run_ours(args):
                        "layout": "column-major" if res["variant"].endswith("_cm") else "row-major",
                        "inputs": "uniform[-1,1] seeded SplitMix64" if "ffn" not in args.workload
                        else "X~N(0,1), W~N(0,1/4096) seeded SplitMix64",
-                       "l2": f"no flush: A+B+C = {res['footprint_bytes'] / 2**20:.0f} MiB "
-                             f"{'>' if res['footprint_bytes'] > L2_BYTES else '<='} 129 MB L2",
+                       "l2": res["l2"],
                        "parallelism": f"replicas x{world}"},
             "kernel": res["kernel"],
             "roofline": res["roofline"],

@@ -34,6 +34,7 @@
 //     expiry the thread records a code in the status word, raises a CTA-wide
 //     abort flag, waits (bounded) for its own asynchronous work and leaves; the
 //     tensor memory is always released.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -46,6 +47,8 @@
 namespace gemm_gb300 {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int BM = 128, BN = 256, BK = 64, UMMA_K = 16;
 constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;            // 16 KiB
@@ -57,6 +60,12 @@ constexpr int GROUP_M = 8;
 constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 
 constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
+
+// Whether one-row-tile problems with few column tiles split K over clusters.
+#ifndef UMMA_SPLITK
+#define UMMA_SPLITK 1
+#endif
+constexpr bool g_umma_splitk = UMMA_SPLITK != 0;
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + SMEM_TILES + 256 /*barriers*/;
 
 // Status codes ORed into the device status word.
@@ -1012,6 +1021,203 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
+// ------------------------------------------------------ skinny M: split K
+// For M <= 128 (one row tile) the single-CTA kernel has only ceil(N / 256)
+// tiles: for a decode-shaped projection (N = 12288) 48 of the SMs would stream
+// the weights and the rest would idle.  Here a cluster of CS CTAs shares each
+// 128 x 256 tile, CTA r taking k-blocks [r*KB/CS, (r+1)*KB/CS), so that every
+// SM streams its share of B.  Each CTA copies its FP32 partial (rows < M only)
+// from tensor memory into its shared memory (the operand stages are free by
+// then); rank 0 adds the partials of ranks 0 .. CS-1 in that order through
+// distributed shared memory, rounds once and stores C.  Deterministic, no
+// atomics, one launch.  Every barrier wait is bounded as in the single-CTA
+// kernel; the two cluster barriers are reached by every thread on every path.
+constexpr int SK_LD = BN + 4;   // floats per row of a partial tile (16-byte rows, 8 bank offsets)
+constexpr uint32_t SK_TMEM_COLS = 256;
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+template <typename T, uint32_t AB_FORMAT>
+__global__ void __launch_bounds__(THREADS, 1)
+umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   T *__restrict__ C, int M, int N, int K, int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *a_tiles = smem;
+    uint8_t *b_tiles = smem + STAGES * A_STAGE;
+    float *part = reinterpret_cast<float *>(smem);  // [M][SK_LD] once the stages are drained
+    Bars *bars = reinterpret_cast<Bars *>(smem + SMEM_TILES);
+    volatile int *abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank(), cs = cluster_nctarank();
+    const int n0 = (int)cluster_id_x() * BN;
+    const int num_kb = (K + BK - 1) / BK;
+    const int kb0 = (int)(((long long)num_kb * rank) / cs), kb1 = (int)(((long long)num_kb * (rank + 1)) / cs);
+    const bool has_work = kb1 > kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->acc_full[0], 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, SK_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        const int n_left = N - n0;
+        const int boxes = n_left >= BN ? 4 : (n_left + 63) / 64;
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, true)) {
+                atomicOr(status, ST_PRODUCER);
+                *abort_flag = 1;
+                break;
+            }
+            mbar_arrive_expect_tx(&bars->full[stage], (uint32_t)(A_STAGE + boxes * B_BOX));
+            tma_load_2d(a_tiles + stage * A_STAGE, &tmA, &bars->full[stage], kb * BK, 0);
+            for (int j = 0; j < boxes; ++j)
+                tma_load_2d(b_tiles + stage * B_STAGE + j * B_BOX, &tmB, &bars->full[stage], n0 + j * 64, kb * BK);
+            ++issued;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        // Let every load this thread issued land before the stages are reused.
+        for (long long i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i) {
+            const int s = (int)(i % STAGES);
+            const uint32_t par = (uint32_t)((i / STAGES) & 1);
+            if (!mbar_wait(&bars->full[s], par, abort_flag, false)) {
+                atomicOr(status, ST_DRAIN);
+                break;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = make_idesc(AB_FORMAT);
+        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(a_tiles), 16, 1024);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_tiles), B_BOX, 1024);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ad = a_desc0 + (uint64_t)((stage * A_STAGE) >> 4);
+            const uint64_t bd = b_desc0 + (uint64_t)((stage * B_STAGE) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < BK / UMMA_K; ++ks)
+                umma(tmem_base, ad + ks * (32u >> 4), bd + ks * (2048u >> 4), idesc, (kb != kb0 || ks != 0));
+            umma_commit(&bars->empty[stage]);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) {
+            umma_commit(&bars->acc_full[0]);
+        } else {
+            atomicOr(status, ST_MMA);
+            *abort_flag = 1;
+        }
+        umma_commit(&bars->drain);
+        if (!mbar_wait(&bars->drain, 0, abort_flag, false)) atomicOr(status, ST_DRAIN);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ partials
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int row = quarter * 32 + lane;
+        bool ready = true;
+        if (has_work && !mbar_wait(&bars->acc_full[0], 0, abort_flag, true)) {
+            atomicOr(status, ST_EPILOGUE);
+            *abort_flag = 1;
+            ready = false;
+        }
+        tc_fence_after();
+        if (quarter * 32 < M) {  // warp-uniform
+#pragma unroll 1
+            for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                uint32_t r[32];
+                if (has_work && ready) {
+                    tmem_ld_32cols(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(chunk * 32), r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;
+                }
+                if (row < M) {
+                    float4 *dst = reinterpret_cast<float4 *>(part + row * SK_LD + chunk * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();  // every partial is in its CTA's shared memory, visible cluster-wide
+
+    if (rank == 0) {
+        // ------------------------------------------------------------ reduction
+        // Thread t takes groups of four columns; the partials of ranks 0 .. cs-1
+        // are added in that order (16-byte loads through distributed shared
+        // memory, all issued before the additions).
+        cg::cluster_group cluster = cg::this_cluster();
+        const int cols = min(BN, N - n0);
+        const int groups = (cols + 3) / 4;
+        for (int e = threadIdx.x; e < M * groups; e += THREADS) {
+            const int r = e / groups, c = (e - r * groups) * 4;
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < (int)cs)
+                    v[j] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(part + r * SK_LD + c, j));
+            float4 acc = v[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) {
+                if (j < (int)cs) {
+                    acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+                }
+            }
+            T *dst = C + (size_t)r * N + n0 + c;
+            if (c + 4 <= cols) {
+                uint2 w;
+                w.x = pack2(acc.x, acc.y, (T *)nullptr);
+                w.y = pack2(acc.z, acc.w, (T *)nullptr);
+                *reinterpret_cast<uint2 *>(dst) = w;   // N % 8 == 0 and C 16-byte aligned
+            } else {
+                const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                for (int q = 0; q < cols - c; ++q) store1(dst + q, a4[q]);
+            }
+        }
+    }
+    __syncwarp();
+    cluster_sync();  // peers keep their shared memory until rank 0 has read it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, SK_TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -1074,6 +1280,71 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     kern<<<grid, A_CPASYNC ? THREADS + 128 : THREADS, SMEM_BYTES, s>>>(
         ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K, status, stall);
     return cudaGetLastError();
+}
+
+// Largest number of co-resident clusters of cs CTAs of the skinny-M kernel
+// (cs = 2, 4 or 8), per device and element type.
+int splitk_clusters_max(Elt elt, int cs, int dev) {
+    static std::atomic<int> cached[64][2][3];
+    static std::once_flag once[64][2][3];
+    const int t = elt == Elt::BF16 ? 1 : 0, ci = cs == 2 ? 0 : cs == 4 ? 1 : 2;
+    std::call_once(once[dev & 63][t][ci], [&] {
+        const void *kern = t ? reinterpret_cast<const void *>(umma_splitk_kernel<__nv_bfloat16, 1>)
+                             : reinterpret_cast<const void *>(umma_splitk_kernel<__half, 0>);
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)cs, 1, 1);
+            cfg.blockDim = dim3(THREADS, 1, 1);
+            cfg.dynamicSmemBytes = SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        cached[dev & 63][t][ci].store(n);
+    });
+    return cached[dev & 63][t][ci].load();
+}
+
+// Split-K launch of the skinny-M kernel: ceil(N / 256) clusters of cs CTAs.
+template <typename T, uint32_t F>
+cudaError_t launch_splitk_typed(const Problem &p, int cs, int *status, cudaStream_t s) {
+    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, p.A, dt, p.M, p.K, BM, BK) || !make_map(&tb, p.B, dt, p.K, p.N, BK, 64))
+        return cudaErrorInvalidValue;
+    auto kern = umma_splitk_kernel<T, F>;
+    static std::atomic<uint64_t> attr_done{0};  // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_release);
+    }
+    const long long tiles_n = (p.N + BN - 1) / BN;
+    if (tiles_n * cs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles_n * cs), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, status);
 }
 
 // 3-D tensor map of `batch` matrices of [outer, inner] 16-bit elements: row
@@ -1341,6 +1612,25 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
         }
         return p.elt == Elt::BF16 ? launch_typed<__nv_bfloat16, 1, true>(p, num_sms, status, s)
                                   : launch_typed<__half, 0, true>(p, num_sms, status, s);
+    }
+    // A few rows (M <= 64) and too few column tiles to occupy the GPU: split K
+    // over clusters -- the largest of 8, 4, 2 CTAs whose clusters all fit on the
+    // GPU at once (a cluster of CTAs with this much shared memory needs that
+    // many SMs of one GPC: 76, 36 and 15 clusters of 2, 4 and 8 fit on a GB300).
+    // Measured at N = 12288, K = 4096: M = 32 in 27.3 us against 31.3 unsplit;
+    // at M = 128 the larger cluster reduction made it slower (37.3 vs 34.8).
+    if (p.M <= 64 && g_umma_splitk) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const long long tiles_n = (p.N + BN - 1) / BN;
+        const long long num_kb = (p.K + BK - 1) / BK;
+        int cs = 0;
+        for (int c = 8; c >= 2 && cs == 0; c /= 2)
+            if (num_kb >= c && splitk_clusters_max(p.elt, c, dev) >= tiles_n) cs = c;
+        if (cs >= 2)
+            return p.elt == Elt::BF16 ? launch_splitk_typed<__nv_bfloat16, 1>(p, cs, status, s)
+                                      : launch_splitk_typed<__half, 0>(p, cs, status, s);
     }
     // 256-row tiles on CTA pairs once M fills more than one 128-row tile.
     if (p.M > BM) {

@@ -109,14 +109,23 @@ MID_CASES = [
     ("bf16_rm", 520, 1032, 260, None, "umma_bf16"),         # unaligned A staged, CTA pairs
     ("f16_cm", 1032, 520, 260, None, "umma_f16"),
     ("bf16_rm", 256, 256, 256, "simt_scalar", "simt_bf16_scalar"),
-    ("bf16_rm", 4, 520, 1000, None, "gemv_bf16_vec"),
+    ("bf16_rm", 4, 520, 1000, "gemv", "gemv_bf16_vec"),
+    ("bf16_rm", 4, 520, 1000, None, "umma_bf16"),            # skinny M: split K over a cluster
     ("bf16_rm", 7, 130, 77, None, "gemv_bf16_scalar"),
     ("bf16_rm", 16, 256, 64, "umma", "umma_bf16"),
     ("f16_cm", 512, 256, 512, None, "umma_f16"),
     ("f16_cm", 264, 300, 520, None, "umma_f16"),
     ("f16_cm", 300, 264, 520, None, "simt_f16_scalar"),
     ("f16_cm", 250, 3, 128, None, "gemv_f16_scalar"),
-    ("f16_cm", 1000, 8, 1000, None, "gemv_f16_vec"),
+    ("f16_cm", 1000, 8, 1000, "gemv", "gemv_f16_vec"),
+    ("f16_cm", 1000, 8, 1000, None, "umma_f16"),
+    ("bf16_rm", 1, 1024, 512, "umma", "umma_bf16"),          # split K: 4 tiles x 8 ranks
+    ("bf16_rm", 2, 264, 128, None, "umma_bf16"),             # 2 tiles x 2 ranks
+    ("bf16_rm", 64, 2048, 4096, None, "umma_bf16"),          # 8 tiles x 8 ranks
+    ("bf16_rm", 60, 520, 1000, None, "umma_bf16"),           # ragged N and K
+    ("bf16_rm", 40, 5000, 520, None, "umma_bf16"),           # 20 tiles x 4 ranks
+    ("bf16_rm", 33, 10240, 256, None, "umma_bf16"),          # 40 tiles x 2 ranks
+    ("f16_cm", 2000, 128, 2056, None, "umma_f16"),           # row-major M = 128, N = 2000
 ]
 
 
