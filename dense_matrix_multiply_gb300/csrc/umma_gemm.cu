@@ -1,10 +1,19 @@
-// Tensor-core GEMM for 16-bit inputs on sm_103a: tcgen05 MMA, TMEM
-// accumulators, TMA loads, warp specialisation, persistent tile loop.
+// Tensor-core GEMM on sm_103a: tcgen05 MMA, TMEM accumulators, TMA loads,
+// warp specialisation, persistent tile loops.  The file holds four kernels:
+//   * umma_gemm_kernel -- one CTA per 128 x 256 tile (M <= 128, and A rows that
+//     only 8-byte cp.async can fetch); described first, below;
+//   * umma_pair_kernel -- 256 x 256 tiles on 2-CTA clusters (cta_group::2), the
+//     kernel of every larger problem, of the general form (3-D tensor maps,
+//     either major-ness, alpha/beta, batches), of the fused FFN gate/up
+//     projection (DUAL) and of the row-scaled E4M3 product (F8,
+//     kind::f8f6f4);
+//   * umma_splitk_kernel -- M <= 64 with few column tiles: K split over a
+//     cluster, partials reduced through distributed shared memory.
 //
-// Problem (row-major, tight): C[M,N] = A[M,K] · B[K,N], A and B both f16 or
-// both bf16, FP32 accumulation in tensor memory, one rounding to the output
-// type.  A is K-major (k contiguous); B is MN-major (n contiguous).  The
-// column-major half entry point reaches this kernel through C^T = B^T · A^T.
+// Problem (row-major): C[M,N] = A[M,K] · B[K,N], A and B both f16 or both bf16
+// (or both E4M3 codes), FP32 accumulation in tensor memory, one rounding to
+// the output type.  The column-major half entry point reaches these kernels
+// through C^T = B^T · A^T.
 //
 // Prior art and what is kept ("Chapter 5 Operators and Runtime", section 5.1.5
 // on asynchronous matrix instructions fed from shared memory, producer and
