@@ -229,3 +229,41 @@ def test_plain_case_matches_the_plain_entry_point():
     g.gemm_ex("bf16", "rm", "N", "N", M, N, K, 1.0, dA, K, 0, dB, N, 0, 0.0, c2, N, 0, 1)
     g.gemm_synchronize()
     assert torch.equal(c1, c2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_overlapping_batches_of_A(dtype):
+    """Batch strides smaller than a matrix (a sliding window over A's rows) are
+    legal for the operands that are only read."""
+    M, N, K, batch = 136, 200, 64, 3
+    lda = K
+    sa = 8 * lda                     # each A_b starts 8 rows after A_{b-1}
+    A = synthetic.matrix(dtype, M + 8 * (batch - 1), K, synthetic.seed_for(SEED, 40))
+    B = synthetic.matrix(dtype, batch * K, N, synthetic.seed_for(SEED, 41))
+    C0 = np.zeros(batch * M * N, dtype=np.float32 if dtype == "f32" else np.uint16)
+    dA, dB, dC = dev(A), dev(B), dev(C0)
+    g.gemm_ex(dtype, "rm", "N", "N", M, N, K, 1.0, dA, lda, sa, dB, N, K * N, 0.0, dC, N, M * N, batch)
+    g.gemm_synchronize()
+    out = widen(dtype, host(dC, dtype)).reshape(batch, M, N)
+    ref = oracle.gemm_ex(dtype, "rm", "N", "N", M, N, K, 1.0, A, lda, sa, B, N, K * N, 0.0, None, N, M * N, batch)
+    check(dtype, out, ref, K, 1.0)
+
+
+def test_column_major_batched_half_sampled():
+    """Column-major f16, A transposed, 16 batch entries of 512 x 768 x 1024 on
+    the tensor cores; every output of entries 0 and 15 against the oracle."""
+    M, N, K, batch = 512, 768, 1024, 16
+    A = synthetic.matrix("f16", batch * M, K, synthetic.seed_for(SEED, 42))    # A_b^T stored [K, M] col-major
+    B = synthetic.matrix("f16", batch * K, N, synthetic.seed_for(SEED, 43))
+    C0 = np.zeros(batch * M * N, dtype=np.uint16)
+    dA, dB, dC = dev(A), dev(B), dev(C0)
+    # column-major: A stored K x M (op T) with lda = K, B stored K x N with ldb = K, C M x N with ldc = M
+    g.gemm_ex("f16", "cm", "T", "N", M, N, K, 1.0, dA, K, M * K, dB, K, K * N, 0.0, dC, M, M * N, batch)
+    assert g.gemm_last_kernel() == "umma_ex_f16"
+    g.gemm_synchronize()
+    out = widen("f16", host(dC, "f16"))
+    for b in (0, batch - 1):
+        ref = oracle.gemm_ex("f16", "cm", "T", "N", M, N, K, 1.0, A[b * M * K:(b + 1) * M * K], K, 0,
+                             B[b * K * N:(b + 1) * K * N], K, 0, 0.0, None, M, 0, 1)
+        got = out[b * M * N:(b + 1) * M * N].reshape(N, M).T[None]
+        check("f16", got, ref, K, 1.0)
