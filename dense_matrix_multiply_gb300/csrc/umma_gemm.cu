@@ -75,6 +75,13 @@ constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
 #define UMMA_SPLITK 1
 #endif
 constexpr bool g_umma_splitk = UMMA_SPLITK != 0;
+// Narrowest column tile and largest cluster of the cluster split.
+#ifndef SPLITK_MIN_BN
+#define SPLITK_MIN_BN 128
+#endif
+#ifndef SPLITK_MAX_CS
+#define SPLITK_MAX_CS 8
+#endif
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + SMEM_TILES + 256 /*barriers*/;
 
 // Status codes ORed into the device status word.
@@ -1034,14 +1041,22 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // For M <= 128 (one row tile) the single-CTA kernel has only ceil(N / 256)
 // tiles: for a decode-shaped projection (N = 12288) 48 of the SMs would stream
 // the weights and the rest would idle.  Here a cluster of CS CTAs shares each
-// 128 x 256 tile, CTA r taking k-blocks [r*KB/CS, (r+1)*KB/CS), so that every
-// SM streams its share of B.  Each CTA copies its FP32 partial (rows < M only)
-// from tensor memory into its shared memory (the operand stages are free by
-// then); rank 0 adds the partials of ranks 0 .. CS-1 in that order through
-// distributed shared memory, rounds once and stores C.  Deterministic, no
-// atomics, one launch.  Every barrier wait is bounded as in the single-CTA
-// kernel; the two cluster barriers are reached by every thread on every path.
-constexpr int SK_LD = BN + 4;   // floats per row of a partial tile (16-byte rows, 8 bank offsets)
+// 128 x bn tile (bn = 128, 192 or 256), CTA r taking k-blocks
+// [r*KB/CS, (r+1)*KB/CS), so that most SMs stream their share of B.  A stage
+// holds only M rows of A (rounded up to 8): a 128-row box would have TMA
+// zero-fill the rest on every stage, which measured 31 against 24 us at
+// M = 2..8.  Each CTA copies its FP32 partial (rows < M only) from tensor
+// memory into its shared memory (the operand stages are free by then); the
+// tile's (row, column group) pairs are dealt out to the CS CTAs, and each adds
+// the partials of ranks 0 .. CS-1 in that order through distributed shared
+// memory, rounds once and stores C.  Deterministic, no atomics, one launch, no
+// workspace.  Every barrier wait is bounded as in the single-CTA kernel; the
+// two cluster barriers are reached by every thread on every path.
+constexpr int SK_LD = BN + 4;
+// Rows of A a stage holds: M rounded up to the 8-row swizzle atom.  The MMA
+// still reads 128 rows; rows past these hold stale shared memory and only
+// reach accumulator rows that are never stored.
+__host__ __device__ constexpr int splitk_a_rows(int M) { return M >= BM ? BM : (M + 7) / 8 * 8; }   // floats per row of a partial tile (16-byte rows, 8 bank offsets)
 constexpr uint32_t SK_TMEM_COLS = 256;
 
 __device__ __forceinline__ uint32_t cluster_nctarank() {
@@ -1053,7 +1068,7 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 template <typename T, uint32_t AB_FORMAT>
 __global__ void __launch_bounds__(THREADS, 1)
 umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   T *__restrict__ C, int M, int N, int K, int *status)
+                   T *__restrict__ C, int M, int N, int K, int bn, int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -1066,7 +1081,7 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank(), cs = cluster_nctarank();
-    const int n0 = (int)cluster_id_x() * BN;
+    const int n0 = (int)cluster_id_x() * bn;
     const int num_kb = (K + BK - 1) / BK;
     const int kb0 = (int)(((long long)num_kb * rank) / cs), kb1 = (int)(((long long)num_kb * (rank + 1)) / cs);
     const bool has_work = kb1 > kb0;
@@ -1095,7 +1110,7 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer
         const int n_left = N - n0;
-        const int boxes = n_left >= BN ? 4 : (n_left + 63) / 64;
+        const int boxes = n_left >= bn ? bn / 64 : (n_left + 63) / 64;
         int stage = 0;
         uint32_t phase = 0;
         long long issued = 0;
@@ -1105,7 +1120,7 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 *abort_flag = 1;
                 break;
             }
-            mbar_arrive_expect_tx(&bars->full[stage], (uint32_t)(A_STAGE + boxes * B_BOX));
+            mbar_arrive_expect_tx(&bars->full[stage], (uint32_t)(splitk_a_rows(M) * BK * 2 + boxes * B_BOX));
             tma_load_2d(a_tiles + stage * A_STAGE, &tmA, &bars->full[stage], kb * BK, 0);
             for (int j = 0; j < boxes; ++j)
                 tma_load_2d(b_tiles + stage * B_STAGE + j * B_BOX, &tmB, &bars->full[stage], n0 + j * 64, kb * BK);
@@ -1123,7 +1138,7 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = make_idesc(AB_FORMAT);
+        const uint32_t idesc = make_idesc(AB_FORMAT, BM, (uint32_t)bn);
         const uint64_t a_desc0 = smem_desc_sw128(smem_u32(a_tiles), 16, 1024);
         const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_tiles), B_BOX, 1024);
         int stage = 0;
@@ -1161,7 +1176,7 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         tc_fence_after();
         if (quarter * 32 < M) {  // warp-uniform
 #pragma unroll 1
-            for (int chunk = 0; chunk < BN / 32; ++chunk) {
+            for (int chunk = 0; chunk < bn / 32; ++chunk) {
                 uint32_t r[32];
                 if (has_work && ready) {
                     tmem_ld_32cols(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(chunk * 32), r);
@@ -1185,15 +1200,18 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncwarp();
     cluster_sync();  // every partial is in its CTA's shared memory, visible cluster-wide
 
-    if (rank == 0) {
+    {
         // ------------------------------------------------------------ reduction
-        // Thread t takes groups of four columns; the partials of ranks 0 .. cs-1
-        // are added in that order (16-byte loads through distributed shared
-        // memory, all issued before the additions).
+        // The (row, four-column group) pairs of the tile are dealt out to the
+        // cs CTAs in equal contiguous ranges; for each, the partials of ranks
+        // 0 .. cs-1 are added in that order (16-byte loads through distributed
+        // shared memory, all issued before the additions).
         cg::cluster_group cluster = cg::this_cluster();
-        const int cols = min(BN, N - n0);
+        const int cols = min(bn, N - n0);
         const int groups = (cols + 3) / 4;
-        for (int e = threadIdx.x; e < M * groups; e += THREADS) {
+        const int total = M * groups;
+        const int e0 = (int)(((long long)total * rank) / cs), e1 = (int)(((long long)total * (rank + 1)) / cs);
+        for (int e = e0 + threadIdx.x; e < e1; e += THREADS) {
             const int r = e / groups, c = (e - r * groups) * 4;
             float4 v[8];
 #pragma unroll
@@ -1220,7 +1238,7 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
     }
     __syncwarp();
-    cluster_sync();  // peers keep their shared memory until rank 0 has read it
+    cluster_sync();  // every CTA keeps its shared memory until the others have read it
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, SK_TMEM_COLS);
@@ -1292,11 +1310,12 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
 }
 
 // Largest number of co-resident clusters of cs CTAs of the skinny-M kernel
-// (cs = 2, 4 or 8), per device and element type.
+// (2 <= cs <= 8), per device and element type.
 int splitk_clusters_max(Elt elt, int cs, int dev) {
-    static std::atomic<int> cached[64][2][3];
-    static std::once_flag once[64][2][3];
-    const int t = elt == Elt::BF16 ? 1 : 0, ci = cs == 2 ? 0 : cs == 4 ? 1 : 2;
+    static std::atomic<int> cached[64][2][9];
+    static std::once_flag once[64][2][9];
+    if (cs < 2 || cs > 8) return 0;
+    const int t = elt == Elt::BF16 ? 1 : 0, ci = cs;
     std::call_once(once[dev & 63][t][ci], [&] {
         const void *kern = t ? reinterpret_cast<const void *>(umma_splitk_kernel<__nv_bfloat16, 1>)
                              : reinterpret_cast<const void *>(umma_splitk_kernel<__half, 0>);
@@ -1321,12 +1340,13 @@ int splitk_clusters_max(Elt elt, int cs, int dev) {
     return cached[dev & 63][t][ci].load();
 }
 
-// Split-K launch of the skinny-M kernel: ceil(N / 256) clusters of cs CTAs.
+// Split-K launch of the skinny-M kernel: ceil(N / bn) clusters of cs CTAs,
+// bn = 128, 192 or 256 columns per tile.
 template <typename T, uint32_t F>
-cudaError_t launch_splitk_typed(const Problem &p, int cs, int *status, cudaStream_t s) {
+cudaError_t launch_splitk_typed(const Problem &p, int cs, int bn, int *status, cudaStream_t s) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, p.A, dt, p.M, p.K, BM, BK) || !make_map(&tb, p.B, dt, p.K, p.N, BK, 64))
+    if (!make_map(&ta, p.A, dt, p.M, p.K, splitk_a_rows(p.M), BK) || !make_map(&tb, p.B, dt, p.K, p.N, BK, 64))
         return cudaErrorInvalidValue;
     auto kern = umma_splitk_kernel<T, F>;
     static std::atomic<uint64_t> attr_done{0};  // one bit per device
@@ -1339,7 +1359,8 @@ cudaError_t launch_splitk_typed(const Problem &p, int cs, int *status, cudaStrea
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit, std::memory_order_release);
     }
-    const long long tiles_n = (p.N + BN - 1) / BN;
+    if (bn % 64 != 0 || bn < 64 || bn > BN) return cudaErrorInvalidValue;
+    const long long tiles_n = (p.N + bn - 1) / bn;
     if (tiles_n * cs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles_n * cs), 1, 1);
@@ -1353,7 +1374,7 @@ cudaError_t launch_splitk_typed(const Problem &p, int cs, int *status, cudaStrea
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, status);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, bn, status);
 }
 
 // 3-D tensor map of `batch` matrices of [outer, inner] 16-bit elements: row
@@ -1622,24 +1643,35 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
         return p.elt == Elt::BF16 ? launch_typed<__nv_bfloat16, 1, true>(p, num_sms, status, s)
                                   : launch_typed<__half, 0, true>(p, num_sms, status, s);
     }
-    // A few rows (M <= 64) and too few column tiles to occupy the GPU: split K
-    // over clusters -- the largest of 8, 4, 2 CTAs whose clusters all fit on the
-    // GPU at once (a cluster of CTAs with this much shared memory needs that
-    // many SMs of one GPC: 76, 36 and 15 clusters of 2, 4 and 8 fit on a GB300).
-    // Measured at N = 12288, K = 4096: M = 32 in 27.3 us against 31.3 unsplit;
-    // at M = 128 the larger cluster reduction made it slower (37.3 vs 34.8).
+    // Split K over clusters: tiles of bn = 256, 192 or 128 columns and clusters
+    // of 2 to 8 CTAs, the pair that puts the most CTAs to work with every
+    // cluster on the GPU at once (a cluster of CTAs with this much shared
+    // memory needs that many SMs of one GPC: 76, 36 and 15 clusters of 2, 4
+    // and 8 fit on a GB300); ties go to the wider tile.  N = 12288 takes
+    // 64 x 192-column tiles on clusters of 2 (128 CTAs).  Measured back to
+    // back with B from DRAM at N = 12288, K = 4096: M = 2 / 8 / 32 / 64 in
+    // 24.8 / 24.7 / 25.7 / 27.0 us; at N = 4096, K = 12288, M = 64 in 24.7 us
+    // (the 256-wide tiles on clusters of 2, 4, 8 alone with a full A box and
+    // the reduction on rank 0 took 30.9 / 28.1 / 27.6 / 31.5 and 33.8 us).
+    // At M = 128 a cluster reduction made it slower than the unsplit kernel
+    // (37.3 vs 34.8 us).
     if (p.M <= 64 && g_umma_splitk) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        const long long tiles_n = (p.N + BN - 1) / BN;
         const long long num_kb = (p.K + BK - 1) / BK;
-        int cs = 0;
-        for (int c = 8; c >= 2 && cs == 0; c /= 2)
-            if (num_kb >= c && splitk_clusters_max(p.elt, c, dev) >= tiles_n) cs = c;
+        int cs = 0, bn = 0;
+        long long best = 0;
+        for (int w = BN; w >= SPLITK_MIN_BN; w -= 64) {
+            const long long tiles_n = (p.N + w - 1) / w;
+            for (int c = SPLITK_MAX_CS; c >= 2; --c) {
+                if (num_kb < c || splitk_clusters_max(p.elt, c, dev) < tiles_n) continue;
+                if (tiles_n * c > best) { best = tiles_n * c; cs = c; bn = w; }
+            }
+        }
         if (cs >= 2)
-            return p.elt == Elt::BF16 ? launch_splitk_typed<__nv_bfloat16, 1>(p, cs, status, s)
-                                      : launch_splitk_typed<__half, 0>(p, cs, status, s);
+            return p.elt == Elt::BF16 ? launch_splitk_typed<__nv_bfloat16, 1>(p, cs, bn, status, s)
+                                      : launch_splitk_typed<__half, 0>(p, cs, bn, status, s);
     }
     // 256-row tiles on CTA pairs once M fills more than one 128-row tile.
     if (p.M > BM) {

@@ -126,6 +126,10 @@ MID_CASES = [
     ("bf16_rm", 40, 5000, 520, None, "umma_bf16"),           # 20 tiles x 4 ranks
     ("bf16_rm", 33, 10240, 256, None, "umma_bf16"),          # 40 tiles x 2 ranks
     ("f16_cm", 2000, 128, 2056, None, "umma_f16"),           # row-major M = 128, N = 2000
+    ("bf16_rm", 8, 12288, 1024, None, "umma_bf16"),          # 192-column tiles, clusters of 2
+    ("bf16_rm", 16, 4096, 12288, None, "umma_bf16"),         # long K, clusters wider than 4
+    ("bf16_rm", 3, 1032, 2000, None, "umma_bf16"),           # 8-row A box, 3 rows used; ragged K
+    ("f16_cm", 1000, 24, 3000, None, "umma_f16"),            # row-major M = 24 through the swap
 ]
 
 

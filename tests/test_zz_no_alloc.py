@@ -28,7 +28,7 @@ def _bits_to_f64(t: torch.Tensor) -> np.ndarray:
 
 
 @pytest.mark.parametrize("shape", [(1024, 12288, 4096), (1000, 1000, 1000), (300, 520, 264), (256, 512, 100),
-                                   (1024, 2048, 1028)])
+                                   (1024, 2048, 1028), (32, 4096, 4096)])
 def test_noalloc_matches_allocating_entry_point(lib, shape):
     M, N, K = shape
     clib = g.load()
