@@ -232,6 +232,16 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
         peak = float(peaks["hbm_gbs"])
         return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "algorithmic_bytes": algo_bytes, "peak_source": peaks_src}
+    if kind == "umma":
+        # below the ridge point (FLOPs per byte at which the measured tensor and
+        # HBM peaks meet) the tensor-core kernel is bound by HBM: skinny M
+        tpeak = float(peaks["bf16_tflops"]) * (2.0 if variant == "e4m3_rowscale" else 1.0)
+        if flops / algo_bytes < tpeak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9):
+            achieved = algo_bytes / seconds_per_launch / 1e9
+            peak = float(peaks["hbm_gbs"])
+            return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": traffic, "algorithmic_bytes": algo_bytes, "algorithmic_flops": flops,
+                    "peak_source": peaks_src}
     achieved = flops / seconds_per_launch / 1e12
     if kind == "umma" and variant == "e4m3_rowscale":
         # dense FP8 rate = 2 x the dense BF16 rate (4.5 vs 2.25 PFLOP/s nominal)
@@ -866,7 +876,8 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
     p.add_argument("--paths", nargs="*", default=["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144",
                                                    "ffn_bf16_rm_1024x12288x4096", "edge_bf16_rm_1x12288x4096",
-                                                   "edge_f32_rm_1x12288x4096", "edge_bf16_rm_8192x4096x4100",
+                                                   "edge_f32_rm_1x12288x4096", "edge_bf16_rm_32x12288x4096",
+                                                   "edge_bf16_rm_8192x4096x4100",
                                                    "edge_f32_rm_8192x4096x4100", "sgemm_f32_rm_256",
                                                    "ffn_gate_up_bf16_silu_mul_1024x12288x4096",
                                                    "gemm_ex_bf16_rm_NT_8192x8192x8192",

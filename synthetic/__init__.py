@@ -145,6 +145,7 @@ WORKLOADS = {
 EDGE_SHAPES = [  # (M, N, K) of the ragged/edge sweep, run on the f32 and bf16 paths
     (1000, 1000, 1000),
     (1, 12288, 4096),
+    (32, 12288, 4096),
     (64, 64, 64),
     (8192, 4096, 4100),
     (8192, 4096, 4096),
