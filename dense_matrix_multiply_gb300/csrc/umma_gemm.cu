@@ -75,6 +75,12 @@ constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
 #define UMMA_SPLITK 1
 #endif
 constexpr bool g_umma_splitk = UMMA_SPLITK != 0;
+// Whether the CTA-pair kernel evens out a part-full last wave with a stream-K
+// tail (needs stream-ordered scratch).
+#ifndef PAIR_SK
+#define PAIR_SK 1
+#endif
+constexpr bool g_pair_sk = PAIR_SK != 0;
 // Narrowest column tile and largest cluster of the cluster split.
 #ifndef SPLITK_MIN_BN
 #define SPLITK_MIN_BN 128
@@ -346,6 +352,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half *) {
 }
 __device__ __forceinline__ void store1(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void store1(__half *p, float x) { *p = __float2half_rn(x); }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
 
 // One element of Z = SiLU(G) * U with the unfused chain's rounding points: G and
 // U rounded to the storage type, T = round(SiLU(G)) with SiLU(g) = g / (1 + e^-g)
@@ -663,7 +671,61 @@ struct PairArgs {
     float alpha, beta;
     const float *row_scale;   // FP8 products: per-row scale of the output
     int *status;
+    // Stream-K tail (sk_tiles > 0): the last sk_tiles tiles are cut into
+    // K-block ranges of sk_w spread over clusters sk_first .. G-1, whose FP32
+    // partials go to sk_ws (two slots per stream-K cluster, one 32-row x
+    // 256-column slab per epilogue warp and CTA, column-major) instead of C.
+    float *sk_ws;
+    int sk_tiles, sk_w, sk_first;
 };
+
+// Tile t -> (batch index, row tile, column tile); M-grouped raster inside a batch.
+__device__ __forceinline__ void pair_coords(int t, int tiles_m, int tiles_n, int &bt, int &tm, int &tn) {
+    const int tiles_per_batch = tiles_m * tiles_n;
+    bt = t / tiles_per_batch;
+    const int r0 = t - bt * tiles_per_batch;
+    const int per_group = pairk::P_GROUP_M * tiles_n;
+    const int group = r0 / per_group;
+    const int first_m = group * pairk::P_GROUP_M;
+    const int gsize = min(tiles_m - first_m, pairk::P_GROUP_M);
+    const int r = r0 - group * per_group;
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+}
+
+// Work unit u of cluster c: tile t, K-block range [kb0, kb1) and the index sk
+// of the stream-K tile (-1 for a whole tile).  Whole tiles c, c + G, ... below
+// num_tiles - sk_tiles come first; then, for c >= sk_first, the cluster's share
+// [c'*W, (c'+1)*W) (c' = c - sk_first) of the stream-K iterations (tile-major,
+// K-block minor), cut at tile boundaries.  W <= num_kb, so a share touches at
+// most two tiles.  Producer, MMA issuer and epilogue walk the same sequence.
+__device__ __forceinline__ bool pair_unit(int u, int c, int G, int num_tiles, const PairArgs &a, int num_kb, int &t,
+                                          int &kb0, int &kb1, int &sk) {
+    const int t_dp = num_tiles - a.sk_tiles;
+    const int n_dp = c < t_dp ? (t_dp - 1 - c) / G + 1 : 0;
+    if (u < n_dp) {
+        t = c + u * G;
+        kb0 = 0;
+        kb1 = num_kb;
+        sk = -1;
+        return true;
+    }
+    if (a.sk_tiles == 0 || c < a.sk_first) return false;
+    const long long cc = c - a.sk_first;
+    const long long total = (long long)a.sk_tiles * num_kb;
+    const long long end = min((cc + 1) * a.sk_w, total);
+    long long it = cc * a.sk_w;
+    for (int q = u - n_dp; q > 0; --q) {
+        if (it >= end) return false;
+        it = min((it / num_kb + 1) * num_kb, end);
+    }
+    if (it >= end) return false;
+    sk = (int)(it / num_kb);
+    t = t_dp + sk;
+    kb0 = (int)(it - (long long)sk * num_kb);
+    kb1 = (int)min((long long)num_kb, kb0 + (end - it));
+    return true;
+}
 
 __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
                                                  int y, int z) {
@@ -784,18 +846,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
 
-    // Tile t -> (batch index, row tile, column tile); M-grouped raster inside a batch.
-    auto coords = [&](int t, int &bt, int &tm, int &tn) {
-        bt = t / tiles_per_batch;
-        const int r0 = t - bt * tiles_per_batch;
-        const int per_group = P_GROUP_M * tiles_n;
-        const int group = r0 / per_group;
-        const int first_m = group * P_GROUP_M;
-        const int gsize = min(tiles_m - first_m, P_GROUP_M);
-        const int r = r0 - group * per_group;
-        tm = first_m + r % gsize;
-        tn = r / gsize;
-    };
+    auto coords = [&](int t, int &bt, int &tm, int &tn) { pair_coords(t, tiles_m, tiles_n, bt, tm, tn); };
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
@@ -803,13 +854,15 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
-        for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+        for (int u = 0; ok; ++u) {
+            int t, kb0, kb1, sk;
+            if (!pair_unit(u, cluster, nclusters, num_tiles, args, num_kb, t, kb0, kb1, sk)) break;
             int bt, tm, tn;
             coords(t, bt, tm, tn);
             const int za = args.a_bcast ? 0 : bt, zb = args.b_bcast ? 0 : bt;
             const int row0 = tm * PBM + (int)rank * 128;
             const int col0 = tn * bn + (int)rank * (bn >> 1);
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait_cluster(&bars->empty[stage], phase ^ 1u, abort_flag, true)) { ok = false; break; }
                 const uint32_t full_leader = map_to_rank(&bars->full[stage], 0);
                 if (leader) mbar_arrive_expect_tx(&bars->full[stage], P_STAGE_TX);
@@ -873,23 +926,26 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const uint64_t a_desc0 = smem_desc_sw128(smem_u32(a_tiles), a_mn ? P_BOX64 : 16, 1024);
         const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_tiles), b_mn ? P_BOX64 : 16, 1024);
         const uint32_t a_kstep = (a_mn ? 2048u : 32u) >> 4, b_kstep = (b_mn ? 2048u : 32u) >> 4;
-        for (int t = cluster; t < num_tiles && ok; t += nclusters, ++it) {
+        for (int u = 0; ok; ++u, ++it) {
+            int t, kb0, kb1, sk;
+            if (!pair_unit(u, cluster, nclusters, num_tiles, args, num_kb, t, kb0, kb1, sk)) break;
             const int buf = it & 1;
             const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
             if (!mbar_wait_cluster(&bars->acc_empty[buf], acc_par ^ 1u, abort_flag, true)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(buf * PBN);
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait_cluster(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t ad = a_desc0 + (uint64_t)((stage * P_A_STAGE) >> 4);
                 const uint64_t bd = b_desc0 + (uint64_t)((stage * P_B_STAGE) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < BK / UMMA_K; ++ks) {
+                    const uint32_t acc = (kb != kb0) | (ks != 0);
                     if constexpr (F8)
-                        umma_pair_f8(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, (kb | ks) != 0);
+                        umma_pair_f8(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, acc);
                     else
-                        umma_pair(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, (kb | ks) != 0);
+                        umma_pair(d_tmem, ad + ks * a_kstep, bd + ks * b_kstep, idesc, acc);
                 }
                 umma_commit_pair_multicast(&bars->empty[stage], 0x3);
                 if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
@@ -912,7 +968,9 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         int sb = 0;
         int it = 0;
         bool ok = true;
-        for (int t = cluster; t < num_tiles; t += nclusters, ++it) {
+        for (int u = 0;; ++u, ++it) {
+            int t, kb0, kb1, sk;
+            if (!pair_unit(u, cluster, nclusters, num_tiles, args, num_kb, t, kb0, kb1, sk)) break;
             int bt, tm, tn;
             coords(t, bt, tm, tn);
             const int buf = it & 1;
@@ -923,6 +981,26 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int n0 = tn * bn;
             const int box_row0 = tm * PBM + (int)rank * 128 + quarter * 32;  // warp-uniform
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * PBN);
+            // Stream-K segment: write this warp's FP32 partial of the tile
+            // (column-major slab: 128-byte rows across the lanes) and free the
+            // accumulator; pair_sk_fixup_kernel adds the partials in K order.
+            if (sk >= 0) {
+                const int ord = ((long long)(cluster - args.sk_first) * args.sk_w) / num_kb == sk ? 0 : 1;
+                float *mine = args.sk_ws +
+                              ((size_t)(2 * (cluster - args.sk_first) + ord) * 8 + rank * 4 + quarter) * (256 * 32);
+                const int ncols = DUAL ? 256 : bn;
+#pragma unroll 1
+                for (int cc = 0; cc < ncols / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(t_row + (uint32_t)(cc * 32), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) __stcg(mine + (cc * 32 + c) * 32 + lane, __uint_as_float(r[c]));
+                }
+                tc_fence_before();
+                mbar_arrive_cluster(map_to_rank(&bars->acc_empty[buf], 0));
+                continue;
+            }
             if constexpr (DUAL) {
 #pragma unroll 1
                 for (int g = 0; g < 2; ++g) {
@@ -1034,6 +1112,84 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+// Stream-K fix-up: each stream-K tile of the CTA-pair kernel is the sum, in K
+// order, of the FP32 partials of the clusters whose K ranges cover it; this
+// kernel adds them and applies the pair kernel's epilogue (alpha, beta * old
+// C, the fused SiLU * U chain, the FP8 row scale; one rounding to T).  Launched
+// after the pair kernel on the same stream.  Block (2 sk + r, y): rows
+// [128 r, 128 r + 128) of stream-K tile sk, one per thread, output columns
+// [8y, 8y + 8) of the tile.
+template <typename T, bool DUAL, bool F8>
+__global__ void __launch_bounds__(128)
+pair_sk_fixup_kernel(const PairArgs args, int num_kb)
+{
+    const int sk = (int)(blockIdx.x >> 1), rank = (int)(blockIdx.x & 1);
+    const int quarter = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+    const int bn = args.bn, M = args.M, N = args.N;
+    const int tiles_m = (M + pairk::PBM - 1) / pairk::PBM, tiles_n = (N + bn - 1) / bn;
+    const int num_tiles = tiles_m * tiles_n * args.batch;
+    const int zc = (int)blockIdx.y * 8;  // first output column of this thread, in the tile
+    if (zc >= bn) return;
+    int bt, tm, tn;
+    pair_coords(num_tiles - args.sk_tiles + sk, tiles_m, tiles_n, bt, tm, tn);
+    const int row = tm * pairk::PBM + rank * 128 + (int)threadIdx.x, col = tn * bn + zc;
+    if (row >= M || col >= N) return;
+    const long long it0 = (long long)sk * num_kb;
+    const int cf = (int)(it0 / args.sk_w), cl = (int)((it0 + num_kb - 1) / args.sk_w);
+    // accumulator columns: DUAL -- G at 128 g + j, U at 128 g + 64 + j for
+    // output column 64 g + j; otherwise the output column itself.
+    constexpr int NACC = DUAL ? 16 : 8;
+    int acol[NACC];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if constexpr (DUAL) {
+            const int g = (zc + e) >> 6, j = (zc + e) & 63;
+            acol[e] = 128 * g + j;
+            acol[8 + e] = 128 * g + 64 + j;
+        } else {
+            acol[e] = zc + e;
+        }
+    }
+    float acc[NACC];
+#pragma unroll 1
+    for (int c = cf; c <= cl; ++c) {
+        const int ord = ((long long)c * args.sk_w) / num_kb == sk ? 0 : 1;
+        const float *slab = args.sk_ws + ((size_t)(2 * c + ord) * 8 + rank * 4 + quarter) * (256 * 32) + lane;
+        float v[NACC];
+#pragma unroll
+        for (int e = 0; e < NACC; ++e) v[e] = __ldcg(slab + acol[e] * 32);
+#pragma unroll
+        for (int e = 0; e < NACC; ++e) acc[e] = c == cf ? v[e] : acc[e] + v[e];
+    }
+    float z[8];
+    if constexpr (DUAL) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[e] = silu_mul(acc[e], acc[8 + e], (T *)nullptr);
+    } else {
+        const float sc = F8 ? args.row_scale[row] : args.alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[e] = sc * acc[e];
+    }
+    T *dst = static_cast<T *>(args.C) + (long long)bt * args.stride_c + (long long)row * args.ldc + col;
+    if (!DUAL && !F8 && args.beta != 0.0f) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (col + e < N) z[e] = fmaf(args.beta, to_float(dst[e]), z[e]);
+    }
+    if (col + 8 <= N) {
+        uint4 w;
+        w.x = pack2(z[0], z[1], (T *)nullptr);
+        w.y = pack2(z[2], z[3], (T *)nullptr);
+        w.z = pack2(z[4], z[5], (T *)nullptr);
+        w.w = pack2(z[6], z[7], (T *)nullptr);
+        *reinterpret_cast<uint4 *>(dst) = w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (col + e < N) store1(dst + e, z[e]);
     }
 }
 
@@ -1444,10 +1600,62 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>, ta, tb, tc, tb2, args);
 }
 
+// Whether T tiles of KB K-blocks on G clusters take a stream-K tail: the last
+// wave holds rem = T mod G <= G / 4 tiles (a nearly empty wave still costs
+// most of a tile time: with half the clusters busy it measured 85 % of a full
+// wave, so spreading a fuller one gains too little) and a tile is long
+// enough (KB >= 48) for the saving to exceed the fix-up's cost (scratch, a
+// second kernel, ~8 us back to back).  Measured on GB300: FP16 3072 x 5120 x
+// 6144 (240 tiles, rem 12) 142 -> 126 us; the BF16 FFN 1024 x 12288 x 4096
+// (rem 40) 66 -> 77 us, so it keeps whole tiles.
+bool sk_worth(long long tiles, int clusters, long long num_kb) {
+    if (!g_pair_sk || clusters <= 0 || tiles <= clusters) return false;
+    const long long rem = tiles % clusters;
+    return rem > 0 && rem * 4 <= clusters && num_kb >= 48;
+}
+
+// Launch with a stream-K tail when sk_worth: the last rem tiles' K iterations
+// are spread over the G_sk = min(G, 4 rem) highest clusters,
+// W = ceil(rem * KB / G_sk) each, instead of leaving G - rem clusters idle for
+// a whole tile time; a tile then has at most ceil(KB / W) + 1 <= 5
+// contributors.  Their partial slabs live in stream-ordered scratch, and
+// pair_sk_fixup_kernel, next on the stream, adds them.  Without scratch (or
+// allow_sk false) the tail runs as whole tiles.
+template <typename T, uint32_t F, bool DUAL = false, bool F8 = false>
+cudaError_t launch_pair_planned(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                                const CUtensorMap &tb2, PairArgs args, int clusters, long long tiles, bool allow_sk,
+                                cudaStream_t s) {
+    const long long num_kb = (args.K + (F8 ? 128 : BK) - 1) / (F8 ? 128 : BK);
+    const long long rem = clusters > 0 ? tiles % clusters : 0;
+    if (allow_sk && sk_worth(tiles, clusters, num_kb)) {
+        const long long g_sk = std::min<long long>(clusters, 4 * rem);
+        const long long w = (rem * num_kb + g_sk - 1) / g_sk;
+        const size_t ws_bytes = (size_t)g_sk * 2 * 8 * 256 * 32 * sizeof(float);
+        void *buf = nullptr;
+        if (cudaMallocAsync(&buf, ws_bytes, s) == cudaSuccess) {
+            args.sk_ws = static_cast<float *>(buf);
+            args.sk_tiles = (int)rem;
+            args.sk_w = (int)w;
+            args.sk_first = clusters - (int)g_sk;
+            cudaError_t e = launch_pair_cfg<T, F, DUAL, F8>(ta, tb, tc, tb2, args, clusters, s);
+            if (e == cudaSuccess) {
+                pair_sk_fixup_kernel<T, DUAL, F8><<<dim3((unsigned)(2 * rem), (unsigned)(args.bn / 8), 1), 128, 0, s>>>(
+                    args, (int)num_kb);
+                e = cudaGetLastError();
+            }
+            const cudaError_t f = cudaFreeAsync(buf, s);
+            return e != cudaSuccess ? e : f;
+        }
+        cudaGetLastError();
+    }
+    return launch_pair_cfg<T, F, DUAL, F8>(ta, tb, tc, tb2, args, clusters, s);
+}
+
 // The general problem on CTA pairs.  Returns cudaErrorNotSupported, before any
 // launch, when a tensor map cannot describe an operand.
 template <typename T, uint32_t F>
-cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status, cudaStream_t s) {
+cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status, cudaStream_t s,
+                              bool allow_sk = true) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const long long ba = p.sa == 0 ? 1 : p.batch, bb = p.sb == 0 ? 1 : p.batch;
     CUtensorMap ta, tb, tc;
@@ -1457,14 +1665,16 @@ cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status,
                             : make_map3(&tb, p.B, dt, p.N, p.K, bb, p.ldb, p.sb, 64, BK);
     const bool ok_c = make_map3(&tc, p.C, dt, p.N, p.M, p.batch, p.ldc, p.sc, 64, 32);
     if (!ok_a || !ok_b || !ok_c) return cudaErrorNotSupported;
-    // N extent of a tile: the one of 256, 192, 128 (TMA-store boxes are 64
-    // columns wide) with the fewest waves of tiles over the clusters, widest on
-    // ties: per-tile time is set mostly by the operand feed, which does not
-    // shrink with the tile's N.
+    // N extent of a tile: 256 when a stream-K tail evens out the last wave;
+    // otherwise the one of 256, 192, 128 (TMA-store boxes are 64 columns wide)
+    // with the fewest waves of tiles over the clusters, widest on ties:
+    // per-tile time is set mostly by the operand feed, which does not shrink
+    // with the tile's N.
     const long long tiles_mb = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * p.batch;
     int bn = 256;
+    const bool sk_ok = allow_sk && sk_worth(tiles_mb * ((p.N + 255) / 256), clusters_max, (p.K + BK - 1) / BK);
     long long best = -1;
-    for (int cand = 256; cand >= 128; cand -= 64) {
+    for (int cand = 256; cand >= 128 && !sk_ok; cand -= 64) {
         const long long t = tiles_mb * ((p.N + cand - 1) / cand);
         const long long waves = (t + clusters_max - 1) / clusters_max;
         const long long cost = waves * (cand > 224 ? cand : 224);
@@ -1489,7 +1699,7 @@ cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status,
     args.alpha = p.alpha;
     args.beta = p.beta;
     args.status = status;
-    return launch_pair_cfg<T, F, false>(ta, tb, tc, tb, args, clusters, s);
+    return launch_pair_planned<T, F>(ta, tb, tc, tb, args, clusters, tiles, allow_sk, s);
 }
 
 // Z = SiLU(X W_g) * (X W_u): p.A = X [M,K], p.B = W_g [K,N], p.C = Z [M,N];
@@ -1517,7 +1727,7 @@ cudaError_t launch_pair_silu_mul_typed(const Problem &p, const void *w_u, int cl
     args.bn = bn;
     args.alpha = 1.0f;
     args.status = status;
-    return launch_pair_cfg<T, F, true>(ta, tg, tc, tu, args, clusters, s);
+    return launch_pair_planned<T, F, true>(ta, tg, tc, tu, args, clusters, tiles, true, s);
 }
 
 // C [M,N] half = diag(scale) Q Wt^T on CTA pairs, Q [M,K] and Wt [N,K] E4M3.
@@ -1530,8 +1740,9 @@ cudaError_t launch_pair_e4m3(const void *Q, const float *scale, const void *Wt, 
         return cudaErrorNotSupported;
     const long long tiles_m = (M + pairk::PBM - 1) / pairk::PBM;
     int bn = 256;
+    const bool sk_ok = sk_worth(tiles_m * ((N + 255) / 256), clusters_max, (K + 127) / 128);
     long long best = -1;
-    for (int cand = 256; cand >= 128; cand -= 64) {
+    for (int cand = 256; cand >= 128 && !sk_ok; cand -= 64) {
         const long long t = tiles_m * ((N + cand - 1) / cand);
         const long long waves = (t + clusters_max - 1) / clusters_max;
         const long long cost = waves * (cand > 224 ? cand : 224);
@@ -1552,7 +1763,7 @@ cudaError_t launch_pair_e4m3(const void *Q, const float *scale, const void *Wt, 
     args.alpha = 1.0f;
     args.row_scale = scale;
     args.status = status;
-    return launch_pair_cfg<__half, 0, false, true>(ta, tb, tc, tb, args, clusters, s);
+    return launch_pair_planned<__half, 0, false, true>(ta, tb, tc, tb, args, clusters, tiles, true, s);
 }
 
 // The tight problem of the plain entry points as a general one; lda: row
@@ -1682,8 +1893,8 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
                                             : pair_clusters_max<__half, 0>(dev);
         if (cmax > 0) {
             const ProblemEx q = plain_ex(p);
-            return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(q, cmax, status, s)
-                                      : launch_pair_typed<__half, 0>(q, cmax, status, s);
+            return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(q, cmax, status, s, may_allocate)
+                                      : launch_pair_typed<__half, 0>(q, cmax, status, s, may_allocate);
         }
     }
     if (p.elt == Elt::BF16) return launch_typed<__nv_bfloat16, 1, false>(p, num_sms, status, s);

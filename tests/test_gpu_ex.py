@@ -267,3 +267,30 @@ def test_column_major_batched_half_sampled():
                              B[b * K * N:(b + 1) * K * N], K, 0, 0.0, None, M, 0, 1)
         got = out[b * M * N:(b + 1) * M * N].reshape(N, M).T[None]
         check("f16", got, ref, K, 1.0)
+
+
+@pytest.mark.parametrize("dtype,op_a,op_b", [("bf16", "N", "T"), ("f16", "T", "N")])
+def test_stream_k_tail_batched_alpha_beta(dtype, op_a, op_b):
+    """Five batches of 256 x 4096 x 3072 make 80 pair tiles: the 4-6 tiles past
+    a full wave (all in the last batch) are summed from stream-K partials, and
+    alpha and beta * old C are applied once, after the sum.  The last batch is
+    checked whole against the oracle."""
+    M, N, K, batch, alpha, beta = 256, 4096, 3072, 5, 0.5, -1.25
+    a_r, a_c = (M, K) if op_a == "N" else (K, M)
+    b_r, b_c = (K, N) if op_b == "N" else (N, K)
+    lda, ldb, ldc = a_c + 8, b_c + 16, N + 8
+    sa, sb, sc = a_r * lda + 64, b_r * ldb + 32, M * ldc + 8
+    s0 = synthetic.seed_for(SEED, 0) + 7000
+    A = padded(dtype, a_r, a_c, lda, sa, batch, s0 + 100)
+    B = padded(dtype, b_r, b_c, ldb, sb, batch, s0 + 200)
+    C0 = padded(dtype, M, N, ldc, sc, batch, s0 + 300)
+    dA, dB, dC = dev(A), dev(B), dev(C0.copy())
+    g.gemm_ex(dtype, "rm", op_a, op_b, M, N, K, alpha, dA, lda, sa, dB, ldb, sb, beta, dC, ldc, sc, batch)
+    assert g.gemm_last_kernel() == f"umma_ex_{dtype}"
+    g.gemm_synchronize()
+    C1 = host(dC, dtype)
+    for b in (batch - 1,):
+        ref = oracle.gemm_ex(dtype, "rm", op_a, op_b, M, N, K, alpha, A[b * sa:], lda, 0, B[b * sb:], ldb, 0,
+                             beta, C0[b * sc:], ldc, 0, 1)
+        out = widen(dtype, C1[b * sc: b * sc + M * ldc].reshape(M, ldc)[:, :N])[None]
+        check(dtype, out, ref, K, alpha)
