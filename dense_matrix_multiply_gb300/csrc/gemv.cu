@@ -65,6 +65,8 @@ template <typename T, int VW, int TC, int MM>
 __global__ void __launch_bounds__(THREADS)
 gemv_kernel(const T *__restrict__ X, const T *__restrict__ W, T *__restrict__ C, int M, int N, int K)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int TK = THREADS / TC;
     constexpr int CW = TC * VW;
     extern __shared__ float red[];
@@ -173,13 +175,14 @@ cudaError_t launch_cfg(const Problem &p, int num_sms, cudaStream_t s) {
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    pdl_attr(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<const T *>(p.A), static_cast<const T *>(p.B),
                               static_cast<T *>(p.C), p.M, p.N, p.K);
 }

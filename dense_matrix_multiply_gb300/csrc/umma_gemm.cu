@@ -81,6 +81,11 @@ constexpr bool g_umma_splitk = UMMA_SPLITK != 0;
 #define PAIR_SK 1
 #endif
 constexpr bool g_pair_sk = PAIR_SK != 0;
+// Whether problems with M <= 64 run on the swapped-operand skinny kernel.
+#ifndef UMMA_SKINNY
+#define UMMA_SKINNY 1
+#endif
+constexpr bool g_umma_skinny = UMMA_SKINNY != 0;
 // Narrowest column tile and largest cluster of the cluster split.
 #ifndef SPLITK_MIN_BN
 #define SPLITK_MIN_BN 128
@@ -414,6 +419,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel's writes are visible from here on
 
     if (A_CPASYNC && warp >= 6) {
         // ------------------------------------------------ producer: cp.async A + TMA B
@@ -845,6 +852,8 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     cluster_sync();  // barriers of both CTAs initialised before any cross-CTA use
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel's writes are visible from here on
 
     auto coords = [&](int t, int &bt, int &tm, int &tn) { pair_coords(t, tiles_m, tiles_n, bt, tm, tn); };
 
@@ -1126,6 +1135,8 @@ template <typename T, bool DUAL, bool F8>
 __global__ void __launch_bounds__(128)
 pair_sk_fixup_kernel(const PairArgs args, int num_kb)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int sk = (int)(blockIdx.x >> 1), rank = (int)(blockIdx.x & 1);
     const int quarter = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
     const int bn = args.bn, M = args.M, N = args.N;
@@ -1262,6 +1273,8 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel's writes are visible from here on
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer
@@ -1401,7 +1414,229 @@ umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
 }
 
+// ------------------------------------------- skinny M: weights as the MMA's rows
+// For M <= 64 the roles of the operands swap: D = W^T X^T, i.e. C^T, with the
+// weights W [K, N] as the MMA's 128-row operand (a 128-column strip of W, MN-
+// major in shared memory: two 64 x 64 boxes per stage, as the CTA-pair
+// kernel's transposed A) and the M rows of X as its N = nb operand (K-major,
+// a box of M rows rounded up to 8; nb = M rounded up to 16, the stale rows past
+// the box only reaching accumulator columns that are never stored).  Every MMA
+// row is a useful output column, a stage is 16 KiB of W + at most 8 KiB of X,
+// so SKS stages keep ~128 KiB of W in flight per SM, and the accumulator is
+// nb <= 64 tensor-memory columns.  Tile t = 128 columns of C; the CS CTAs of a
+// cluster split its K-blocks as the split-K kernel does and add their partials
+// through distributed shared memory in rank order (CS = 1: no cluster, C is
+// stored straight from tensor memory).  Deterministic, one launch, no
+// workspace; every barrier wait is bounded.
+constexpr int SKS = 8;                       // stages
+constexpr int SK_W_STAGE = 2 * B_BOX;        // 128 columns x 64 k of W: 16 KiB
+constexpr int SK_X_STAGE = 64 * BK * 2;      // up to 64 rows x 64 k of X: 8 KiB
+constexpr int SK_SMEM_TILES = SKS * (SK_W_STAGE + SK_X_STAGE);
+constexpr int SK_SMEM_BYTES = 1024 + SK_SMEM_TILES + 256;
+constexpr uint32_t SK2_TMEM_COLS = 64;
+constexpr int SK2_LD = 128 + 4;              // floats per m-row of a partial [nb][128]
+using SkBars = BarsT<SKS>;
+static_assert(sizeof(SkBars) <= 256, "barrier block");
+static_assert(64 * SK2_LD * 4 <= SK_SMEM_TILES, "partial fits in the drained stages");
+
+__host__ __device__ constexpr int skinny_x_rows(int M) { return (M + 7) / 8 * 8; }
+__host__ __device__ constexpr int skinny_nb(int M) { return (M + 15) / 16 * 16; }
+
+template <typename T, uint32_t AB_FORMAT>
+__global__ void __launch_bounds__(THREADS, 1)
+umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   T *__restrict__ C, int M, int N, int K, int cs, int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *w_tiles = smem;
+    uint8_t *x_tiles = smem + SKS * SK_W_STAGE;
+    float *part = reinterpret_cast<float *>(smem);  // [nb][SK2_LD] once the stages are drained
+    SkBars *bars = reinterpret_cast<SkBars *>(smem + SK_SMEM_TILES);
+    volatile int *abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cs > 1 ? cluster_ctarank() : 0u;
+    const int n0 = (int)(cs > 1 ? cluster_id_x() : blockIdx.x) * 128;
+    const int num_kb = (K + BK - 1) / BK;
+    const int kb0 = (int)(((long long)num_kb * rank) / cs), kb1 = (int)(((long long)num_kb * (rank + 1)) / cs);
+    const bool has_work = kb1 > kb0;
+    const int x_rows = skinny_x_rows(M), nb = skinny_nb(M);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SKS; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->acc_full[0], 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, SK2_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+    pdl_launch_dependents();
+    pdl_wait();  // the previous kernel's writes are visible from here on
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        const int n_left = N - n0;
+        const int wboxes = n_left >= 128 ? 2 : (n_left + 63) / 64;
+        const uint32_t tx = (uint32_t)(wboxes * B_BOX + x_rows * BK * 2);
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, true)) {
+                atomicOr(status, ST_PRODUCER);
+                *abort_flag = 1;
+                break;
+            }
+            mbar_arrive_expect_tx(&bars->full[stage], tx);
+            for (int j = 0; j < wboxes; ++j)
+                tma_load_2d(w_tiles + stage * SK_W_STAGE + j * B_BOX, &tmW, &bars->full[stage], n0 + 64 * j,
+                            kb * BK);
+            tma_load_2d(x_tiles + stage * SK_X_STAGE, &tmX, &bars->full[stage], kb * BK, 0);
+            ++issued;
+            if (++stage == SKS) { stage = 0; phase ^= 1u; }
+        }
+        // Let every load this thread issued land before the stages are reused.
+        for (long long i = (issued > SKS ? issued - SKS : 0); i < issued; ++i) {
+            const int s = (int)(i % SKS);
+            const uint32_t par = (uint32_t)((i / SKS) & 1);
+            if (!mbar_wait(&bars->full[s], par, abort_flag, false)) {
+                atomicOr(status, ST_DRAIN);
+                break;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        // A = the W strip, MN-major: 64-column chunks B_BOX bytes apart, a K step
+        // of 16 rows is 2048 bytes.  B = the X rows, K-major: a K step is 32
+        // bytes inside the 128-byte swizzle row, 8-row groups 1024 bytes apart.
+        const uint32_t idesc = make_idesc(AB_FORMAT, 128, (uint32_t)nb, true, false);
+        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(w_tiles), B_BOX, 1024);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(x_tiles), 16, 1024);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ad = a_desc0 + (uint64_t)((stage * SK_W_STAGE) >> 4);
+            const uint64_t bd = b_desc0 + (uint64_t)((stage * SK_X_STAGE) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < BK / UMMA_K; ++ks)
+                umma(tmem_base, ad + ks * (2048u >> 4), bd + ks * (32u >> 4), idesc, (kb != kb0 || ks != 0));
+            umma_commit(&bars->empty[stage]);
+            if (++stage == SKS) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) {
+            umma_commit(&bars->acc_full[0]);
+        } else {
+            atomicOr(status, ST_MMA);
+            *abort_flag = 1;
+        }
+        umma_commit(&bars->drain);
+        if (!mbar_wait(&bars->drain, 0, abort_flag, false)) atomicOr(status, ST_DRAIN);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        // TMEM lane = column n0 + nl of C, TMEM column = row m.
+        const int quarter = warp & 3;
+        const int nl = quarter * 32 + lane, n = n0 + nl;
+        bool ready = true;
+        if (has_work && !mbar_wait(&bars->acc_full[0], 0, abort_flag, true)) {
+            atomicOr(status, ST_EPILOGUE);
+            *abort_flag = 1;
+            ready = false;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < nb; c += 32) {
+            uint32_t r[32];
+            if (has_work && ready) {
+                tmem_ld_32cols(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, r);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+            if (cs == 1) {
+                if (n < N) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c + j < M) store1(C + (size_t)(c + j) * N + n, __uint_as_float(r[j]));
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c + j < M) part[(c + j) * SK2_LD + nl] = __uint_as_float(r[j]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    if (cs > 1) {
+        cluster_sync();  // every partial is in its CTA's shared memory, visible cluster-wide
+        // (row, four-column group) pairs dealt out to the cs CTAs in equal
+        // ranges; the partials of ranks 0 .. cs-1 added in that order.
+        cg::cluster_group cluster = cg::this_cluster();
+        const int groups = min(128, N - n0) / 4;  // N % 8 == 0: whole groups
+        const int total = M * groups;
+        const int e0 = (int)(((long long)total * rank) / cs), e1 = (int)(((long long)total * (rank + 1)) / cs);
+        for (int e = e0 + threadIdx.x; e < e1; e += THREADS) {
+            const int m = e / groups, c4 = (e - m * groups) * 4;
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < cs) v[j] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(part + m * SK2_LD + c4, j));
+            float4 acc = v[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) {
+                if (j < cs) {
+                    acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+                }
+            }
+            uint2 w;
+            w.x = pack2(acc.x, acc.y, (T *)nullptr);
+            w.y = pack2(acc.z, acc.w, (T *)nullptr);
+            *reinterpret_cast<uint2 *>(C + (size_t)m * N + n0 + c4) = w;
+        }
+        __syncwarp();
+        cluster_sync();  // every CTA keeps its shared memory until the others have read it
+    } else {
+        __syncthreads();  // tensor memory read out before it is freed
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, SK2_TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
+// Launch configuration of a kernel without clusters, with programmatic
+// dependent launch allowed (the attribute array must outlive the launch call).
+cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    pdl_attr(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = g_pdl ? 1 : 0;
+    return cfg;
+}
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                    CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -1460,9 +1695,10 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     const long long tiles = (long long)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-    kern<<<grid, A_CPASYNC ? THREADS + 128 : THREADS, SMEM_BYTES, s>>>(
-        ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K, status, stall);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(A_CPASYNC ? THREADS + 128 : THREADS), SMEM_BYTES, s, attr);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K,
+                              status, stall);
 }
 
 // Largest number of co-resident clusters of cs CTAs of the skinny-M kernel
@@ -1496,6 +1732,80 @@ int splitk_clusters_max(Elt elt, int cs, int dev) {
     return cached[dev & 63][t][ci].load();
 }
 
+// Largest number of co-resident clusters of cs CTAs (2 <= cs <= 8) of the
+// swapped-operand skinny kernel, per device and element type.
+int skinny_clusters_max(Elt elt, int cs, int dev) {
+    static std::atomic<int> cached[64][2][9];
+    static std::once_flag once[64][2][9];
+    if (cs < 2 || cs > 8) return 0;
+    const int t = elt == Elt::BF16 ? 1 : 0;
+    std::call_once(once[dev & 63][t][cs], [&] {
+        const void *kern = t ? reinterpret_cast<const void *>(umma_skinny_kernel<__nv_bfloat16, 1>)
+                             : reinterpret_cast<const void *>(umma_skinny_kernel<__half, 0>);
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)cs, 1, 1);
+            cfg.blockDim = dim3(THREADS, 1, 1);
+            cfg.dynamicSmemBytes = SK_SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        cached[dev & 63][t][cs].store(n);
+    });
+    return cached[dev & 63][t][cs].load();
+}
+
+// Swapped-operand skinny launch: ceil(N / 128) column strips, each on one CTA
+// (cs = 1) or on a cluster of cs CTAs splitting K.
+template <typename T, uint32_t F>
+cudaError_t launch_skinny_typed(const Problem &p, int cs, int *status, cudaStream_t s) {
+    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (p.M < 1 || p.M > 64 || cs < 1 || cs > 8) return cudaErrorInvalidValue;
+    CUtensorMap tx, tw;
+    if (!make_map(&tx, p.A, dt, p.M, p.K, skinny_x_rows(p.M), BK) || !make_map(&tw, p.B, dt, p.K, p.N, BK, 64))
+        return cudaErrorInvalidValue;
+    auto kern = umma_skinny_kernel<T, F>;
+    static std::atomic<uint64_t> attr_done{0};  // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_release);
+    }
+    const long long tiles_n = (p.N + 127) / 128;
+    if (tiles_n * cs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (cs == 1) {
+        cudaLaunchAttribute a1[1];
+        const cudaLaunchConfig_t c1 = pdl_config(dim3((unsigned)tiles_n), dim3(THREADS), SK_SMEM_BYTES, s, a1);
+        return cudaLaunchKernelEx(&c1, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, 1, status);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles_n * cs), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SK_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    pdl_attr(attr[1]);
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, cs, status);
+}
+
 // Split-K launch of the skinny-M kernel: ceil(N / bn) clusters of cs CTAs,
 // bn = 128, 192 or 256 columns per tile.
 template <typename T, uint32_t F>
@@ -1523,13 +1833,14 @@ cudaError_t launch_splitk_typed(const Problem &p, int cs, int bn, int *status, c
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    pdl_attr(attr[1]);
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, bn, status);
 }
 
@@ -1590,13 +1901,14 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = pairk::smem_bytes(pairk::P_STAGES);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    pdl_attr(attr[1]);
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>, ta, tb, tc, tb2, args);
 }
 
@@ -1639,9 +1951,11 @@ cudaError_t launch_pair_planned(const CUtensorMap &ta, const CUtensorMap &tb, co
             args.sk_first = clusters - (int)g_sk;
             cudaError_t e = launch_pair_cfg<T, F, DUAL, F8>(ta, tb, tc, tb2, args, clusters, s);
             if (e == cudaSuccess) {
-                pair_sk_fixup_kernel<T, DUAL, F8><<<dim3((unsigned)(2 * rem), (unsigned)(args.bn / 8), 1), 128, 0, s>>>(
-                    args, (int)num_kb);
-                e = cudaGetLastError();
+                cudaLaunchAttribute fa[1];
+                const cudaLaunchConfig_t fc =
+                    pdl_config(dim3((unsigned)(2 * rem), (unsigned)(args.bn / 8), 1), dim3(128), 0, s, fa);
+                e = cudaLaunchKernelEx(&fc, pair_sk_fixup_kernel<T, DUAL, F8>, static_cast<const PairArgs>(args),
+                                       (int)num_kb);
             }
             const cudaError_t f = cudaFreeAsync(buf, s);
             return e != cudaSuccess ? e : f;
@@ -1853,6 +2167,23 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
         }
         return p.elt == Elt::BF16 ? launch_typed<__nv_bfloat16, 1, true>(p, num_sms, status, s)
                                   : launch_typed<__half, 0, true>(p, num_sms, status, s);
+    }
+    // Weights as the MMA's rows (umma_skinny_kernel): 128-column strips of C,
+    // one CTA each, or clusters of cs CTAs splitting K when the strips alone
+    // leave SMs idle -- the cs with the most CTAs, all of them resident at once.
+    if (p.M <= 64 && g_umma_skinny) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const long long tiles_n = (p.N + 127) / 128;
+        const long long num_kb = (p.K + BK - 1) / BK;
+        if (tiles_n <= num_sms) {
+            int cs = 1;
+            for (int c = 2; c <= 8; ++c)
+                if (c <= num_kb && tiles_n * c <= num_sms && skinny_clusters_max(p.elt, c, dev) >= tiles_n) cs = c;
+            return p.elt == Elt::BF16 ? launch_skinny_typed<__nv_bfloat16, 1>(p, cs, status, s)
+                                      : launch_skinny_typed<__half, 0>(p, cs, status, s);
+        }
     }
     // Split K over clusters: tiles of bn = 256, 192 or 128 columns and clusters
     // of 2 to 8 CTAs, the pair that puts the most CTAs to work with every
