@@ -26,6 +26,20 @@ inline void pdl_attr(cudaLaunchAttribute &a) {
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a.val.programmaticStreamSerializationAllowed = 1;
 }
+// Launch configuration of a kernel without clusters, with programmatic
+// dependent launch allowed (the attribute array must outlive the launch call).
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    pdl_attr(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = g_pdl ? 1 : 0;
+    return cfg;
+}
 #ifdef __CUDACC__
 __device__ __forceinline__ void pdl_launch_dependents() {
     if (g_pdl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

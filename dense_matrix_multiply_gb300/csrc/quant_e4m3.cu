@@ -32,6 +32,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(WARPS * 32)
 quantize_rows_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, float *__restrict__ scale, int M,
                      int K) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
     if (row >= M) return;
@@ -96,13 +98,13 @@ bool quantize_rows_vec_ok(const void *A, const void *Q, int K) {
 cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int M, int K, cudaStream_t s) {
     const long long blocks = ((long long)M + WARPS - 1) / WARPS;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(WARPS * 32), 0, s, attr);
     if (quantize_rows_vec_ok(A, Q, K))
-        quantize_rows_kernel<true><<<(unsigned)blocks, WARPS * 32, 0, s>>>(
-            static_cast<const __half *>(A), static_cast<uint8_t *>(Q), scale, M, K);
-    else
-        quantize_rows_kernel<false><<<(unsigned)blocks, WARPS * 32, 0, s>>>(
-            static_cast<const __half *>(A), static_cast<uint8_t *>(Q), scale, M, K);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<true>, static_cast<const __half *>(A),
+                                  static_cast<uint8_t *>(Q), scale, M, K);
+    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<false>, static_cast<const __half *>(A),
+                              static_cast<uint8_t *>(Q), scale, M, K);
 }
 
 }  // namespace gemm_gb300

@@ -97,6 +97,8 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
                  int M, int N, int K, int tile_begin, SimtEx ex)
 {
     static_assert(MT == 128 || MT == 64, "CTA covers a whole or half tile");
+    pdl_launch_dependents();
+    pdl_wait();
     static_assert(EX || (!TA && !TB), "transposed operands need the general form");
     constexpr int RG = MT / 32;  // groups of four rows per thread
     constexpr int BLD = TB ? B_LD + 4 : B_LD;
@@ -328,6 +330,8 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
                   int N, int K, SimtEx ex)
 {
     static_assert(EX || (!TA && !TB), "transposed operands need the general form");
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ __align__(16) uint8_t f2_smem[];
     F2Shared &sm = *reinterpret_cast<F2Shared *>(f2_smem);
     constexpr int QA = G_BK / 4;                     // quads of k per A row ([M,K] storage)
@@ -555,8 +559,9 @@ cudaError_t launch_ffma2(const float *A, const float *B, float *C, int M, int N,
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     constexpr int smem = (int)sizeof(F2Shared);
     static_assert(smem <= 48 * 1024, "launched without the large-shared-memory attribute");
-    simt_ffma2_kernel<EX, TA, TB><<<dim3((unsigned)tiles, batches, 1), THREADS, smem, s>>>(A, B, C, M, N, K, ex);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)tiles, batches, 1), dim3(THREADS), smem, s, attr);
+    return cudaLaunchKernelEx(&cfg, simt_ffma2_kernel<EX, TA, TB>, A, B, C, M, N, K, ex);
 }
 
 // Tile configuration of the SIMT kernel: K step and CTAs per SM.
@@ -589,15 +594,17 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     const long long split = 2 * tiles <= slots ? tiles : 0;
     const long long whole = tiles - split;
     if (whole > 0) {
-        simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 128><<<(unsigned)whole, THREADS, 0, s>>>(
-            A, B, C, p.M, p.N, p.K, 0, SimtEx{});
-        const cudaError_t e = cudaGetLastError();
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)whole), dim3(THREADS), 0, s, attr);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 128>, A,
+                                                 B, C, p.M, p.N, p.K, 0, SimtEx{});
         if (e != cudaSuccess) return e;
     }
     if (split > 0) {
-        simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 64><<<(unsigned)(2 * split), THREADS, 0, s>>>(
-            A, B, C, p.M, p.N, p.K, (int)whole, SimtEx{});
-        const cudaError_t e = cudaGetLastError();
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(2 * split)), dim3(THREADS), 0, s, attr);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 64>, A,
+                                                 B, C, p.M, p.N, p.K, (int)whole, SimtEx{});
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -620,9 +627,10 @@ cudaError_t launch_ex_typed(const ProblemEx &p, cudaStream_t s) {
             // float4-able FP32: the packed-FMA kernel
             e = launch_ffma2<true, TA, TB>(A, B, C, p.M, p.N, p.K, ex, (unsigned)nb, s);
         } else {
-            simt_gemm_kernel<TIn, TIn, VEC, SIMT_BK, SIMT_MINB, 128, true, TA, TB>
-                <<<dim3((unsigned)tiles, (unsigned)nb, 1), THREADS, 0, s>>>(A, B, C, p.M, p.N, p.K, 0, ex);
-            e = cudaGetLastError();
+            cudaLaunchAttribute attr[1];
+            const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)tiles, (unsigned)nb, 1), dim3(THREADS), 0, s, attr);
+            e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TIn, TIn, VEC, SIMT_BK, SIMT_MINB, 128, true, TA, TB>, A, B,
+                                   C, p.M, p.N, p.K, 0, ex);
         }
         if (e != cudaSuccess) return e;
     }

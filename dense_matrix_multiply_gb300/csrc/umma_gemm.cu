@@ -1624,19 +1624,6 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 }
 
 // ------------------------------------------------------------------ host side
-// Launch configuration of a kernel without clusters, with programmatic
-// dependent launch allowed (the attribute array must outlive the launch call).
-cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute *attr) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    pdl_attr(attr[0]);
-    cfg.attrs = attr;
-    cfg.numAttrs = g_pdl ? 1 : 0;
-    return cfg;
-}
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                    CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
