@@ -1,14 +1,16 @@
 // Tensor-core GEMM on sm_103a: tcgen05 MMA, TMEM accumulators, TMA loads,
 // warp specialisation, persistent tile loops.  The file holds four kernels:
-//   * umma_gemm_kernel -- one CTA per 128 x 256 tile (M <= 128, and A rows that
-//     only 8-byte cp.async can fetch); described first, below;
+//   * umma_gemm_kernel -- one CTA per 128 x 256 tile: one row tile (M <= 128)
+//     that the skinny kernel does not take, and A rows that only 8-byte
+//     cp.async can fetch; described first, below;
 //   * umma_pair_kernel -- 256 x 256 tiles on 2-CTA clusters (cta_group::2), the
 //     kernel of every larger problem, of the general form (3-D tensor maps,
 //     either major-ness, alpha/beta, batches), of the fused FFN gate/up
 //     projection (DUAL) and of the row-scaled E4M3 product (F8,
 //     kind::f8f6f4);
-//   * umma_splitk_kernel -- M <= 64 with few column tiles: K split over a
-//     cluster, partials reduced through distributed shared memory.
+//   * umma_skinny_kernel -- M <= 64: the weights as the MMA's 128 rows, the
+//     M rows of the activations as its N (decode batches);
+//   * pair_sk_fixup_kernel -- adds the stream-K partials of the pair kernel.
 //
 // Problem (row-major): C[M,N] = A[M,K] · B[K,N], A and B both f16 or both bf16
 // (or both E4M3 codes), FP32 accumulation in tensor memory, one rounding to
@@ -70,11 +72,6 @@ constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 
 constexpr int SMEM_TILES = STAGES * (A_STAGE + B_STAGE);
 
-// Whether one-row-tile problems with few column tiles split K over clusters.
-#ifndef UMMA_SPLITK
-#define UMMA_SPLITK 1
-#endif
-constexpr bool g_umma_splitk = UMMA_SPLITK != 0;
 // Whether the CTA-pair kernel evens out a part-full last wave with a stream-K
 // tail (needs stream-ordered scratch).
 #ifndef PAIR_SK
@@ -86,13 +83,6 @@ constexpr bool g_pair_sk = PAIR_SK != 0;
 #define UMMA_SKINNY 1
 #endif
 constexpr bool g_umma_skinny = UMMA_SKINNY != 0;
-// Narrowest column tile and largest cluster of the cluster split.
-#ifndef SPLITK_MIN_BN
-#define SPLITK_MIN_BN 128
-#endif
-#ifndef SPLITK_MAX_CS
-#define SPLITK_MAX_CS 8
-#endif
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + SMEM_TILES + 256 /*barriers*/;
 
 // Status codes ORed into the device status word.
@@ -1204,216 +1194,6 @@ pair_sk_fixup_kernel(const PairArgs args, int num_kb)
     }
 }
 
-// ------------------------------------------------------ skinny M: split K
-// For M <= 128 (one row tile) the single-CTA kernel has only ceil(N / 256)
-// tiles: for a decode-shaped projection (N = 12288) 48 of the SMs would stream
-// the weights and the rest would idle.  Here a cluster of CS CTAs shares each
-// 128 x bn tile (bn = 128, 192 or 256), CTA r taking k-blocks
-// [r*KB/CS, (r+1)*KB/CS), so that most SMs stream their share of B.  A stage
-// holds only M rows of A (rounded up to 8): a 128-row box would have TMA
-// zero-fill the rest on every stage, which measured 31 against 24 us at
-// M = 2..8.  Each CTA copies its FP32 partial (rows < M only) from tensor
-// memory into its shared memory (the operand stages are free by then); the
-// tile's (row, column group) pairs are dealt out to the CS CTAs, and each adds
-// the partials of ranks 0 .. CS-1 in that order through distributed shared
-// memory, rounds once and stores C.  Deterministic, no atomics, one launch, no
-// workspace.  Every barrier wait is bounded as in the single-CTA kernel; the
-// two cluster barriers are reached by every thread on every path.
-constexpr int SK_LD = BN + 4;
-// Rows of A a stage holds: M rounded up to the 8-row swizzle atom.  The MMA
-// still reads 128 rows; rows past these hold stale shared memory and only
-// reach accumulator rows that are never stored.
-__host__ __device__ constexpr int splitk_a_rows(int M) { return M >= BM ? BM : (M + 7) / 8 * 8; }   // floats per row of a partial tile (16-byte rows, 8 bank offsets)
-constexpr uint32_t SK_TMEM_COLS = 256;
-
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-template <typename T, uint32_t AB_FORMAT>
-__global__ void __launch_bounds__(THREADS, 1)
-umma_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   T *__restrict__ C, int M, int N, int K, int bn, int *status)
-{
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t *a_tiles = smem;
-    uint8_t *b_tiles = smem + STAGES * A_STAGE;
-    float *part = reinterpret_cast<float *>(smem);  // [M][SK_LD] once the stages are drained
-    Bars *bars = reinterpret_cast<Bars *>(smem + SMEM_TILES);
-    volatile int *abort_flag = &bars->abort;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank(), cs = cluster_nctarank();
-    const int n0 = (int)cluster_id_x() * bn;
-    const int num_kb = (K + BK - 1) / BK;
-    const int kb0 = (int)(((long long)num_kb * rank) / cs), kb1 = (int)(((long long)num_kb * (rank + 1)) / cs);
-    const bool has_work = kb1 > kb0;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1);
-        }
-        mbar_init(&bars->acc_full[0], 1);
-        mbar_init(&bars->drain, 1);
-        bars->abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-    }
-    if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, SK_TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = bars->tmem_base;
-    pdl_launch_dependents();
-    pdl_wait();  // the previous kernel's writes are visible from here on
-
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------------ producer
-        const int n_left = N - n0;
-        const int boxes = n_left >= bn ? bn / 64 : (n_left + 63) / 64;
-        int stage = 0;
-        uint32_t phase = 0;
-        long long issued = 0;
-        for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort_flag, true)) {
-                atomicOr(status, ST_PRODUCER);
-                *abort_flag = 1;
-                break;
-            }
-            mbar_arrive_expect_tx(&bars->full[stage], (uint32_t)(splitk_a_rows(M) * BK * 2 + boxes * B_BOX));
-            tma_load_2d(a_tiles + stage * A_STAGE, &tmA, &bars->full[stage], kb * BK, 0);
-            for (int j = 0; j < boxes; ++j)
-                tma_load_2d(b_tiles + stage * B_STAGE + j * B_BOX, &tmB, &bars->full[stage], n0 + j * 64, kb * BK);
-            ++issued;
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-        // Let every load this thread issued land before the stages are reused.
-        for (long long i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i) {
-            const int s = (int)(i % STAGES);
-            const uint32_t par = (uint32_t)((i / STAGES) & 1);
-            if (!mbar_wait(&bars->full[s], par, abort_flag, false)) {
-                atomicOr(status, ST_DRAIN);
-                break;
-            }
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------------------ MMA issuer
-        const uint32_t idesc = make_idesc(AB_FORMAT, BM, (uint32_t)bn);
-        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(a_tiles), 16, 1024);
-        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_tiles), B_BOX, 1024);
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t ad = a_desc0 + (uint64_t)((stage * A_STAGE) >> 4);
-            const uint64_t bd = b_desc0 + (uint64_t)((stage * B_STAGE) >> 4);
-#pragma unroll
-            for (int ks = 0; ks < BK / UMMA_K; ++ks)
-                umma(tmem_base, ad + ks * (32u >> 4), bd + ks * (2048u >> 4), idesc, (kb != kb0 || ks != 0));
-            umma_commit(&bars->empty[stage]);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-        if (ok) {
-            umma_commit(&bars->acc_full[0]);
-        } else {
-            atomicOr(status, ST_MMA);
-            *abort_flag = 1;
-        }
-        umma_commit(&bars->drain);
-        if (!mbar_wait(&bars->drain, 0, abort_flag, false)) atomicOr(status, ST_DRAIN);
-    } else if (warp >= 2) {
-        // ------------------------------------------------------------ partials
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-        const int row = quarter * 32 + lane;
-        bool ready = true;
-        if (has_work && !mbar_wait(&bars->acc_full[0], 0, abort_flag, true)) {
-            atomicOr(status, ST_EPILOGUE);
-            *abort_flag = 1;
-            ready = false;
-        }
-        tc_fence_after();
-        if (quarter * 32 < M) {  // warp-uniform
-#pragma unroll 1
-            for (int chunk = 0; chunk < bn / 32; ++chunk) {
-                uint32_t r[32];
-                if (has_work && ready) {
-                    tmem_ld_32cols(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(chunk * 32), r);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = 0u;
-                }
-                if (row < M) {
-                    float4 *dst = reinterpret_cast<float4 *>(part + row * SK_LD + chunk * 32);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-                }
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncwarp();
-    cluster_sync();  // every partial is in its CTA's shared memory, visible cluster-wide
-
-    {
-        // ------------------------------------------------------------ reduction
-        // The (row, four-column group) pairs of the tile are dealt out to the
-        // cs CTAs in equal contiguous ranges; for each, the partials of ranks
-        // 0 .. cs-1 are added in that order (16-byte loads through distributed
-        // shared memory, all issued before the additions).
-        cg::cluster_group cluster = cg::this_cluster();
-        const int cols = min(bn, N - n0);
-        const int groups = (cols + 3) / 4;
-        const int total = M * groups;
-        const int e0 = (int)(((long long)total * rank) / cs), e1 = (int)(((long long)total * (rank + 1)) / cs);
-        for (int e = e0 + threadIdx.x; e < e1; e += THREADS) {
-            const int r = e / groups, c = (e - r * groups) * 4;
-            float4 v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < (int)cs)
-                    v[j] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(part + r * SK_LD + c, j));
-            float4 acc = v[0];
-#pragma unroll
-            for (int j = 1; j < 8; ++j) {
-                if (j < (int)cs) {
-                    acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
-                }
-            }
-            T *dst = C + (size_t)r * N + n0 + c;
-            if (c + 4 <= cols) {
-                uint2 w;
-                w.x = pack2(acc.x, acc.y, (T *)nullptr);
-                w.y = pack2(acc.z, acc.w, (T *)nullptr);
-                *reinterpret_cast<uint2 *>(dst) = w;   // N % 8 == 0 and C 16-byte aligned
-            } else {
-                const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-                for (int q = 0; q < cols - c; ++q) store1(dst + q, a4[q]);
-            }
-        }
-    }
-    __syncwarp();
-    cluster_sync();  // every CTA keeps its shared memory until the others have read it
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, SK_TMEM_COLS);
-    }
-}
-
 // ------------------------------------------- skinny M: weights as the MMA's rows
 // For M <= 64 the roles of the operands swap: D = W^T X^T, i.e. C^T, with the
 // weights W [K, N] as the MMA's 128-row operand (a 128-column strip of W, MN-
@@ -1695,37 +1475,6 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
                               status, stall);
 }
 
-// Largest number of co-resident clusters of cs CTAs of the skinny-M kernel
-// (2 <= cs <= 8), per device and element type.
-int splitk_clusters_max(Elt elt, int cs, int dev) {
-    static std::atomic<int> cached[64][2][9];
-    static std::once_flag once[64][2][9];
-    if (cs < 2 || cs > 8) return 0;
-    const int t = elt == Elt::BF16 ? 1 : 0, ci = cs;
-    std::call_once(once[dev & 63][t][ci], [&] {
-        const void *kern = t ? reinterpret_cast<const void *>(umma_splitk_kernel<__nv_bfloat16, 1>)
-                             : reinterpret_cast<const void *>(umma_splitk_kernel<__half, 0>);
-        int n = 0;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)cs, 1, 1);
-            cfg.blockDim = dim3(THREADS, 1, 1);
-            cfg.dynamicSmemBytes = SMEM_BYTES;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = (unsigned)cs;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
-        }
-        cudaGetLastError();
-        cached[dev & 63][t][ci].store(n);
-    });
-    return cached[dev & 63][t][ci].load();
-}
-
 // Largest number of co-resident clusters of cs CTAs (2 <= cs <= 8) of the
 // swapped-operand skinny kernel, per device and element type.
 int skinny_clusters_max(Elt elt, int cs, int dev) {
@@ -1798,44 +1547,6 @@ cudaError_t launch_skinny_typed(const Problem &p, int cs, int *status, cudaStrea
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, cs, status);
-}
-
-// Split-K launch of the skinny-M kernel: ceil(N / bn) clusters of cs CTAs,
-// bn = 128, 192 or 256 columns per tile.
-template <typename T, uint32_t F>
-cudaError_t launch_splitk_typed(const Problem &p, int cs, int bn, int *status, cudaStream_t s) {
-    const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap ta, tb;
-    if (!make_map(&ta, p.A, dt, p.M, p.K, splitk_a_rows(p.M), BK) || !make_map(&tb, p.B, dt, p.K, p.N, BK, 64))
-        return cudaErrorInvalidValue;
-    auto kern = umma_splitk_kernel<T, F>;
-    static std::atomic<uint64_t> attr_done{0};  // one bit per device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done.fetch_or(bit, std::memory_order_release);
-    }
-    if (bn % 64 != 0 || bn < 64 || bn > BN) return cudaErrorInvalidValue;
-    const long long tiles_n = (p.N + bn - 1) / bn;
-    if (tiles_n * cs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(tiles_n * cs), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    pdl_attr(attr[1]);
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = g_pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, static_cast<T *>(p.C), p.M, p.N, p.K, bn, status);
 }
 
 // 3-D tensor map of `batch` matrices of [outer, inner] 16-bit elements: row
@@ -2178,36 +1889,6 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
             return p.elt == Elt::BF16 ? launch_skinny_typed<__nv_bfloat16, 1>(p, cs, status, s)
                                       : launch_skinny_typed<__half, 0>(p, cs, status, s);
         }
-    }
-    // Split K over clusters: tiles of bn = 256, 192 or 128 columns and clusters
-    // of 2 to 8 CTAs, the pair that puts the most CTAs to work with every
-    // cluster on the GPU at once (a cluster of CTAs with this much shared
-    // memory needs that many SMs of one GPC: 76, 36 and 15 clusters of 2, 4
-    // and 8 fit on a GB300); ties go to the wider tile.  N = 12288 takes
-    // 64 x 192-column tiles on clusters of 2 (128 CTAs).  Measured back to
-    // back with B from DRAM at N = 12288, K = 4096: M = 2 / 8 / 32 / 64 in
-    // 24.8 / 24.7 / 25.7 / 27.0 us; at N = 4096, K = 12288, M = 64 in 24.7 us
-    // (the 256-wide tiles on clusters of 2, 4, 8 alone with a full A box and
-    // the reduction on rank 0 took 30.9 / 28.1 / 27.6 / 31.5 and 33.8 us).
-    // At M = 128 a cluster reduction made it slower than the unsplit kernel
-    // (37.3 vs 34.8 us).
-    if (p.M <= 64 && g_umma_splitk) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        const long long num_kb = (p.K + BK - 1) / BK;
-        int cs = 0, bn = 0;
-        long long best = 0;
-        for (int w = BN; w >= SPLITK_MIN_BN; w -= 64) {
-            const long long tiles_n = (p.N + w - 1) / w;
-            for (int c = SPLITK_MAX_CS; c >= 2; --c) {
-                if (num_kb < c || splitk_clusters_max(p.elt, c, dev) < tiles_n) continue;
-                if (tiles_n * c > best) { best = tiles_n * c; cs = c; bn = w; }
-            }
-        }
-        if (cs >= 2)
-            return p.elt == Elt::BF16 ? launch_splitk_typed<__nv_bfloat16, 1>(p, cs, bn, status, s)
-                                      : launch_splitk_typed<__half, 0>(p, cs, bn, status, s);
     }
     // 256-row tiles on CTA pairs once M fills more than one 128-row tile.
     if (p.M > BM) {

@@ -110,7 +110,7 @@ MID_CASES = [
     ("f16_cm", 1032, 520, 260, None, "umma_f16"),
     ("bf16_rm", 256, 256, 256, "simt_scalar", "simt_bf16_scalar"),
     ("bf16_rm", 4, 520, 1000, "gemv", "gemv_bf16_vec"),
-    ("bf16_rm", 4, 520, 1000, None, "umma_bf16"),            # skinny M: split K over a cluster
+    ("bf16_rm", 4, 520, 1000, None, "umma_bf16"),            # skinny M: 5 strips, K split over clusters
     ("bf16_rm", 7, 130, 77, None, "gemv_bf16_scalar"),
     ("bf16_rm", 16, 256, 64, "umma", "umma_bf16"),
     ("f16_cm", 512, 256, 512, None, "umma_f16"),
@@ -119,16 +119,16 @@ MID_CASES = [
     ("f16_cm", 250, 3, 128, None, "gemv_f16_scalar"),
     ("f16_cm", 1000, 8, 1000, "gemv", "gemv_f16_vec"),
     ("f16_cm", 1000, 8, 1000, None, "umma_f16"),
-    ("bf16_rm", 1, 1024, 512, "umma", "umma_bf16"),          # split K: 4 tiles x 8 ranks
-    ("bf16_rm", 2, 264, 128, None, "umma_bf16"),             # 2 tiles x 2 ranks
-    ("bf16_rm", 64, 2048, 4096, None, "umma_bf16"),          # 8 tiles x 8 ranks
+    ("bf16_rm", 1, 1024, 512, "umma", "umma_bf16"),          # skinny M = 1: 8 strips x 4 ranks
+    ("bf16_rm", 2, 264, 128, None, "umma_bf16"),             # 3 strips (the last one 8 columns)
+    ("bf16_rm", 64, 2048, 4096, None, "umma_bf16"),          # 16 strips on clusters, M = 64
     ("bf16_rm", 60, 520, 1000, None, "umma_bf16"),           # ragged N and K
-    ("bf16_rm", 40, 5000, 520, None, "umma_bf16"),           # 20 tiles x 4 ranks
-    ("bf16_rm", 33, 10240, 256, None, "umma_bf16"),          # 40 tiles x 2 ranks
+    ("bf16_rm", 40, 5000, 520, None, "umma_bf16"),           # 40 strips, ragged N
+    ("bf16_rm", 33, 10240, 256, None, "umma_bf16"),          # 80 strips, one CTA each, M = 33
     ("f16_cm", 2000, 128, 2056, None, "umma_f16"),           # row-major M = 128, N = 2000
-    ("bf16_rm", 8, 12288, 1024, None, "umma_bf16"),          # 192-column tiles, clusters of 2
-    ("bf16_rm", 16, 4096, 12288, None, "umma_bf16"),         # long K, clusters wider than 4
-    ("bf16_rm", 3, 1032, 2000, None, "umma_bf16"),           # 8-row A box, 3 rows used; ragged K
+    ("bf16_rm", 8, 12288, 1024, None, "umma_bf16"),          # 96 strips, one CTA each
+    ("bf16_rm", 16, 4096, 12288, None, "umma_bf16"),         # long K, 32 strips on clusters
+    ("bf16_rm", 3, 1032, 2000, None, "umma_bf16"),           # 8-row X box, 3 rows used; ragged K
     ("f16_cm", 1000, 24, 3000, None, "umma_f16"),            # row-major M = 24 through the swap
 ]
 
