@@ -61,15 +61,15 @@ L2_BYTES = 129e6
 TRAFFIC = {
     "sgemm_f32_rm_4096": {"bytes": 332552960 + 56349184, "source": "4591f96fc095"},
     "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 332350208 + 56457216, "source": "4591f96fc095"},
-    "hgemm_f16_cm_8192": {"bytes": 1070711808 + 127571712, "source": "be67485f009d"},
+    "hgemm_f16_cm_8192": {"bytes": 1051184896 + 125360384, "source": "d24d5e09f2f7"},
     # the CTA-pair kernel of a stream-K call (its fix-up kernel adds ~13 MB of reads)
-    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183149568 + 22814208, "source": "be67485f009d"},
-    "ffn_bf16_rm_1024x12288x4096": {"bytes": 109986816 + 11990784, "source": "be67485f009d"},
-    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211716608 + 18852096, "source": "be67485f009d"},
-    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1061788160 + 126854144, "source": "be67485f009d"},
-    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23119360 + 0, "source": "be67485f009d"},
+    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183051520 + 23331584, "source": "d24d5e09f2f7"},
+    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110027264 + 11684608, "source": "d24d5e09f2f7"},
+    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211818496 + 18851840, "source": "d24d5e09f2f7"},
+    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1065491200 + 125358592, "source": "d24d5e09f2f7"},
+    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120128 + 0, "source": "d24d5e09f2f7"},
     "edge_bf16_rm_1x12288x4096": {"bytes": 100694272 + 2970368, "source": "5f207a626cba"},
-    "edge_bf16_rm_32x12288x4096": {"bytes": 100953600 + 3487488, "source": "be67485f009d"},
+    "edge_bf16_rm_32x12288x4096": {"bytes": 100960512 + 3789824, "source": "d24d5e09f2f7"},
 }
 
 KERNEL_SOURCE = {
