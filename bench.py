@@ -57,19 +57,20 @@ L2_BYTES = 129e6
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture, keyed by workload; valid only while the kernel's source is the one
-# captured (sha256 prefix of the .cu file), else reported as null.
+# captured (sha256 prefix of the .cu file's code, comments and blank lines
+# removed), else reported as null.
 TRAFFIC = {
-    "sgemm_f32_rm_4096": {"bytes": 332552960 + 56349184, "source": "4591f96fc095"},
-    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 332350208 + 56457216, "source": "4591f96fc095"},
-    "hgemm_f16_cm_8192": {"bytes": 1051184896 + 125360384, "source": "d24d5e09f2f7"},
+    "sgemm_f32_rm_4096": {"bytes": 332552960 + 56349184, "source": "ba24604662c2"},
+    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 332350208 + 56457216, "source": "ba24604662c2"},
+    "hgemm_f16_cm_8192": {"bytes": 1051184896 + 125360384, "source": "2c2aa80a2c68"},
     # the CTA-pair kernel of a stream-K call (its fix-up kernel adds ~13 MB of reads)
-    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183051520 + 23331584, "source": "d24d5e09f2f7"},
-    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110027264 + 11684608, "source": "d24d5e09f2f7"},
-    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211818496 + 18851840, "source": "d24d5e09f2f7"},
-    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1065491200 + 125358592, "source": "d24d5e09f2f7"},
-    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120128 + 0, "source": "d24d5e09f2f7"},
-    "edge_bf16_rm_1x12288x4096": {"bytes": 100694272 + 2970368, "source": "5f207a626cba"},
-    "edge_bf16_rm_32x12288x4096": {"bytes": 100960512 + 3789824, "source": "d24d5e09f2f7"},
+    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183051520 + 23331584, "source": "2c2aa80a2c68"},
+    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110027264 + 11684608, "source": "2c2aa80a2c68"},
+    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211818496 + 18851840, "source": "2c2aa80a2c68"},
+    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1065491200 + 125358592, "source": "2c2aa80a2c68"},
+    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120128 + 0, "source": "2c2aa80a2c68"},
+    "edge_bf16_rm_1x12288x4096": {"bytes": 100694272 + 2970368, "source": "5b281193703f"},
+    "edge_bf16_rm_32x12288x4096": {"bytes": 100960512 + 3789824, "source": "2c2aa80a2c68"},
 }
 
 KERNEL_SOURCE = {
@@ -119,10 +120,40 @@ def read_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_text(src: str) -> str:
+    """C/C++/CUDA source without its comments and blank lines, each line stripped:
+    what the compiler sees, so that editing a comment keeps a capture valid."""
+    out, i, n = [], 0, len(src)
+    in_str = in_chr = False
+    while i < n:
+        c = src[i]
+        if in_str or in_chr:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(src[i + 1])
+                i += 2
+                continue
+            if (in_str and c == '"') or (in_chr and c == "'"):
+                in_str = in_chr = False
+            i += 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            in_str, in_chr = c == '"', c == "'"
+            out.append(c)
+            i += 1
+    return "\n".join(line.strip() for line in "".join(out).splitlines() if line.strip())
+
+
 def source_hash(kind: str) -> str:
+    """sha256 prefix of a kernel file's code (comments and blank lines removed)."""
     path = os.path.join(ROOT, "dense_matrix_multiply_gb300", "csrc", KERNEL_SOURCE[kind])
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:12]
+    with open(path, encoding="utf-8") as f:
+        return hashlib.sha256(code_text(f.read()).encode()).hexdigest()[:12]
 
 
 # ------------------------------------------------------------------ clocks

@@ -191,9 +191,9 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     }
 
     // Skinny M: the streaming GEMV for FP32, for M = 1, and for 16-bit problems
-    // the tensor-core kernel cannot take; other 16-bit problems with M <= 8 run
-    // on the tensor cores (split K over clusters), which stream B faster once
-    // more than one row of A multiplies it.
+    // the tensor-core kernels cannot take; other 16-bit problems with M <= 8 run
+    // on the tensor cores (the skinny kernel, weights as the MMA's rows), which
+    // stream B faster once more than one row of A multiplies it.
     if (M <= kGemvMaxM && (elt == Elt::F32 || M == 1 || !umma_supported(p)))
         return gemv_vec_ok ? finish(launch_gemv(p, true, dev->num_sms, s), kernel_name("gemv", elt))
                            : finish(launch_gemv(p, false, dev->num_sms, s), kernel_name("gemv_scalar", elt));

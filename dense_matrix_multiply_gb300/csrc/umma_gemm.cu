@@ -1204,11 +1204,11 @@ pair_sk_fixup_kernel(const PairArgs args, int num_kb)
 // output column, a stage is 32 KiB of W + at most 16 KiB of X, so the four
 // stages keep 128 KiB of W in flight per SM in few, large TMA requests (a
 // 100 MB stream in 64 x 128 boxes measured 17.4 against 18.6 us in 64 x 64
-// boxes), and the accumulator is nb <= 64 tensor-memory columns.  Tile t = 128 columns of C; the CS CTAs of a
-// cluster split its K-blocks as the split-K kernel does and add their partials
-// through distributed shared memory in rank order (CS = 1: no cluster, C is
-// stored straight from tensor memory).  Deterministic, one launch, no
-// workspace; every barrier wait is bounded.
+// boxes), and the accumulator is nb <= 64 tensor-memory columns.  Tile t = 128
+// columns of C; the CS CTAs of a cluster take K-blocks [r*KB/CS, (r+1)*KB/CS)
+// of it and add their partials through distributed shared memory in rank
+// order (CS = 1: no cluster, C is stored straight from tensor memory).
+// Deterministic, one launch, no workspace; every barrier wait is bounded.
 constexpr int SKB = 128;                     // K per stage
 constexpr int SKS = 4;                       // stages
 constexpr int SK_W_BOX = 64 * SKB * 2;       // 64 columns x 128 k of W: 16 KiB
