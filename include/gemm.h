@@ -25,7 +25,12 @@
  * aligned (e.g. bf16 with K = 4100), an aligned copy of A taken from the
  * device's default stream-ordered pool (cudaMallocAsync / cudaFreeAsync on the
  * caller's stream); if that allocation fails the call uses a slower kernel
- * instead.
+ * instead.  A 16-bit problem on the CTA-pair tensor-core kernel whose tiles
+ * leave a nearly empty last wave (at most a quarter of the clusters busy, K of
+ * at least 48 blocks of 64) takes FP32 partial tiles for its stream-K tail from
+ * the same pool (512 KiB per participating CTA pair, at most ~39 MB), freed on
+ * the stream after the call; without it the call runs whole tiles.  The
+ * allocation-free entry point never allocates.
  *
  * Leading dimensions are tight:
  *   _rm (row-major):    A is [M,K] with lda = K, B is [K,N] with ldb = N,
@@ -37,9 +42,13 @@
  *
  * Execution.  Calls are asynchronous and ordered on the calling host thread's
  * stream (gemm_set_stream; default: the legacy default stream).  A call returns
- * once its kernel is enqueued; gemm_synchronize() waits for it.  Results are
- * deterministic: the same inputs give bit-identical C on every run (no atomics,
- * fixed summation order per element).
+ * once its kernels are enqueued; gemm_synchronize() waits for them.  The kernels
+ * are launched as programmatic dependents: one may start its set-up while the
+ * kernel before it on the stream drains, but it touches global memory only once
+ * that kernel has completed, so stream order holds for any producer of A or B
+ * and any consumer of C, the library's or not.  Calls may be captured into CUDA
+ * graphs.  Results are deterministic: the same inputs give bit-identical C on
+ * every run (no atomics, fixed summation order per element).
  *
  * Errors.  Every entry point returns a status; nothing is thrown across the ABI.
  *   GEMM_ERR_INVALID_VALUE      a dimension < 0, or a null pointer needed by the
