@@ -190,11 +190,25 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
         break;
     }
 
-    // Skinny M: the streaming GEMV for FP32, for M = 1, and for 16-bit problems
-    // the tensor-core kernels cannot take; other 16-bit problems with M <= 8 run
-    // on the tensor cores (the skinny kernel, weights as the MMA's rows), which
-    // stream B faster once more than one row of A multiplies it.
-    if (M <= kGemvMaxM && (elt == Elt::F32 || M == 1 || !umma_supported(p)))
+    // Skinny M: the streaming GEMV for FP32 and for 16-bit problems the
+    // tensor-core kernels cannot take; other 16-bit problems with 2 <= M <= 8
+    // run on the tensor cores (the skinny kernel, weights as the MMA's rows),
+    // which stream B faster once more than one row of A multiplies it.  For
+    // M = 1 the skinny kernel is taken when its 128-column strips, times the K
+    // split it can use, occupy at least 80 % of the SMs, or when N <= 2048;
+    // otherwise the GEMV, whose many small CTAs fill the GPU.  Measured back to
+    // back (bf16, W from DRAM), skinny against GEMV: N = 4096, K = 12288 20.4
+    // vs 23.7 us; N = 18944, K = 3584 22.8 vs 26.4; N = 4096, K = 4096 9.1 vs
+    // 10.5; N = 1024, K = 4096 5.9 vs 8.3; N = 12288, K = 4096 (96 strips on
+    // 152 SMs) 20.0 vs 19.3.
+    bool m1_tensor = false;
+    if (M == 1 && elt != Elt::F32 && umma_supported(p) && (K % 8) == 0 && aligned16(A)) {
+        const long long strips = (N + 127) / 128, kb = (K + 127) / 128;
+        long long cs = 1;
+        while (cs < 8 && strips * (cs + 1) <= dev->num_sms && cs + 1 <= kb) ++cs;
+        m1_tensor = strips <= dev->num_sms && (strips <= 16 || strips * cs * 5 >= 4LL * dev->num_sms);
+    }
+    if (M <= kGemvMaxM && (elt == Elt::F32 || (M == 1 && !m1_tensor) || !umma_supported(p)))
         return gemv_vec_ok ? finish(launch_gemv(p, true, dev->num_sms, s), kernel_name("gemv", elt))
                            : finish(launch_gemv(p, false, dev->num_sms, s), kernel_name("gemv_scalar", elt));
     if (elt == Elt::F32)
