@@ -65,8 +65,7 @@ template <typename T, int VW, int TC, int MM>
 __global__ void __launch_bounds__(THREADS)
 gemv_kernel(const T *__restrict__ X, const T *__restrict__ W, T *__restrict__ C, int M, int N, int K)
 {
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait();  // dependents launch as this grid's CTAs exit (several CTAs per SM: no early trigger)
     constexpr int TK = THREADS / TC;
     constexpr int CW = TC * VW;
     extern __shared__ float red[];

@@ -32,8 +32,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(WARPS * 32)
 quantize_rows_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, float *__restrict__ scale, int M,
                      int K) {
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait();  // dependents launch as this grid's CTAs exit (several CTAs per SM: no early trigger)
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
     if (row >= M) return;
