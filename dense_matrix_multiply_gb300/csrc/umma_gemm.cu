@@ -1201,22 +1201,31 @@ pair_sk_fixup_kernel(const PairArgs args, int num_kb)
 // rows of X as its N = nb operand (K-major, two boxes of 64 k x M rows rounded
 // up to 8; nb = M rounded up to 16, the stale rows past the box only reaching
 // accumulator columns that are never stored).  Every MMA row is a useful
-// output column, a stage is 32 KiB of W + at most 16 KiB of X, so the four
-// stages keep 128 KiB of W in flight per SM in few, large TMA requests (a
-// 100 MB stream in 64 x 128 boxes measured 17.4 against 18.6 us in 64 x 64
-// boxes), and the accumulator is nb <= 64 tensor-memory columns.  Tile t = 128
+// output column; a stage is 32 KiB of W + two X boxes of nb rows, and the
+// 216 KiB ring holds 6, 5 or 4 stages for M <= 16, 32 or 64 (used in full when
+// the grid leaves a third of the SMs idle, else four), keeping up to 192 KiB
+// of W in flight per SM in few, large TMA requests (a 100 MB stream in 64 x
+// 128 boxes measured 17.4 against 18.6 us in 64 x 64 boxes); the accumulator
+// is nb <= 64 tensor-memory columns.  Tile t = 128
 // columns of C; the CS CTAs of a cluster take K-blocks [r*KB/CS, (r+1)*KB/CS)
 // of it and add their partials through distributed shared memory in rank
 // order (CS = 1: no cluster, C is stored straight from tensor memory).
 // Deterministic, one launch, no workspace; every barrier wait is bounded.
 constexpr int SKB = 128;                     // K per stage
-constexpr int SKS = 4;                       // stages
+constexpr int SKS = 8;                       // stages, at most (barrier arrays)
 constexpr int SK_W_BOX = 64 * SKB * 2;       // 64 columns x 128 k of W: 16 KiB
 constexpr int SK_W_STAGE = 2 * SK_W_BOX;     // 128 columns: 32 KiB
-constexpr int SK_X_BOX = 64 * 64 * 2;        // up to 64 rows x 64 k of X: 8 KiB
-constexpr int SK_X_STAGE = 2 * SK_X_BOX;     // 128 k: 16 KiB
-constexpr int SK_SMEM_TILES = SKS * (SK_W_STAGE + SK_X_STAGE);
+constexpr int SK_SMEM_TILES = 216 * 1024;   // the ring: as many stages as fit
 constexpr int SK_SMEM_BYTES = 1024 + SK_SMEM_TILES + 256;
+// X's box per 64 k: nb rows of 128 bytes (the MMA reads nb rows; TMA fills the
+// first M rounded up to 8); a stage holds two.  W 32 KiB + X 4 / 8 / 12 / 16
+// KiB for M <= 16 / 32 / 48 / 64: 6, 5, 4, 4 stages.
+__host__ __device__ constexpr int skinny_x_box(int nb) { return nb * 128; }
+__host__ __device__ constexpr int skinny_stages(int nb) {
+    return SK_SMEM_TILES / (SK_W_STAGE + 2 * skinny_x_box(nb)) < SKS
+               ? SK_SMEM_TILES / (SK_W_STAGE + 2 * skinny_x_box(nb))
+               : SKS;
+}
 constexpr uint32_t SK2_TMEM_COLS = 64;
 constexpr int SK2_LD = 128 + 4;              // floats per m-row of a partial [nb][128]
 using SkBars = BarsT<SKS>;
@@ -1229,13 +1238,15 @@ __host__ __device__ constexpr int skinny_nb(int M) { return (M + 15) / 16 * 16; 
 template <typename T, uint32_t AB_FORMAT>
 __global__ void __launch_bounds__(THREADS, 1)
 umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   T *__restrict__ C, int M, int N, int K, int cs, int *status)
+                   T *__restrict__ C, int M, int N, int K, int cs, int max_stages, int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *w_tiles = smem;
-    uint8_t *x_tiles = smem + SKS * SK_W_STAGE;
+    const int stages = min(skinny_stages(skinny_nb(M)), max_stages);
+    const int x_box = skinny_x_box(skinny_nb(M)), x_stage = 2 * x_box;
+    uint8_t *x_tiles = smem + stages * SK_W_STAGE;
     float *part = reinterpret_cast<float *>(smem);  // [nb][SK2_LD] once the stages are drained
     SkBars *bars = reinterpret_cast<SkBars *>(smem + SK_SMEM_TILES);
     volatile int *abort_flag = &bars->abort;
@@ -1249,7 +1260,7 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const int x_rows = skinny_x_rows(M), nb = skinny_nb(M);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SKS; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
@@ -1289,15 +1300,15 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             for (int j = 0; j < wboxes; ++j)
                 tma_load_2d(w_tiles + stage * SK_W_STAGE + j * SK_W_BOX, &tmW, &bars->full[stage], n0 + 64 * j,
                             kb * SKB);
-            tma_load_2d(x_tiles + stage * SK_X_STAGE, &tmX, &bars->full[stage], kb * SKB, 0);
-            tma_load_2d(x_tiles + stage * SK_X_STAGE + SK_X_BOX, &tmX, &bars->full[stage], kb * SKB + 64, 0);
+            tma_load_2d(x_tiles + stage * x_stage, &tmX, &bars->full[stage], kb * SKB, 0);
+            tma_load_2d(x_tiles + stage * x_stage + x_box, &tmX, &bars->full[stage], kb * SKB + 64, 0);
             ++issued;
-            if (++stage == SKS) { stage = 0; phase ^= 1u; }
+            if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
         // Let every load this thread issued land before the stages are reused.
-        for (long long i = (issued > SKS ? issued - SKS : 0); i < issued; ++i) {
-            const int s = (int)(i % SKS);
-            const uint32_t par = (uint32_t)((i / SKS) & 1);
+        for (long long i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+            const int s = (int)(i % stages);
+            const uint32_t par = (uint32_t)((i / stages) & 1);
             if (!mbar_wait(&bars->full[s], par, abort_flag, false)) {
                 atomicOr(status, ST_DRAIN);
                 break;
@@ -1319,13 +1330,13 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             if (!mbar_wait(&bars->full[stage], phase, abort_flag, true)) { ok = false; break; }
             tc_fence_after();
             const uint64_t ad = a_desc0 + (uint64_t)((stage * SK_W_STAGE) >> 4);
-            const uint64_t bd = b_desc0 + (uint64_t)((stage * SK_X_STAGE) >> 4);
+            const uint64_t bd = b_desc0 + (uint64_t)((stage * x_stage) >> 4);
 #pragma unroll
             for (int ks = 0; ks < SKB / UMMA_K; ++ks)
                 umma(tmem_base, ad + ks * (2048u >> 4),
-                     bd + (uint32_t)(((ks >> 2) * SK_X_BOX + (ks & 3) * 32) >> 4), idesc, (kb != kb0 || ks != 0));
+                     bd + (uint32_t)(((ks >> 2) * x_box + (ks & 3) * 32) >> 4), idesc, (kb != kb0 || ks != 0));
             umma_commit(&bars->empty[stage]);
-            if (++stage == SKS) { stage = 0; phase ^= 1u; }
+            if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
         if (ok) {
             umma_commit(&bars->acc_full[0]);
@@ -1509,7 +1520,7 @@ int skinny_clusters_max(Elt elt, int cs, int dev) {
 // Swapped-operand skinny launch: ceil(N / 128) column strips, each on one CTA
 // (cs = 1) or on a cluster of cs CTAs splitting K.
 template <typename T, uint32_t F>
-cudaError_t launch_skinny_typed(const Problem &p, int cs, int *status, cudaStream_t s) {
+cudaError_t launch_skinny_typed(const Problem &p, int cs, int num_sms, int *status, cudaStream_t s) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (p.M < 1 || p.M > 64 || cs < 1 || cs > 8) return cudaErrorInvalidValue;
     CUtensorMap tx, tw;
@@ -1528,10 +1539,15 @@ cudaError_t launch_skinny_typed(const Problem &p, int cs, int *status, cudaStrea
     }
     const long long tiles_n = (p.N + 127) / 128;
     if (tiles_n * cs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    // The whole ring (up to six stages) when the grid leaves a third of the SMs
+    // idle, else four stages: measured back to back at N = 12288 (96 CTAs),
+    // M = 1 / 8 / 32, 18.8 / 18.9 / 19.9 us against 19.9 / 20.4 / 21.2 with
+    // four; with 128-148 CTAs the deeper ring was 3 % slower.
+    const int max_stages = 3 * tiles_n * cs <= 2LL * num_sms ? SKS : 4;
     if (cs == 1) {
         cudaLaunchAttribute a1[1];
         const cudaLaunchConfig_t c1 = pdl_config(dim3((unsigned)tiles_n), dim3(THREADS), SK_SMEM_BYTES, s, a1);
-        return cudaLaunchKernelEx(&c1, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, 1, status);
+        return cudaLaunchKernelEx(&c1, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, 1, max_stages, status);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles_n * cs), 1, 1);
@@ -1546,7 +1562,7 @@ cudaError_t launch_skinny_typed(const Problem &p, int cs, int *status, cudaStrea
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, cs, status);
+    return cudaLaunchKernelEx(&cfg, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, cs, max_stages, status);
 }
 
 // 3-D tensor map of `batch` matrices of [outer, inner] 16-bit elements: row
@@ -1886,8 +1902,8 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
             int cs = 1;
             for (int c = 2; c <= 8; ++c)
                 if (c <= num_kb && tiles_n * c <= num_sms && skinny_clusters_max(p.elt, c, dev) >= tiles_n) cs = c;
-            return p.elt == Elt::BF16 ? launch_skinny_typed<__nv_bfloat16, 1>(p, cs, status, s)
-                                      : launch_skinny_typed<__half, 0>(p, cs, status, s);
+            return p.elt == Elt::BF16 ? launch_skinny_typed<__nv_bfloat16, 1>(p, cs, num_sms, status, s)
+                                      : launch_skinny_typed<__half, 0>(p, cs, num_sms, status, s);
         }
     }
     // 256-row tiles on CTA pairs once M fills more than one 128-row tile.
