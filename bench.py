@@ -62,15 +62,15 @@ L2_BYTES = 129e6
 TRAFFIC = {
     "sgemm_f32_rm_4096": {"bytes": 330672640 + 56088576, "source": "6fc1384050df"},
     "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 332369920 + 56633344, "source": "6fc1384050df"},
-    "hgemm_f16_cm_8192": {"bytes": 1051184896 + 125360384, "source": "2c2aa80a2c68"},
+    "hgemm_f16_cm_8192": {"bytes": 1074523904 + 127308800, "source": "008d4192250d"},
     # the CTA-pair kernel of a stream-K call (its fix-up kernel adds ~13 MB of reads)
-    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183051520 + 23331584, "source": "2c2aa80a2c68"},
-    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110027264 + 11684608, "source": "2c2aa80a2c68"},
-    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211818496 + 18851840, "source": "2c2aa80a2c68"},
-    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1065491200 + 125358592, "source": "2c2aa80a2c68"},
-    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120128 + 0, "source": "2c2aa80a2c68"},
+    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183213824 + 22895872, "source": "008d4192250d"},
+    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110055936 + 12133632, "source": "008d4192250d"},
+    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211762176 + 18856192, "source": "008d4192250d"},
+    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1069819392 + 126654464, "source": "008d4192250d"},
+    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120128 + 0, "source": "008d4192250d"},
     "edge_bf16_rm_1x12288x4096": {"bytes": 100693760 + 3156992, "source": "d90871b19f35"},
-    "edge_bf16_rm_32x12288x4096": {"bytes": 100960512 + 3789824, "source": "2c2aa80a2c68"},
+    "edge_bf16_rm_32x12288x4096": {"bytes": 100962560 + 3704832, "source": "008d4192250d"},
 }
 
 KERNEL_SOURCE = {
