@@ -55,22 +55,24 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "sm_max_mhz": 2070.0}
 L2_BYTES = 129e6
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# DRAM traffic per call (dram__bytes_read.sum + dram__bytes_write.sum, summed over
+# the kernels the call launches, the fix-up of a stream-K call excepted) from one
 # ncu capture, keyed by workload; valid only while the kernel's source is the one
 # captured (sha256 prefix of the .cu file's code, comments and blank lines
 # removed), else reported as null.
 TRAFFIC = {
-    "sgemm_f32_rm_4096": {"bytes": 330672640 + 56088576, "source": "6fc1384050df"},
-    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 332369920 + 56633344, "source": "6fc1384050df"},
-    "hgemm_f16_cm_8192": {"bytes": 1074523904 + 127308800, "source": "008d4192250d"},
-    # the CTA-pair kernel of a stream-K call (its fix-up kernel adds ~13 MB of reads)
-    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183213824 + 22895872, "source": "008d4192250d"},
-    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110055936 + 12133632, "source": "008d4192250d"},
-    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211762176 + 18856192, "source": "008d4192250d"},
-    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1069819392 + 126654464, "source": "008d4192250d"},
-    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120128 + 0, "source": "008d4192250d"},
-    "edge_bf16_rm_1x12288x4096": {"bytes": 100693760 + 3156992, "source": "d90871b19f35"},
-    "edge_bf16_rm_32x12288x4096": {"bytes": 100962560 + 3704832, "source": "008d4192250d"},
+    # both grids of the call: the whole rounds (304.2 + 51.4 MB) and the half-K last round (46.2 + 1.2 MB)
+    "sgemm_f32_rm_4096": {"bytes": 304213248 + 51446528 + 46163712 + 1196544, "source": "eced23f8e828"},
+    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 331792384 + 56420608, "source": "eced23f8e828"},
+    "hgemm_f16_cm_8192": {"bytes": 1046693632 + 125557248, "source": "7fc1ab5c13f8"},
+    # the CTA-pair kernel of a stream-K call (its fix-up kernel adds 12.6 MB of reads)
+    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183561472 + 22897408, "source": "7fc1ab5c13f8"},
+    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110036736 + 11962624, "source": "7fc1ab5c13f8"},
+    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211854336 + 18776064, "source": "7fc1ab5c13f8"},
+    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1065488896 + 124942848, "source": "7fc1ab5c13f8"},
+    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120640 + 0, "source": "7fc1ab5c13f8"},
+    "edge_bf16_rm_1x12288x4096": {"bytes": 100693760 + 3052544, "source": "a821897d27f4"},
+    "edge_bf16_rm_32x12288x4096": {"bytes": 100961024 + 3403776, "source": "7fc1ab5c13f8"},
 }
 
 KERNEL_SOURCE = {
@@ -699,7 +701,9 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     torch.cuda.synchronize()
     time.sleep(0.2 if clocks else 0)
     t_host0 = time.time()
+    launches0 = g.gemm_kernel_launches()
     ms = (time_device_flushed if flushed else time_device)(step, steps, 0, stream)
+    launches = g.gemm_kernel_launches() - launches0  # the library's own count of its launches
     t_host1 = time.time()
     g.gemm_synchronize()
     clk = None
@@ -717,7 +721,7 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         "ms_per_step": ms / steps, "tflops": flops / s_per / 1e12, "steps": steps, "ms_total": ms,
         "roofline": roofline_for(kind, variant, M, N, K, s_kernel, peaks, peaks_src,
                                  clk["sm_mhz"] if clk else None, sms, name, prop_mhz),
-        "clocks": clk, "footprint_bytes": int(footprint),
+        "clocks": clk, "footprint_bytes": int(footprint), "gpu_launches": int(launches),
         "l2": (f"{footprint / 2**20:.1f} MiB of operands fit in the 129 MB L2: calls rotate over {rotated} "
                f"copies ({rotated * footprint / 2**20:.0f} MiB), each read from DRAM, back to back"
                if rotated > 1 else
@@ -822,7 +826,8 @@ def run_ours(args):
             r = measure_workload(wl, max(5, args.path_steps), 3, peaks, peaks_src, sms, stream,
                                  sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True, prop_mhz=prop_mhz)
             paths.append({k: r[k] for k in ("workload", "kernel", "M", "N", "K", "ms_per_step", "tflops",
-                                            "roofline", "clocks", "kernels", "cublas", "l2") if k in r})
+                                            "roofline", "clocks", "kernels", "cublas", "l2", "gpu_launches")
+                          if k in r})
 
     if rank == 0:
         M, N, K = res["M"], res["N"], res["K"]
@@ -842,7 +847,8 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "kernel": res["kernel"],
             "roofline": res["roofline"],
-            "gpu_launches": args.steps * (2 if res["variant"] == "e4m3_rowscale" else 1),
+            # counted by the library over rank 0's timed steps; every replica runs the same calls
+            "gpu_launches": res["gpu_launches"] * world,
             "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
                        "reasons": clk.get("reasons", []), "samples": clk.get("samples", 0)},
         }

@@ -47,6 +47,7 @@ SIGNATURES = {
     "gemm_synchronize": ([], _I),
     "gemm_status_string": ([_I], ctypes.c_char_p),
     "gemm_last_kernel": ([], ctypes.c_char_p),
+    "gemm_kernel_launches": ([], ctypes.c_ulonglong),
     "gemm_last_error": ([], ctypes.c_char_p),
     "gemm_force_kernel": ([ctypes.c_char_p], _I),
 }
@@ -208,6 +209,10 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_last_kernel() -> str:
     return load().gemm_last_kernel().decode()
+
+
+def gemm_kernel_launches() -> int:
+    return int(load().gemm_kernel_launches())
 
 
 def gemm_last_error() -> str:

@@ -14,6 +14,8 @@
 
 using namespace gemm_gb300;
 
+std::atomic<unsigned long long> gemm_gb300::g_launches{0};
+
 namespace {
 
 enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma, UmmaStall };
@@ -49,6 +51,7 @@ __global__ void zero_fill_bytes_kernel(uint8_t *p, size_t n) {
 // Zeros `bytes` bytes at p on stream s (16-byte stores when p is aligned).
 cudaError_t zero_fill(void *p, size_t bytes, int num_sms, cudaStream_t s) {
     const unsigned grid = (unsigned)(num_sms * 4);
+    note_launch();
     if (((uintptr_t)p & 15u) == 0) {
         zero_fill_kernel<<<grid, 256, 0, s>>>((uint4 *)p, bytes / 16, (uint8_t *)p + (bytes & ~(size_t)15),
                                               bytes & 15);
@@ -328,6 +331,7 @@ gemm_status_t run_ex(int dtype, int layout, int op_a, int op_b, int M, int N, in
     if (!use_ab) {
         if (t_force != Family::Auto) return GEMM_ERR_INVALID_VALUE;
         const unsigned grid = (unsigned)(dev->num_sms * 8);
+        note_launch();
         switch (elt) {
         case Elt::F32: scale_c_kernel<<<grid, 256, 0, s>>>((float *)C, M, N, ldc, sc, batch, beta); break;
         case Elt::F16: scale_c_kernel<<<grid, 256, 0, s>>>((__half *)C, M, N, ldc, sc, batch, beta); break;
@@ -547,6 +551,8 @@ GEMM_API const char *gemm_status_string(gemm_status_t s) {
 }
 
 GEMM_API const char *gemm_last_kernel(void) { return t_last_kernel; }
+
+GEMM_API unsigned long long gemm_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 GEMM_API const char *gemm_last_error(void) { return t_last_error; }
 

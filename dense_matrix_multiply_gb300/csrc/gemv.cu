@@ -182,7 +182,7 @@ cudaError_t launch_cfg(const Problem &p, int num_sms, cudaStream_t s) {
     pdl_attr(attr[1]);
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<const T *>(p.A), static_cast<const T *>(p.B),
+    return launch_counted(&cfg, kern, static_cast<const T *>(p.A), static_cast<const T *>(p.B),
                               static_cast<T *>(p.C), p.M, p.N, p.K);
 }
 

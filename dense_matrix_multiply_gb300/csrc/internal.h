@@ -8,6 +8,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <utility>
+
 namespace gemm_gb300 {
 
 // Programmatic dependent launch.  Every kernel is launched with programmatic
@@ -19,18 +22,29 @@ namespace gemm_gb300 {
 // at once (pdl_launch_dependents); kernels with several CTAs per SM leave that
 // to their CTAs' exit, so that a small grid's successor is not placed, and
 // packed onto the same SMs, while the grid still runs (FP32 1000^3: 86 against
-// 49 us).  Back to back on GB300 this hides the 2-3 us between kernels: a
+// 49 us).  The one exception is the first grid of an FP32 problem split in two,
+// whose dependent is its own last round (that packing is the point).  Back to back on GB300 this hides the 2-3 us between kernels: a
 // 100 MB weight stream went from 18.5 to 15.9 us.
 #ifndef GEMM_PDL
 #define GEMM_PDL 1
 #endif
 constexpr bool g_pdl = GEMM_PDL != 0;
+// Kernel launches issued by the library (gemm_kernel_launches): every launch
+// goes through launch_counted or calls note_launch next to its <<< >>>.
+extern std::atomic<unsigned long long> g_launches;
+inline void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_counted(const cudaLaunchConfig_t *cfg, void (*kern)(KArgs...), Args &&...args) {
+    note_launch();
+    return cudaLaunchKernelEx(cfg, kern, std::forward<Args>(args)...);
+}
 inline void pdl_attr(cudaLaunchAttribute &a) {
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a.val.programmaticStreamSerializationAllowed = 1;
 }
-// Launch configuration of a kernel without clusters, with programmatic
-// dependent launch allowed (the attribute array must outlive the launch call).
+// Launch configuration with programmatic dependent launch allowed (the
+// attribute array must outlive the launch call; a cluster dimension may be
+// appended after it).
 inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                                      cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};

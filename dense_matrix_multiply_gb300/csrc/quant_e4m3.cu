@@ -100,9 +100,9 @@ cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int 
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(WARPS * 32), 0, s, attr);
     if (quantize_rows_vec_ok(A, Q, K))
-        return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<true>, static_cast<const __half *>(A),
+        return launch_counted(&cfg, quantize_rows_kernel<true>, static_cast<const __half *>(A),
                                   static_cast<uint8_t *>(Q), scale, M, K);
-    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<false>, static_cast<const __half *>(A),
+    return launch_counted(&cfg, quantize_rows_kernel<false>, static_cast<const __half *>(A),
                               static_cast<uint8_t *>(Q), scale, M, K);
 }
 

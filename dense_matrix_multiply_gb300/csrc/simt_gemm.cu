@@ -35,6 +35,7 @@
 // loaded along k and transposed into the n-contiguous layout on the way in,
 // into rows padded by four floats so that the transposing stores of a warp
 // fall in 32 distinct banks.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <algorithm>
@@ -44,6 +45,8 @@
 
 namespace gemm_gb300 {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int BM = 128, BN = 128, THREADS = 128;
 constexpr int A_LD = BM + 4;  // padded row of the k-major A tile (floats)
@@ -55,6 +58,11 @@ constexpr int GROUP_M = 8;
 #define SIMT_FFMA2 1
 #endif
 constexpr bool g_simt_ffma2 = SIMT_FFMA2 != 0;
+// Whether the packed-FMA kernel's part-full last round runs as K halves.
+#ifndef SIMT_SPLIT_TAIL
+#define SIMT_SPLIT_TAIL 1
+#endif
+constexpr bool g_simt_split_tail = SIMT_SPLIT_TAIL != 0;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
@@ -297,7 +305,13 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 //     has a whole compute step to arrive.  160 registers: three CTAs per SM.
 //   * Grouped rasterisation along M, predicated loads (zero fill) and stores.
 // Every product and sum is the scalar kernel's, in the same order, so the
-// results are bit-identical to it.  Measured on GB300 (CUDA events):
+// results are bit-identical to it, except in a split last round (below).
+//   * Split last round: when the tiles past the last full round of resident
+//     CTAs would fill at most half of a round, they run as a second grid of
+//     two-CTA clusters, one CTA per half of the K blocks, launched as a
+//     programmatic dependent that the first grid releases once all its CTAs
+//     are resident; such a tile is the sum of its two halves' FP32 sums.
+// Measured on GB300 (CUDA events):
 // 62.5 TFLOP/s at 4096^3 against 54.4 for the scalar-FFMA 128 x 128 kernel,
 // 38.9 against 24.3 at 1000^3; 128 x 128 tiles with 16 x 8 packed outputs per
 // thread reached 57.6 (242 registers, two CTAs per SM); K steps 8 and 32, four
@@ -323,13 +337,25 @@ struct F2Shared {
 // alpha and beta), TA: A stored [K, M] -- its tile is already k-major and goes
 // to shared memory by cp.async; TB: B stored [N, K] -- its tile passes through
 // registers to be transposed into the swizzled layout.
-template <bool EX, bool TA, bool TB>
+// MODE 0: every tile of the problem.  A plain problem whose last round of
+// resident CTAs would be part full runs as two grids: MODE 1 the whole tiles
+// before tile_base, MODE 2 the rest on clusters of two CTAs, the first taking
+// the first half of the K blocks and the second the rest; the halves' FP32
+// sums are exchanged through distributed shared memory and added.
+template <bool EX, bool TA, bool TB, int MODE = 0>
 __global__ void __launch_bounds__(THREADS, 2)
 simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ C, int M,
-                  int N, int K, SimtEx ex)
+                  int N, int K, SimtEx ex, int tile_base)
 {
     static_assert(EX || (!TA && !TB), "transposed operands need the general form");
-    pdl_wait();  // no early trigger of dependents: see launch_ffma2
+    static_assert(MODE == 0 || (!EX && !TA && !TB), "split launches are plain problems");
+    // MODE 0 and 1 wait for the previous kernel on the stream; MODE 1 then lets
+    // its dependent (the MODE 2 tail) launch, so the tail's CTAs take the slots
+    // this grid frees.  The tail reads only A and B (complete once every MODE 1
+    // CTA has passed its wait) and waits for MODE 1 before it exits, so that
+    // the next kernel on the stream sees both grids' tiles of C.
+    if constexpr (MODE != 2) pdl_wait();
+    if constexpr (MODE == 1) pdl_launch_dependents();
     extern __shared__ __align__(16) uint8_t f2_smem[];
     F2Shared &sm = *reinterpret_cast<F2Shared *>(f2_smem);
     constexpr int QA = G_BK / 4;                     // quads of k per A row ([M,K] storage)
@@ -351,7 +377,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     const int tiles_m = (M + G_BM - 1) / G_BM, tiles_n = (N + G_BN - 1) / G_BN;
     int tm, tn;
     {
-        const int pid = (int)blockIdx.x;
+        const int pid = MODE == 2 ? tile_base + (int)(blockIdx.x >> 1) : (int)blockIdx.x;
         const int per_group = GROUP_M * tiles_n;
         const int group = pid / per_group;
         const int first_m = group * GROUP_M;
@@ -362,6 +388,10 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     }
     const int m0 = tm * G_BM, n0 = tn * G_BN;
     const int ktiles = (K + G_BK - 1) / G_BK;
+    // K blocks [kt0, kt0 + kcount) of the tile: all of them, or one half (MODE 2)
+    const int khalf = MODE == 2 ? (int)(blockIdx.x & 1) : 0;
+    const int kt0 = khalf ? ktiles / 2 : 0;
+    const int kcount = MODE == 2 ? (khalf ? ktiles - ktiles / 2 : ktiles / 2) : ktiles;
 
     auto cp16 = [&](float *dst, const float *src, bool in) {
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
@@ -377,7 +407,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             for (int i = 0; i < LA; ++i) {
                 const int idx = tid + i * THREADS;
                 const int row = idx / QA, kq = (idx % QA) * 4;
-                const int gm = m0 + row, gk = t * G_BK + kq;
+                const int gm = m0 + row, gk = (kt0 + t) * G_BK + kq;
                 ra[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (gm < M && gk < K) ra[i] = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gm * lda + gk));
             }
@@ -403,7 +433,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             for (int i = 0; i < LA; ++i) {
                 const int idx = tid + i * THREADS;
                 const int kr = idx >> 5, mq = (idx & 31) * 4;
-                const int gk = t * G_BK + kr, gm = m0 + mq;
+                const int gk = (kt0 + t) * G_BK + kr, gm = m0 + mq;
                 cp16(&sm.As[stage][kr][a_col(kr, mq)], A + (size_t)gk * lda + gm, gk < K && gm < M);
             }
         }
@@ -415,7 +445,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             for (int i = 0; i < LB; ++i) {
                 const int idx = tid + i * THREADS;
                 const int kr = idx / QB, nq = (idx % QB) * 4;
-                const int gk = t * G_BK + kr, gn = n0 + nq;
+                const int gk = (kt0 + t) * G_BK + kr, gn = n0 + nq;
                 cp16(&sm.Bs[stage][kr][nq], B + (size_t)gk * ldb + gn, gk < K && gn < N);
             }
         }
@@ -428,7 +458,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             for (int i = 0; i < LB; ++i) {
                 const int idx = tid + i * THREADS;
                 const int col = idx / QA, kq = (idx % QA) * 4;
-                const int gn = n0 + col, gk = t * G_BK + kq;
+                const int gn = n0 + col, gk = (kt0 + t) * G_BK + kq;
                 rb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (gn < N && gk < K) rb[i] = __ldg(reinterpret_cast<const float4 *>(B + (size_t)gn * ldb + gk));
             }
@@ -450,7 +480,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
 
 #pragma unroll
     for (int t = 0; t < G_STAGES - 1; ++t) {
-        if (t < ktiles) {
+        if (t < kcount) {
             copy_a(t, t);
             copy_b(t, t);
             load_a(t);
@@ -460,7 +490,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    if (G_STAGES - 1 < ktiles) {
+    if (G_STAGES - 1 < kcount) {
         load_a(G_STAGES - 1);
         load_b(G_STAGES - 1);
     }
@@ -474,18 +504,18 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     const int a_off = wm * 64 + lm * 4;  // rows a_off + {0..3} + {0, 32}
     const int b_off = wn * 32 + ln * 4;  // columns b_off + {0..3} + {0, 16}
 
-    for (int t = 0; t < ktiles; ++t) {
+    for (int t = 0; t < kcount; ++t) {
         const int stage = t % G_STAGES;
         asm volatile("cp.async.wait_group %0;" ::"n"(G_STAGES - 2) : "memory");
         __syncthreads();
         const int tr = t + G_STAGES - 1;
-        if (tr < ktiles) {
+        if (tr < kcount) {
             const int st = tr % G_STAGES;
             copy_a(tr, st);
             copy_b(tr, st);
             store_a(st);
             store_b(st);
-            if (tr + 1 < ktiles) {
+            if (tr + 1 < kcount) {
                 load_a(tr + 1);
                 load_b(tr + 1);
             }
@@ -515,6 +545,58 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 
     // row i: a_off + 32 (i >> 2) + (i & 3); column pair j: b_off + 16 (j >> 1) + 2 (j & 1).
+    if constexpr (MODE == 2) {
+        // Rows a_off + 32 q + {0..3} are stored by the CTA of rank q.  Each CTA
+        // puts the rows its partner stores into its own shared memory (row
+        // wm 32 + lm 4 + i of a 64-row buffer, stride 68 floats so that the
+        // lanes of a store phase hit distinct banks), then adds the partner's
+        // copy of its own rows.
+        constexpr int PLD = G_BN + 4;
+        static_assert(G_BM / 2 * PLD * 4 <= (int)sizeof(F2Shared), "partial tile fits the stage buffers");
+        cg::cluster_group cluster = cg::this_cluster();
+        const int q = khalf;  // cluster rank = blockIdx.x & 1
+        float *part = reinterpret_cast<float *>(f2_smem);
+        __syncthreads();  // every warp is done with the stage buffers
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // the partner's rows: group 1 - q (selected, not indexed, to keep acc in registers)
+                const float2 lo = q ? acc[i][2 * h] : acc[4 + i][2 * h];
+                const float2 hi = q ? acc[i][2 * h + 1] : acc[4 + i][2 * h + 1];
+                *reinterpret_cast<float4 *>(part + (wm * 32 + (a_off & 31) + i) * PLD + b_off + 16 * h) =
+                    make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+        cluster.sync();
+        const float *peer = cluster.map_shared_rank(part, q ^ 1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gm = m0 + a_off + 32 * q + i;
+            if (gm >= M) continue;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = b_off + 16 * h, gn = n0 + c;
+                const float4 o = *reinterpret_cast<const float4 *>(peer + (wm * 32 + (a_off & 31) + i) * PLD + c);
+                const float2 lo = q ? acc[4 + i][2 * h] : acc[i][2 * h];
+                const float2 hi = q ? acc[4 + i][2 * h + 1] : acc[i][2 * h + 1];
+                // q = 0 holds the first K half, q = 1 the second: the sum is the
+                // same either way round (IEEE addition commutes).
+                const float v[4] = {lo.x + o.x, lo.y + o.y, hi.x + o.z, hi.y + o.w};
+                float *dst = C + (size_t)gm * ldc + gn;
+                if (gn + 3 < N) {
+                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (gn + j < N) dst[j] = v[j];
+                }
+            }
+        }
+        cluster.sync();  // the partner's reads of this CTA's shared memory are done
+        pdl_wait();      // MODE 1 complete before this grid counts as complete
+        return;
+    }
     // The general form scales by alpha and, when beta != 0, adds beta * old C.
     const bool use_beta = EX && ex.beta != 0.0f;
 #pragma unroll
@@ -564,7 +646,41 @@ cudaError_t launch_ffma2(const float *A, const float *B, float *C, int M, int N,
     // 49 us with the trigger left to the CTAs' exit (51 us without PDL).
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)tiles, batches, 1), dim3(THREADS), smem, s, attr);
-    return cudaLaunchKernelEx(&cfg, simt_ffma2_kernel<EX, TA, TB>, A, B, C, M, N, K, ex);
+    return launch_counted(&cfg, simt_ffma2_kernel<EX, TA, TB>, A, B, C, M, N, K, ex, 0);
+}
+
+// Tiles of a plain problem to run as K halves: the part-full last round of
+// `slots` resident CTAs, when it is at most half full (its half-K CTAs then
+// fit one round), the problem fills at least one round and each half has at
+// least 16 K blocks.  0: one launch.
+long long ffma2_tail_tiles(long long tiles, int K, long long slots) {
+    if (!g_simt_split_tail || !g_pdl) return 0;
+    const long long rem = tiles % slots;
+    const int ktiles = (K + G_BK - 1) / G_BK;
+    if (tiles < slots || rem == 0 || 2 * rem > slots || ktiles < 32) return 0;
+    return rem;
+}
+
+// A plain problem as two grids: the whole tiles (which let the second grid
+// launch as soon as they are all resident), then the last `tail` tiles as
+// clusters of two half-K CTAs, which take the slots the first grid frees.
+cudaError_t launch_ffma2_split(const float *A, const float *B, float *C, int M, int N, int K, long long tiles,
+                               long long tail, cudaStream_t s) {
+    constexpr int smem = (int)sizeof(F2Shared);
+    const long long base = tiles - tail;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)base), dim3(THREADS), smem, s, attr);
+    cudaError_t e = launch_counted(&cfg, simt_ffma2_kernel<false, false, false, 1>, A, B, C, M, N, K,
+                                       SimtEx{}, (int)base);
+    if (e != cudaSuccess) return e;
+    cfg = pdl_config(dim3((unsigned)(2 * tail)), dim3(THREADS), smem, s, attr);
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = 2;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    cfg.numAttrs += 1;
+    return launch_counted(&cfg, simt_ffma2_kernel<false, false, false, 2>, A, B, C, M, N, K, SimtEx{},
+                              (int)base);
 }
 
 // Tile configuration of the SIMT kernel: K step and CTAs per SM.
@@ -583,10 +699,15 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     const TIn *B = static_cast<const TIn *>(p.B);
     TOut *C = static_cast<TOut *>(p.C);
     if constexpr (VEC && sizeof(TIn) == 4) {
-        if (g_simt_ffma2)
-            return launch_ffma2<false, false, false>(static_cast<const float *>(p.A),
-                                                     static_cast<const float *>(p.B), static_cast<float *>(p.C),
-                                                     p.M, p.N, p.K, SimtEx{}, 1, s);
+        if (g_simt_ffma2) {
+            const float *fA = static_cast<const float *>(p.A), *fB = static_cast<const float *>(p.B);
+            float *fC = static_cast<float *>(p.C);
+            // three packed-FMA CTAs are resident per SM
+            const long long ftiles = (long long)((p.M + G_BM - 1) / G_BM) * ((p.N + G_BN - 1) / G_BN);
+            const long long tail = ffma2_tail_tiles(ftiles, p.K, 3LL * num_sms);
+            if (tail > 0) return launch_ffma2_split(fA, fB, fC, p.M, p.N, p.K, ftiles, tail, s);
+            return launch_ffma2<false, false, false>(fA, fB, fC, p.M, p.N, p.K, SimtEx{}, 1, s);
+        }
     }
     // A problem too small to fill half of one round of resident CTAs runs as
     // half tiles: twice the CTAs, half the rows each.  (Splitting only the last
@@ -599,14 +720,14 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     if (whole > 0) {
         cudaLaunchAttribute attr[1];
         const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)whole), dim3(THREADS), 0, s, attr);
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 128>, A,
+        const cudaError_t e = launch_counted(&cfg, simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 128>, A,
                                                  B, C, p.M, p.N, p.K, 0, SimtEx{});
         if (e != cudaSuccess) return e;
     }
     if (split > 0) {
         cudaLaunchAttribute attr[1];
         const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(2 * split)), dim3(THREADS), 0, s, attr);
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 64>, A,
+        const cudaError_t e = launch_counted(&cfg, simt_gemm_kernel<TIn, TOut, VEC, SIMT_BK, SIMT_MINB, 64>, A,
                                                  B, C, p.M, p.N, p.K, (int)whole, SimtEx{});
         if (e != cudaSuccess) return e;
     }
@@ -632,7 +753,7 @@ cudaError_t launch_ex_typed(const ProblemEx &p, cudaStream_t s) {
         } else {
             cudaLaunchAttribute attr[1];
             const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)tiles, (unsigned)nb, 1), dim3(THREADS), 0, s, attr);
-            e = cudaLaunchKernelEx(&cfg, simt_gemm_kernel<TIn, TIn, VEC, SIMT_BK, SIMT_MINB, 128, true, TA, TB>, A, B,
+            e = launch_counted(&cfg, simt_gemm_kernel<TIn, TIn, VEC, SIMT_BK, SIMT_MINB, 128, true, TA, TB>, A, B,
                                    C, p.M, p.N, p.K, 0, ex);
         }
         if (e != cudaSuccess) return e;

@@ -1482,7 +1482,7 @@ cudaError_t launch_typed(const Problem &p, int num_sms, int *status, cudaStream_
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(A_CPASYNC ? THREADS + 128 : THREADS), SMEM_BYTES, s, attr);
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K,
+    return launch_counted(&cfg, kern, ta, tb, static_cast<const T *>(p.A), static_cast<T *>(p.C), p.M, p.N, p.K,
                               status, stall);
 }
 
@@ -1547,7 +1547,7 @@ cudaError_t launch_skinny_typed(const Problem &p, int cs, int num_sms, int *stat
     if (cs == 1) {
         cudaLaunchAttribute a1[1];
         const cudaLaunchConfig_t c1 = pdl_config(dim3((unsigned)tiles_n), dim3(THREADS), SK_SMEM_BYTES, s, a1);
-        return cudaLaunchKernelEx(&c1, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, 1, max_stages, status);
+        return launch_counted(&c1, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, 1, max_stages, status);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles_n * cs), 1, 1);
@@ -1562,7 +1562,7 @@ cudaError_t launch_skinny_typed(const Problem &p, int cs, int num_sms, int *stat
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, cs, max_stages, status);
+    return launch_counted(&cfg, kern, tx, tw, static_cast<T *>(p.C), p.M, p.N, p.K, cs, max_stages, status);
 }
 
 // 3-D tensor map of `batch` matrices of [outer, inner] 16-bit elements: row
@@ -1630,7 +1630,7 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>, ta, tb, tc, tb2, args);
+    return launch_counted(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>, ta, tb, tc, tb2, args);
 }
 
 // Whether T tiles of KB K-blocks on G clusters take a stream-K tail: the last
@@ -1675,7 +1675,7 @@ cudaError_t launch_pair_planned(const CUtensorMap &ta, const CUtensorMap &tb, co
                 cudaLaunchAttribute fa[1];
                 const cudaLaunchConfig_t fc =
                     pdl_config(dim3((unsigned)(2 * rem), (unsigned)(args.bn / 8), 1), dim3(128), 0, s, fa);
-                e = cudaLaunchKernelEx(&fc, pair_sk_fixup_kernel<T, DUAL, F8>, static_cast<const PairArgs>(args),
+                e = launch_counted(&fc, pair_sk_fixup_kernel<T, DUAL, F8>, static_cast<const PairArgs>(args),
                                        (int)num_kb);
             }
             const cudaError_t f = cudaFreeAsync(buf, s);
@@ -1871,6 +1871,7 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
             if (cmax > 0 && cudaMallocAsync(&ap, (size_t)p.M * lda * 2, s) == cudaSuccess) {
                 const long long chunks = (long long)p.M * (p.K / 4);
                 const int grid = (int)std::min<long long>((chunks + 255) / 256, (long long)num_sms * 16);
+                note_launch();
                 pad_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint2 *>(p.A), static_cast<uint2 *>(ap),
                                                      p.M, p.K / 4, lda / 4);
                 e = cudaGetLastError();

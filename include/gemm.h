@@ -250,6 +250,12 @@ GEMM_API const char *gemm_status_string(gemm_status_t status);
  * string; for tests and benchmarks). */
 GEMM_API const char *gemm_last_kernel(void);
 
+/* Number of CUDA kernels this library has launched in this process, on every
+ * thread and device, since it was loaded (one count per launch call issued,
+ * whether or not the kernel has run yet).  The difference over a span of calls
+ * is the kernels those calls queued; for tests and benchmarks. */
+GEMM_API unsigned long long gemm_kernel_launches(void);
+
 /* Message of the last CUDA error seen by the calling thread ("" if none). */
 GEMM_API const char *gemm_last_error(void);
 

@@ -52,6 +52,16 @@ def test_library_is_built_for_sm_103a_only():
     assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
+def test_launch_counter_reads_without_a_gpu(built):
+    # calls rejected on the host launch nothing
+    n0 = g.gemm_kernel_launches()
+    assert isinstance(n0, int) and n0 >= 0
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.addressof(buf)
+    assert built.gemm_f32_rm(p, p + 1024, p + 2048, -1, 4, 4) == 1
+    assert g.gemm_kernel_launches() == n0
+
+
 def test_status_strings(built):
     for code, name in g.STATUS_NAMES.items():
         assert g.gemm_status_string(code) == name
