@@ -46,7 +46,11 @@
  * are launched as programmatic dependents: one may start its set-up while the
  * kernel before it on the stream drains, but it touches global memory only once
  * that kernel has completed, so stream order holds for any producer of A or B
- * and any consumer of C, the library's or not.  Calls may be captured into CUDA
+ * and any consumer of C, the library's or not.  (An FP32 call whose last round
+ * of tiles is at most half full launches two grids; the second reads A and B
+ * while the first still runs, and completes only after it.)  A call launches
+ * one to three kernels, or more for a general-form batch beyond 65535 matrices;
+ * gemm_kernel_launches() counts them.  Calls may be captured into CUDA
  * graphs.  Results are deterministic: the same inputs give bit-identical C on
  * every run (no atomics, fixed summation order per element).
  *
