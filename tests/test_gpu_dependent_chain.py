@@ -94,6 +94,7 @@ CHAINS = [
     ("bf16", 512, [1024, 2048, 520, 1024], "CTA pairs, ragged N then ragged K"),
     ("f32", 256, [512, 1024, 256, 768], "packed-FMA SIMT kernel"),
     ("f32", 4, [1024, 3000, 1024], "FP32 GEMV"),
+    ("f32", 2304, [1024, 1664, 2432], "packed-FMA SIMT kernel, last round split into half-K CTA pairs"),
 ]
 
 
@@ -109,9 +110,10 @@ def test_back_to_back_chain(case):
 
 def test_chain_captured_in_a_cuda_graph():
     """The same chains captured into one CUDA graph (stream-ordered scratch of the
-    stream-K tail becomes graph memory nodes) and replayed twice: the results
-    equal the eager ones bit for bit."""
-    cases = [CHAINS[0], CHAINS[2], CHAINS[4]]
+    stream-K tail becomes graph memory nodes; the SGEMM's split last round a
+    programmatic edge to a cluster launch) and replayed twice: the results equal
+    the eager ones bit for bit."""
+    cases = [CHAINS[0], CHAINS[2], CHAINS[4], CHAINS[6]]
     eager, staged = [], []
     for case in cases:
         dtype, M, dims, _ = case
