@@ -711,9 +711,11 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
     }
     // A problem too small to fill half of one round of resident CTAs runs as
     // half tiles: twice the CTAs, half the rows each.  (Splitting only the last
-    // round of a large problem into a second launch measured slower: a lone
-    // CTA already runs near the SM's full rate, and the second launch waits
-    // for the first to drain.)
+    // round of a large problem into half-height tiles in a second launch
+    // measured slower for this kernel: a lone CTA already runs near the SM's
+    // full rate, and the second launch waited for the first to drain.  The
+    // packed-FMA kernel's split above differs on both counts: half-K CTA pairs,
+    // launched while the first grid still runs.)
     const long long slots = (long long)num_sms * SIMT_MINB;
     const long long split = 2 * tiles <= slots ? tiles : 0;
     const long long whole = tiles - split;
