@@ -784,6 +784,49 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     return res
 
 
+def bench_line(res, workload, steps, warmup, world, ms_total, e2e_ms, paths):
+    """The JSON line of our arm from rank 0's measurement `res`, the slowest
+    rank's timed-region length `ms_total` and per-step end-to-end times `e2e_ms`
+    (slowest rank, keyed "e2e" / "e2e_serial"): whole-job figures over `world`
+    replicas."""
+    M, N, K = res["M"], res["N"], res["K"]
+    value = replica_throughput(res["flops_per_step"], steps, world, ms_total)
+    clk = res["clocks"] or {}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_total / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if res["variant"].startswith("f32") else res["variant"].split("_")[0],
+        "data": "synthetic",
+        "config": {"workload": workload, "M": M, "N": N, "K": K,
+                   "layout": "column-major" if res["variant"].endswith("_cm") else "row-major",
+                   "inputs": "uniform[-1,1] seeded SplitMix64" if "ffn" not in workload
+                   else "X~N(0,1), W~N(0,1/4096) seeded SplitMix64",
+                   "l2": res["l2"],
+                   "parallelism": f"replicas x{world}"},
+        "kernel": res["kernel"],
+        "roofline": res["roofline"],
+        # counted by the library over rank 0's timed steps; every replica runs the same calls
+        "gpu_launches": res["gpu_launches"] * world,
+        "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
+                   "reasons": clk.get("reasons", []), "samples": clk.get("samples", 0)},
+    }
+    for key in ("e2e", "e2e_serial"):
+        if key in res:
+            e = dict(res[key])
+            ms = e2e_ms.get(key, e["ms_per_step"])
+            e["value"] = replica_throughput(res["flops_per_step"], 1, world, ms)
+            e["ms_per_step"] = ms
+            line[key] = e
+    if "cpu_baseline" in res:
+        line["cpu_baseline"] = res["cpu_baseline"]
+    if res.get("cublas"):
+        line["cublas"] = res["cublas"]
+    if paths:
+        line["paths"] = paths
+    return line
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -818,6 +861,12 @@ def run_ours(args):
     ms_total = res["ms_total"]
     ms_total = slowest_rank_ms(ms_total, world, device="cuda")
 
+    # end to end, whole job: every rank's replica through its slowest rank's time
+    e2e_ms = {}
+    for key in ("e2e", "e2e_serial"):
+        if key in res:
+            e2e_ms[key] = slowest_rank_ms(res[key]["ms_per_step"], world, device="cuda")
+
     paths = []
     if not args.no_paths and rank == 0:
         for wl in args.paths:
@@ -830,38 +879,8 @@ def run_ours(args):
                           if k in r})
 
     if rank == 0:
-        M, N, K = res["M"], res["N"], res["K"]
-        value = replica_throughput(res["flops_per_step"], args.steps, world, ms_total)
-        clk = res["clocks"] or {}
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if res["variant"].startswith("f32") else res["variant"].split("_")[0],
-            "data": "synthetic",
-            "config": {"workload": args.workload, "M": M, "N": N, "K": K,
-                       "layout": "column-major" if res["variant"].endswith("_cm") else "row-major",
-                       "inputs": "uniform[-1,1] seeded SplitMix64" if "ffn" not in args.workload
-                       else "X~N(0,1), W~N(0,1/4096) seeded SplitMix64",
-                       "l2": res["l2"],
-                       "parallelism": f"replicas x{world}"},
-            "kernel": res["kernel"],
-            "roofline": res["roofline"],
-            # counted by the library over rank 0's timed steps; every replica runs the same calls
-            "gpu_launches": res["gpu_launches"] * world,
-            "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
-                       "reasons": clk.get("reasons", []), "samples": clk.get("samples", 0)},
-        }
-        if "e2e" in res:
-            line["e2e"] = res["e2e"]
-            line["e2e_serial"] = res["e2e_serial"]
-        if "cpu_baseline" in res:
-            line["cpu_baseline"] = res["cpu_baseline"]
-        if res.get("cublas"):
-            line["cublas"] = res["cublas"]
-        if paths:
-            line["paths"] = paths
-        print(json.dumps(line), flush=True)
+        print(json.dumps(bench_line(res, args.workload, args.steps, args.warmup, world, ms_total, e2e_ms, paths)),
+              flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

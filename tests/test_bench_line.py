@@ -1,0 +1,81 @@
+"""bench.py's JSON line (no GPU): the keys the benchmark contract asks for, and
+whole-job figures over replicas, from a measurement shaped like the one the
+GPU run produces."""
+
+import json
+
+import pytest
+
+import bench
+
+FLOPS = 2 * 4096 ** 3
+
+
+def fake_measurement():
+    return {
+        "workload": "sgemm_f32_rm_4096", "variant": "f32_rm", "M": 4096, "N": 4096, "K": 4096,
+        "kernel": "simt_f32_vec4", "flops_per_step": FLOPS, "ms_per_step": 2.12, "tflops": FLOPS / 2.12e-3 / 1e12,
+        "steps": 10, "ms_total": 21.2,
+        "roofline": {"bound": "alu", "achieved": 64.8, "peak": 80.55, "unit": "TFLOP/s", "frac": 64.8 / 80.55,
+                     "traffic": 403020032},
+        "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 12, "power_w_max": 900.0},
+        "footprint_bytes": 3 * 4096 * 4096 * 4, "gpu_launches": 20, "l2": "no flush: 192 MiB of operands > 129 MB L2",
+        "e2e": {"value": FLOPS / 2.17e-3 / 1e12, "unit": "TFLOP/s", "ms_per_step": 2.17, "steps": 10,
+                "overlap": "pipelined", "h2d_bytes_per_step": 134217728, "d2h_bytes_per_step": 67108864},
+        "e2e_serial": {"value": FLOPS / 3.12e-3 / 1e12, "unit": "TFLOP/s", "ms_per_step": 3.12, "steps": 10,
+                       "h2d_bytes_per_step": 134217728, "d2h_bytes_per_step": 67108864},
+        "cpu_baseline": {"value": 0.043, "unit": "TFLOP/s", "cores": 16, "kind": "oracle",
+                         "sample": "64 of 4096 output rows"},
+        "cublas": {"tflops": 66.8, "ms_per_step": 2.06, "mode": "FP32, CUBLAS_PEDANTIC_MATH"},
+    }
+
+
+def test_single_gpu_line_carries_every_contract_key():
+    res = fake_measurement()
+    line = bench.bench_line(res, "sgemm_f32_rm_4096", 10, 3, 1, 21.2, {}, [])
+    json.dumps(line)  # serialisable
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "gpu_launches", "clocks", "e2e",
+                "cpu_baseline"):
+        assert key in line, key
+    assert line["n_gpus"] == 1 and line["steps"] == 10 and line["warmup"] == 3
+    assert line["value"] == pytest.approx(FLOPS * 10 / 21.2e-3 / 1e12)
+    assert line["ms_per_step"] == pytest.approx(2.12)
+    assert line["higher_is_better"] is True and line["scaling"] == "weak" and line["vs_baseline"] is None
+    assert line["dtype"] == "f32" and line["data"] == "synthetic"
+    assert line["config"]["workload"] == "sgemm_f32_rm_4096" and "l2" in line["config"]
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in line["roofline"]
+    assert set(("sm_mhz", "sm_max_mhz", "reasons")) <= set(line["clocks"])
+    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+        assert key in line["e2e"]
+    assert line["e2e"]["value"] == pytest.approx(FLOPS / 2.17e-3 / 1e12)
+    assert line["e2e"]["unit"] == line["unit"]
+    assert line["gpu_launches"] == 20
+    for key in ("value", "unit", "cores", "kind", "sample"):
+        assert key in line["cpu_baseline"]
+
+
+def test_replicas_aggregate_over_ranks():
+    """Two replicas: FLOPs of both ranks over the slowest rank's time, the same
+    for the end-to-end figures; launches summed."""
+    res = fake_measurement()
+    line = bench.bench_line(res, "sgemm_f32_rm_4096", 10, 3, 2, 25.0, {"e2e": 2.5, "e2e_serial": 3.5}, [])
+    assert line["n_gpus"] == 2 and line["config"]["parallelism"] == "replicas x2"
+    assert line["value"] == pytest.approx(FLOPS * 10 * 2 / 25.0e-3 / 1e12)
+    assert line["e2e"]["value"] == pytest.approx(FLOPS * 2 / 2.5e-3 / 1e12)
+    assert line["e2e"]["ms_per_step"] == 2.5
+    assert line["e2e_serial"]["value"] == pytest.approx(FLOPS * 2 / 3.5e-3 / 1e12)
+    assert line["gpu_launches"] == 40
+    # the measurement itself is left as it was
+    assert res["e2e"]["ms_per_step"] == 2.17
+
+
+def test_half_precision_workloads_name_their_dtype_and_layout():
+    res = fake_measurement()
+    res.update(variant="f16_cm", workload="hgemm_f16_cm_8192")
+    for key in ("e2e", "e2e_serial", "cpu_baseline"):
+        res.pop(key)
+    line = bench.bench_line(res, "hgemm_f16_cm_8192", 10, 3, 1, 6.0, {}, [{"workload": "x"}])
+    assert line["dtype"] == "f16" and line["config"]["layout"] == "column-major"
+    assert "e2e" not in line and line["paths"] == [{"workload": "x"}]
