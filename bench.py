@@ -377,16 +377,17 @@ def host_inputs(variant, cfg, M, N, K, da, sa, db, sb):
 
 def oracle_rows(variant, A, B, M, N, K, rows, extra=()):
     """The oracle on output rows `rows` (for a batched workload: rows 0..len-1
-    of the first batch entry); returns the FLOPs that took."""
+    of the first batch entry).  Returns (the FLOPs that took, (C_ref, S) of
+    those rows for the three plain variants, else None)."""
     import oracle
     if variant == "bf16_silu_mul":
         oracle.silu_mul(A, B, extra[0], M, N, K, rows=rows)
-        return 4.0 * len(rows) * N * K
+        return 4.0 * len(rows) * N * K, None
     if variant == "e4m3_rowscale":  # quantise the rows, then their products
         a = np.ascontiguousarray(A.reshape(M, K)[rows])
         Q, S = oracle.quantize_rows_e4m3(a, len(rows), K)
         oracle.gemm_e4m3_rowscale(Q, S, B, len(rows), N, K)
-        return 2.0 * len(rows) * N * K
+        return 2.0 * len(rows) * N * K, None
     if variant.startswith("ex:"):
         dtype, layout, op_a, op_b, _ = ex_parse(variant)
         m = len(rows)
@@ -394,14 +395,23 @@ def oracle_rows(variant, A, B, M, N, K, rows, extra=()):
         ldb = K if op_b == "T" else N
         oracle.gemm_ex(dtype, layout, op_a, op_b, m, N, K, 1.0, A[:M * K], lda, 0, B[:K * N], ldb, 0, 0.0,
                        None, N, 0, 1)
-        return 2.0 * m * N * K
-    oracle.gemm_rows(variant, A, B, M, N, K, rows)
-    return 2.0 * len(rows) * N * K
+        return 2.0 * m * N * K, None
+    ref = oracle.gemm_rows(variant, A, B, M, N, K, rows)
+    return 2.0 * len(rows) * N * K, ref
+
+
+def sample_rows(M: int, n: int) -> np.ndarray:
+    """n distinct output rows spread evenly over 0..M-1, first and last included."""
+    n = max(1, min(int(n), M))
+    if n == 1:
+        return np.zeros(1, dtype=np.int64)
+    return (np.arange(n, dtype=np.int64) * (M - 1)) // (n - 1)
 
 
 def cpu_sample(variant, A, B, M, N, K, budget_s: float, extra=()):
-    """Times the oracle on a bounded sample of output rows of the same problem.
-    Returns (flop/s, rows, seconds, threads)."""
+    """Times the oracle on a bounded sample of output rows of the same problem,
+    spread over all of M.  Returns (flop/s, rows, seconds, threads, the rows,
+    their (C_ref, S) or None)."""
     import oracle
     threads = oracle.num_threads()
     # calibrate on one row per thread
@@ -412,11 +422,31 @@ def cpu_sample(variant, A, B, M, N, K, budget_s: float, extra=()):
     per_round = max(dt, 1e-6)
     rounds = max(1, int(budget_s / per_round))
     nrows = int(min(M, rows.size * rounds))
-    sel = np.arange(nrows, dtype=np.int64) % M
+    sel = sample_rows(M, nrows)
     t0 = time.perf_counter()
-    fl = oracle_rows(variant, A, B, M, N, K, sel, extra)
+    fl, ref = oracle_rows(variant, A, B, M, N, K, sel, extra)
     dt = time.perf_counter() - t0
-    return fl / dt, nrows, dt, threads
+    return fl / dt, nrows, dt, threads, sel, ref
+
+
+def sample_parity(variant, host_c, M, N, K, rows, ref):
+    """The library's C (host copy of the timed output buffer: float32, or half /
+    bf16 bits as int16) on the oracle's sampled rows, against the oracle within
+    the variant's tolerance."""
+    from oracle import compare
+    C_ref, S = ref
+    c = np.asarray(host_c)
+    if variant == "f32_rm":
+        got = c.astype(np.float64).reshape(M, N)[rows]
+    elif variant == "bf16_rm":
+        got = (c.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(M, N)[rows]
+    elif variant == "f16_cm":  # column-major: element (i, j) at i + j*M
+        got = c.view(np.float16).astype(np.float64).reshape(N, M).T[rows]
+    else:
+        raise ValueError(variant)
+    r = compare.check(variant, got, C_ref, S, K)
+    return {"rows": int(len(rows)), "elements": int(got.size), "ok": bool(r["ok"]),
+            "max_err_over_tol": float(r["max_err_over_tol"])}
 
 
 def e2e_pipelined(fn, h_in, d_in, dC, hC, M, N, K, stream, steps, flops):
@@ -775,10 +805,16 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
         res["e2e_serial"] = serial
 
     if cpu_budget > 0:
-        fps, nrows, dt, threads = cpu_sample(variant, A, B, M, N, K, cpu_budget, extra)
+        fps, nrows, dt, threads, sel, ref = cpu_sample(variant, A, B, M, N, K, cpu_budget, extra)
         res["cpu_baseline"] = {"value": fps / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                               "sample": f"{nrows} of {M} output rows ({nrows}x{N}x{K} FMAs, FP64 oracle) "
-                                         f"in {dt:.1f} s"}
+                               "sample": f"{nrows} of {M} output rows spread over M ({nrows}x{N}x{K} FMAs, "
+                                         f"FP64 oracle) in {dt:.1f} s"}
+        if ref is not None:
+            # the same rows of the timed output buffer, against the oracle
+            try:
+                res["cpu_baseline"]["parity"] = sample_parity(variant, dC.cpu().numpy(), M, N, K, sel, ref)
+            except Exception as exc:  # the line is still printed; the failure is named in it
+                res["cpu_baseline"]["parity"] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
     del dA, dB, dC, keep
     torch.cuda.empty_cache()
     return res
@@ -909,7 +945,7 @@ def run_reference(args):
     t0 = time.perf_counter()
     flops = 0.0
     for _ in range(args.steps):
-        flops += oracle_rows(variant, A, B, M, N, K, sel, extra)
+        flops += oracle_rows(variant, A, B, M, N, K, sel, extra)[0]
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     sample = f"{nrows} of {M} output rows per step ({nrows}x{N}x{K} FMAs, FP64 oracle)"
