@@ -357,6 +357,40 @@ def time_device_flushed(fn, steps: int, warmup: int, stream):
     return sum(e0.elapsed_time(e1) for e0, e1 in evs)
 
 
+def spread_stats(times_ms):
+    """Median, 10th and 90th percentiles and coefficient of variation of
+    per-call times (ms); `noisy` when the variation exceeds 2 %."""
+    t = np.sort(np.asarray(times_ms, dtype=np.float64))
+    mean = float(t.mean())
+    cv = float(t.std() / mean) if mean > 0 else 0.0
+    return {"calls": int(t.size), "median_ms": float(np.median(t)), "p10_ms": float(np.percentile(t, 10)),
+            "p90_ms": float(np.percentile(t, 90)), "cv": cv, "noisy": cv > 0.02}
+
+
+def per_call_times(fn, calls: int, stream, flushed: bool):
+    """Each of `calls` calls between its own pair of CUDA events on `stream`
+    (after the L2 flush when `flushed`): ms per call.  A pass of its own after
+    the timed region, whose back-to-back calls overlap one another."""
+    import torch
+    global _FLUSH
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+    sink = None
+    if flushed:
+        if _FLUSH is None:
+            _FLUSH = (torch.ones(512 * 1024 * 1024 // 4, device="cuda"), torch.empty(1, device="cuda"))
+        buf, sink = _FLUSH
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        if sink is not None:
+            with torch.cuda.stream(stream):
+                torch.sum(buf, dim=0, out=sink)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
 def host_inputs(variant, cfg, M, N, K, da, sa, db, sb):
     """Seeded host buffers of a workload: (A, B, extra)."""
     if variant == "bf16_silu_mul":
@@ -760,6 +794,11 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
                f"no flush: {footprint / 2**20:.0f} MiB of operands > 129 MB L2"),
     }
 
+    try:
+        res["per_call"] = spread_stats(per_call_times(step, min(steps, 100), stream, flushed))
+    except Exception as exc:  # the line is still printed; the failure is named in it
+        res["per_call"] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
     if cublas and variant in ("f32_rm", "f16_cm", "bf16_rm"):
         res["cublas"] = cublas_column(variant, M, N, K, dA, dB, dC, stream, steps, flushed,
                                       [(p_[0], p_[1]) for p_ in plain_sets] if variant in ENTRY else None)
@@ -854,6 +893,8 @@ def bench_line(res, workload, steps, warmup, world, ms_total, e2e_ms, paths):
             e["value"] = replica_throughput(res["flops_per_step"], 1, world, ms)
             e["ms_per_step"] = ms
             line[key] = e
+    if "per_call" in res:
+        line["per_call"] = res["per_call"]
     if "cpu_baseline" in res:
         line["cpu_baseline"] = res["cpu_baseline"]
     if res.get("cublas"):
@@ -911,7 +952,8 @@ def run_ours(args):
             r = measure_workload(wl, max(5, args.path_steps), 3, peaks, peaks_src, sms, stream,
                                  sampler_uuid=uuid, e2e=False, cpu_budget=0.0, clocks=True, prop_mhz=prop_mhz)
             paths.append({k: r[k] for k in ("workload", "kernel", "M", "N", "K", "ms_per_step", "tflops",
-                                            "roofline", "clocks", "kernels", "cublas", "l2", "gpu_launches")
+                                            "roofline", "clocks", "kernels", "cublas", "l2", "gpu_launches",
+                                            "per_call")
                           if k in r})
 
     if rank == 0:

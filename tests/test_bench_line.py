@@ -79,3 +79,19 @@ def test_half_precision_workloads_name_their_dtype_and_layout():
     line = bench.bench_line(res, "hgemm_f16_cm_8192", 10, 3, 1, 6.0, {}, [{"workload": "x"}])
     assert line["dtype"] == "f16" and line["config"]["layout"] == "column-major"
     assert "e2e" not in line and line["paths"] == [{"workload": "x"}]
+
+
+def test_per_call_spread_statistics():
+    s = bench.spread_stats([1.0] * 9 + [1.1])
+    assert s["calls"] == 10 and s["median_ms"] == 1.0 and s["p10_ms"] == 1.0
+    assert s["p90_ms"] == pytest.approx(1.01)
+    assert s["cv"] == pytest.approx(0.03 / 1.01)  # population std 0.03 over mean 1.01
+    assert s["noisy"] is True
+    assert bench.spread_stats([2.0, 2.0, 2.0])["noisy"] is False
+
+
+def test_per_call_spread_reaches_the_line():
+    res = fake_measurement()
+    res["per_call"] = bench.spread_stats([2.1, 2.12, 2.11])
+    line = bench.bench_line(res, "sgemm_f32_rm_4096", 10, 3, 1, 21.2, {}, [])
+    assert line["per_call"]["calls"] == 3 and not line["per_call"]["noisy"]
