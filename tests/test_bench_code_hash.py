@@ -17,3 +17,29 @@ def test_comment_markers_inside_literals_are_code():
 
 def test_code_changes_change_the_hash():
     assert bench.code_text("x = 1;") != bench.code_text("x = 2;")
+
+
+def _profile_hashes():
+    """(kernel file, code hash) pairs the committed ncu summaries name."""
+    import os
+    import re
+    root = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles")
+    pairs = set()
+    for name in os.listdir(root):
+        if name.endswith(".md"):
+            text = open(os.path.join(root, name), encoding="utf-8").read()
+            pairs |= set(re.findall(r"([a-z_0-9]+\.cu) code sha256\s+([0-9a-f]{12})", text))
+    return pairs
+
+
+def test_traffic_figures_and_profiles_name_the_same_captures():
+    """Every traffic figure the bench reports comes from a capture that a
+    committed summary describes, and the summaries agree on each file's code."""
+    pairs = _profile_hashes()
+    by_file = {}
+    for f, h in pairs:
+        by_file.setdefault(f, set()).add(h)
+    assert all(len(hs) == 1 for hs in by_file.values()), by_file
+    named = {h for _, h in pairs}
+    for workload, t in bench.TRAFFIC.items():
+        assert t["source"] in named, workload
