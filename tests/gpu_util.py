@@ -8,6 +8,8 @@ import numpy as np
 import torch
 
 import dense_matrix_multiply_gb300 as g
+import oracle
+from oracle import compare
 
 ENTRY = {"f32_rm": "gemm_f32_rm", "f16_cm": "gemm_f16_cm", "bf16_rm": "gemm_bf16_rm"}
 
@@ -70,18 +72,49 @@ def run(variant: str, A: np.ndarray, B: np.ndarray, M: int, N: int, K: int, forc
     return widen(variant, dC, M, N), name, dC
 
 
-def sample_indices(M: int, N: int, n: int, seed: int = 0):
-    """Random (i, j) pairs plus the four corners and the last row/column edges."""
-    rng = np.random.default_rng(seed)
-    ii = list(rng.integers(0, M, size=n))
-    jj = list(rng.integers(0, N, size=n))
-    for i, j in [(0, 0), (0, N - 1), (M - 1, 0), (M - 1, N - 1)]:
-        ii.append(i)
-        jj.append(j)
-    for t in range(min(64, N)):
-        ii.append(M - 1)
-        jj.append(N - 1 - t)
-    for t in range(min(64, M)):
-        ii.append(M - 1 - t)
-        jj.append(N - 1)
-    return np.array(ii, dtype=np.int64), np.array(jj, dtype=np.int64)
+def kernel_view(variant, A, B, M, N, K):
+    """The row-major problem the kernels run: a column-major C = A·B is the
+    row-major C^T = B^T·A^T on the same buffers ("SGEMM measured and the three
+    ledgers", section 2).  Returns (row-major variant, A', B', M', N', transposed)."""
+    if variant.endswith("_cm"):
+        return variant.replace("_cm", "_rm"), B, A, N, M, True
+    return variant, A, B, M, N, False
+
+
+def band_rows(M, band=256):
+    """Two rows of every `band`-row band of the kernel's output, one in each half
+    (the two CTAs of a pair tile), moving through the 32-row quarters (epilogue
+    warps) from band to band; plus the last row."""
+    rows = set()
+    for b in range((M + band - 1) // band):
+        for h in range(2):
+            r = b * band + h * (band // 2) + ((b + h) % 4) * 32 + (7 * b + 3 * h) % 32
+            if r < M:
+                rows.add(r)
+    rows.add(M - 1)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def band_cols(N, band=256):
+    """One column of every `band`-column band, at a varying offset; plus the last."""
+    cols = {min(N - 1, b * band + (67 * b + 13) % band) for b in range((N + band - 1) // band)}
+    cols.add(N - 1)
+    return np.array(sorted(cols), dtype=np.int64)
+
+
+def check_bands(variant, C, A, B, M, N, K):
+    """C (float64, logical [M, N]) against the oracle on whole rows -- two from
+    every 256-row band of the kernel's output -- and whole columns -- one from
+    every 256-column band.  Returns (rows result, columns result) of
+    compare.check."""
+    kv, kA, kB, kM, kN, tr = kernel_view(variant, A, B, M, N, K)
+    Ck = C.T if tr else C  # the kernel's [kM, kN] output
+    rows = band_rows(kM)
+    R_ref, R_S = oracle.gemm_rows(kv, kA, kB, kM, kN, K, rows)
+    res_r = compare.check(kv, Ck[rows], R_ref, R_S, K)
+    cols = band_cols(kN)
+    ii = np.repeat(np.arange(kM, dtype=np.int64), cols.size)
+    jj = np.tile(cols, kM)
+    E_ref, E_S = oracle.gemm_entries(kv, kA, kB, kM, kN, K, ii, jj)
+    res_c = compare.check(kv, Ck[ii, jj], E_ref, E_S, K)
+    return res_r, res_c
