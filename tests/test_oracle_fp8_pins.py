@@ -152,3 +152,37 @@ def test_e4m3_tolerance_admits_rounding_and_rejects_a_step():
     assert compare.check_e4m3(exact, C_ref, S)["ok"]
     moved = C_ref + 4 * compare.ulp_out("f16", C_ref) + 1e-4 * S
     assert not compare.check_e4m3(moved, C_ref, S)["ok"]
+
+
+def test_e4m3_tolerance_is_half_an_ulp_without_cancellation():
+    """Positive codes at K = 4096: nothing cancels (S = |C|), so the FP32
+    allowance is ~1e-5 of |C| and the tolerance is about half an ulp.  The
+    exactly rounded value passes; a result one or two half-precision steps away
+    from it fails."""
+    from oracle import compare
+    import synthetic
+    M, N, K = 8, 16, 4096
+    Q = synthetic.e4m3_codes(M, K, 31, 4, 10) & np.uint8(0x7F)   # clear the sign bits
+    W = synthetic.e4m3_codes(N, K, 32, 4, 10) & np.uint8(0x7F)
+    scale = np.full(M, 2.0 ** -12, dtype=np.float32)
+    C_ref, S = oracle.gemm_e4m3_rowscale(Q, scale, W, M, N, K)
+    assert np.array_equal(S, C_ref)
+    exact = C_ref.astype(np.float16).astype(np.float64)
+    assert compare.check_e4m3(exact, C_ref, S)["ok"]
+    step = compare.ulp_out("f16", exact)
+    for n_steps in (1, 2):
+        for sign in (1.0, -1.0):
+            assert not compare.check_e4m3(exact + sign * n_steps * step, C_ref, S)["ok"], (n_steps, sign)
+    tol = compare.tol_e4m3(C_ref, S)
+    assert np.all(tol < compare.ulp_out("f16", C_ref))
+
+
+def test_e4m3_tolerance_half_ulp_taken_in_the_wider_binade():
+    """A sum just below a power of two whose FP32 value may cross it is allowed
+    half an ulp of the wider binade (where the rounding then happens)."""
+    from oracle import compare
+    C_ref = np.array([2048.0 - 2.0 ** -6])
+    S = np.array([2048.0])
+    tol = compare.tol_e4m3(C_ref, S)
+    d = 1e-5 * 2048.0 + 2.0 ** -23 * C_ref[0]
+    assert tol[0] == d + 0.5 * 2.0  # half of the ulp 2.0 of [2048, 4096)
