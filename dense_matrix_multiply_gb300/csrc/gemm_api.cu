@@ -25,10 +25,9 @@ thread_local const char *t_last_kernel = "none";
 thread_local char t_last_error[256] = "";
 thread_local Family t_force = Family::Auto;
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
     std::once_flag once;
+    std::atomic<bool> ready{false};  // set once the status word exists
     bool supported = false;
     int num_sms = 0;
     int *status = nullptr;  // device word the tensor-core kernel reports timeouts in
@@ -106,6 +105,7 @@ gemm_status_t device_info(DeviceInfo **out) {
         err = cudaMalloc(&d.status, sizeof(int));
         if (err == cudaSuccess) err = cudaMemset(d.status, 0, sizeof(int));
         if (err != cudaSuccess) d.init_error = err;
+        else d.ready.store(true, std::memory_order_release);
     });
     if (d.init_error != cudaSuccess) { record_cuda_error(d.init_error); return GEMM_ERR_CUDA; }
     if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
@@ -430,6 +430,8 @@ GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B
         return finish(zero_fill(C, c_bytes, dev->num_sms, s), "zero_fill");
     }
     Problem p{A, B, C, M, N, K, Elt::BF16};
+    const bool stall = t_force == Family::UmmaStall;
+    if (stall && !umma_supported(p)) return GEMM_ERR_INVALID_VALUE;
     if (!umma_supported(p)) {
         record_message("gemm_bf16_rm_noalloc: needs B and C 16-byte aligned with N % 8 == 0, and A 16-byte "
                        "aligned with K % 8 == 0 or 8-byte aligned with K % 4 == 0");
@@ -439,6 +441,7 @@ GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B
         record_message("gemm_bf16_rm_noalloc: problem needs more scratch than the static array holds");
         return GEMM_ERR_INVALID_VALUE;
     }
+    if (stall) return finish(launch_umma_noalloc(p, dev->num_sms, s, true), "umma_stall");
     return finish(launch_umma_noalloc(p, dev->num_sms, s), "umma_bf16_noalloc");
 }
 
@@ -524,18 +527,27 @@ GEMM_API void *gemm_get_stream(void) { return t_stream; }
 GEMM_API gemm_status_t gemm_synchronize(void) {
     cudaError_t e = cudaStreamSynchronize(t_stream);
     if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
-    DeviceInfo *dev = nullptr;
-    gemm_status_t st = device_info(&dev);
-    if (st != GEMM_OK) return st;
-    int code = 0;
-    e = cudaMemcpy(&code, dev->status, sizeof(int), cudaMemcpyDeviceToHost);
+    int dev = 0;
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
-    if (code != 0) {
-        e = cudaMemset(dev->status, 0, sizeof(int));
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    // The status words that exist on this device: the allocating entry points'
+    // (once one of them has run here) and the allocation-free entry point's
+    // (once it has run here).  Reading them allocates nothing.
+    int code = 0;
+    DeviceInfo &d = g_devices[dev];
+    if (d.ready.load(std::memory_order_acquire)) {
+        e = cudaMemcpy(&code, d.status, sizeof(int), cudaMemcpyDeviceToHost);
         if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
-        return GEMM_ERR_TIMEOUT;
+        if (code != 0) {
+            e = cudaMemset(d.status, 0, sizeof(int));
+            if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
+        }
     }
-    return GEMM_OK;
+    int code_na = 0;
+    e = take_noalloc_status(dev, &code_na);
+    if (e != cudaSuccess) { record_cuda_error(e); return GEMM_ERR_CUDA; }
+    return (code | code_na) != 0 ? GEMM_ERR_TIMEOUT : GEMM_OK;
 }
 
 GEMM_API const char *gemm_status_string(gemm_status_t s) {

@@ -66,6 +66,9 @@ __device__ __forceinline__ void pdl_wait() {
 }
 #endif
 
+// Per-device tables of the library hold this many devices (ordinals 0 .. 63).
+constexpr int kMaxDevices = 64;
+
 enum class Elt { F32, F16, BF16 };
 
 struct Problem {
@@ -154,9 +157,14 @@ bool umma_silu_mul_supported(const Problem &p, const void *w_u);
 cudaError_t launch_umma_silu_mul(const Problem &p, const void *w_u, int *status, cudaStream_t s);
 
 // Allocation-free variant of launch_umma: the status word lives in a static
-// device array of kNoallocScratchBytes bytes (see umma_gemm.cu).
+// device array of kNoallocScratchBytes bytes (see umma_gemm.cu).  stall: the
+// bounded-wait test kernel instead (as launch_umma_stall_test).
 constexpr size_t kNoallocScratchBytes = 256;
 size_t umma_noalloc_scratch_need(const Problem &p);
-cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s);
+cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s, bool stall = false);
+// Reads the allocation-free entry point's status word on device `dev` into
+// *code and clears it; *code = 0 if that entry point was never set up there.
+// Synchronous; allocates nothing.
+cudaError_t take_noalloc_status(int dev, int *code);
 
 }  // namespace gemm_gb300

@@ -1931,36 +1931,53 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
 // memory the library cudaMallocs on first use of a device; this variant keeps
 // it in the file-scope array below instead, so it never allocates.  Every GPU
 // that loads the library holds these kNoallocScratchBytes until the process
-// exits.  All calls share the array: the word is cleared on the caller's
-// stream before each launch, and calls that overlap on the GPU race on it.
+// exits.  The word is zeroed once, at set-up; a timeout ORs a code into it,
+// and it stays set until gemm_synchronize reads and clears it (so a timeout
+// is reported even when further calls were queued after it).  All calls share
+// the array: calls that overlap on the GPU share the word, and a timeout of
+// either is reported to whichever thread synchronises first.
 static __device__ __align__(256) int g_noalloc_scratch[kNoallocScratchBytes / sizeof(int)];
 
 namespace {
 struct NoallocScratch {
     std::once_flag once;
+    std::atomic<bool> ready{false};
     int *ptr = nullptr;  // device address of g_noalloc_scratch on this device
     cudaError_t err = cudaSuccess;
 };
-NoallocScratch g_noalloc[64];
+NoallocScratch g_noalloc[kMaxDevices];
 }  // namespace
 
 size_t umma_noalloc_scratch_need(const Problem &) { return sizeof(int); }
 
-cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s) {
+cudaError_t launch_umma_noalloc(const Problem &p, int num_sms, cudaStream_t s, bool stall) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     NoallocScratch &d = g_noalloc[dev];
     // Set-up, once per device, with that device current: in host code the
     // array's name is only a host-side stand-in, so its device address is
-    // looked up here and passed to the kernel.
-    std::call_once(d.once, [&] { d.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.ptr), g_noalloc_scratch); });
+    // looked up here and passed to the kernel; the status word is zeroed.
+    std::call_once(d.once, [&] {
+        d.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.ptr), g_noalloc_scratch);
+        if (d.err == cudaSuccess) d.err = cudaMemset(d.ptr, 0, sizeof(int));
+        if (d.err == cudaSuccess) d.ready.store(true, std::memory_order_release);
+    });
     if (d.err != cudaSuccess) return d.err;
     if (umma_noalloc_scratch_need(p) > kNoallocScratchBytes) return cudaErrorInvalidValue;
-    e = cudaMemsetAsync(d.ptr, 0, sizeof(int), s);  // the status word starts at zero
-    if (e != cudaSuccess) return e;
+    if (stall) return launch_umma_stall_test(p, num_sms, d.ptr, s);
     return launch_umma(p, num_sms, d.ptr, s, /*may_allocate=*/false);
+}
+
+cudaError_t take_noalloc_status(int dev, int *code) {
+    *code = 0;
+    if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+    NoallocScratch &d = g_noalloc[dev];
+    if (!d.ready.load(std::memory_order_acquire)) return cudaSuccess;
+    cudaError_t e = cudaMemcpy(code, d.ptr, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && *code != 0) e = cudaMemset(d.ptr, 0, sizeof(int));
+    return e;
 }
 
 bool umma_silu_mul_supported(const Problem &p, const void *w_u) {

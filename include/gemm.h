@@ -142,13 +142,15 @@ GEMM_API gemm_status_t gemm_bf16_rm_silu_mul(const uint16_t *X, const uint16_t *
  * GEMM_ERR_INVALID_VALUE.  No call makes cudaMalloc, cudaFree or any other
  * allocating call.
  *
- * The first call on a device looks up the array's device address (set-up, once
- * per device, with that device current); make that first call before any
- * stream capture.  Every call clears the status word on the caller's stream
- * before its kernel runs; all calls share the array, so calls that overlap on
- * the GPU race on it.  A timeout recorded there is not reported by
- * gemm_synchronize, which reads only the status word of the allocating entry
- * points. */
+ * The first call on a device does the set-up, once per device, with that device
+ * current: it looks up the array's device address and zeroes the status word
+ * (a synchronous cudaMemset, which allocates nothing); make that first call
+ * before any stream capture.  A pipeline timeout sets the word, which stays set
+ * until gemm_synchronize reads and clears it: gemm_synchronize returns
+ * GEMM_ERR_TIMEOUT for it, as for the other entry points, and allocates nothing
+ * itself.  All calls share the array, so calls that overlap on the GPU race on
+ * it: a timeout of either is reported to whichever thread synchronises
+ * first. */
 GEMM_API gemm_status_t gemm_bf16_rm_noalloc(const uint16_t *A, const uint16_t *B, uint16_t *C,
                                             int M, int N, int K);
 
@@ -243,7 +245,9 @@ GEMM_API void *gemm_get_stream(void);
 
 /* Waits for the calling thread's stream; returns GEMM_ERR_CUDA for an
  * asynchronous CUDA error and GEMM_ERR_TIMEOUT if a kernel of this library
- * recorded a pipeline timeout on the current device (the record is cleared). */
+ * recorded a pipeline timeout on the current device (the record is cleared).
+ * It reads only status words that calls on this device have already set up,
+ * so it allocates nothing. */
 GEMM_API gemm_status_t gemm_synchronize(void);
 
 /* Static, human-readable name of a status code. */
@@ -271,7 +275,9 @@ GEMM_API const char *gemm_last_error(void);
  * "umma_stall" tests the tensor-core kernel's bounded waits: a 16-bit call whose
  * A, B and C suit the TMA kernel launches it with a producer that issues no
  * loads, every CTA gives up after about two seconds, C is left unwritten and
- * the next gemm_synchronize returns GEMM_ERR_TIMEOUT. */
+ * the next gemm_synchronize returns GEMM_ERR_TIMEOUT.  gemm_bf16_rm_noalloc
+ * honours "umma_stall" (recording in its static status word) and ignores the
+ * other families. */
 GEMM_API gemm_status_t gemm_force_kernel(const char *family);
 
 #ifdef __cplusplus

@@ -1,11 +1,20 @@
 """The allocation-free bf16 entry point, through the C ABI.
 
-It serves callers that cannot call cudaMalloc -- applications whose device
-memory is owned by their own allocator, or latency-critical paths that cannot
-afford cudaMalloc's implicit synchronisation.  Its result must match the
-regular allocating entry point gemm_bf16_rm within the tolerance the parity
-tests use, on two calls in a row (the second reuses the static scratch the
-first one left behind).  This file is collected last on purpose.
+gemm_bf16_rm_noalloc serves callers that cannot call cudaMalloc: programs
+whose device memory is owned by their own allocator (a framework's caching
+pool that has already reserved the GPU, an embedding program with a fixed
+memory budget) and latency-critical paths that cannot take cudaMalloc's
+implicit synchronisation.  Its scratch -- the kernel's 4-byte timeout status
+word -- lives in a static device array instead.
+
+Each case runs it twice in a row (the second call finds the static array as the
+first one left it) and checks every call against the CPU oracle with the
+parity tests' bf16 tolerance, and against the regular entry point
+gemm_bf16_rm within the same tolerance.  The library's own launch count must be
+exactly one kernel per call: the regular entry point's allocating branches (A
+staged into aligned rows, the stream-K tail with its fix-up kernel) each add a
+kernel, so a call that took one of them would show.  This file is collected
+last on purpose.
 """
 
 import ctypes
@@ -14,8 +23,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synthetic
 from oracle import compare
+
+from gpu_util import check_bands
 
 import dense_matrix_multiply_gb300 as g
 
@@ -27,10 +39,23 @@ def _bits_to_f64(t: torch.Tensor) -> np.ndarray:
     return (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("shape", [(1024, 12288, 4096), (1000, 1000, 1000), (300, 520, 264), (256, 512, 100),
-                                   (1024, 2048, 1028), (32, 4096, 4096)])
-def test_noalloc_matches_allocating_entry_point(lib, shape):
-    M, N, K = shape
+# (M, N, K, what gemm_bf16_rm does differently for this shape)
+SHAPES = [
+    (1000, 1000, 1000, "same kernel"),
+    (300, 520, 264, "same kernel"),
+    (256, 512, 100, "same kernel"),
+    (32, 4096, 4096, "skinny kernel"),
+    (1024, 2048, 1028, "stages A into aligned rows (K % 8 = 4)"),
+    (1024, 12288, 4096, "same kernel (the FFN projection)"),
+    (3072, 5120, 6144, "adds a stream-K tail and its fix-up kernel"),
+    (8192, 4096, 4100, "stages A into aligned rows"),
+]
+FULL_ORACLE_FMAS = 3e9  # above this, whole rows and columns from every tile band
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"{s[0]}x{s[1]}x{s[2]}")
+def test_noalloc_matches_oracle_and_allocating_entry_point(lib, shape):
+    M, N, K, _ = shape
     clib = g.load()
     A, B = synthetic.problem_inputs("bf16_rm", M, N, K, 3, "normal", 1.0, "normal", 1.0 / 64.0)
     dA = torch.from_numpy(A.view(np.int16)).cuda()
@@ -39,24 +64,65 @@ def test_noalloc_matches_allocating_entry_point(lib, shape):
     out = torch.full((M * N,), -1, dtype=torch.int16, device="cuda")
     clib.gemm_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
+    # the regular (allocating) entry point on the same inputs
     assert clib.gemm_bf16_rm(dA.data_ptr(), dB.data_ptr(), ref.data_ptr(), M, N, K) == 0
-    torch.cuda.synchronize()
-    want = _bits_to_f64(ref)
-    tol = compare.tol_half(want, K, "bf16")
+    assert clib.gemm_synchronize() == 0
+    regular = _bits_to_f64(ref).reshape(M, N)
+
+    full = M * N * K <= FULL_ORACLE_FMAS
+    if full:
+        C_ref, S = oracle.gemm("bf16_rm", A, B, M, N, K)
 
     for call in range(2):
         out.fill_(-1)
         torch.cuda.synchronize()
         free_before = torch.cuda.mem_get_info()[0]
+        launches = clib.gemm_kernel_launches()
         st = clib.gemm_bf16_rm_noalloc(dA.data_ptr(), dB.data_ptr(), out.data_ptr(), M, N, K)
         assert st == 0, clib.gemm_last_error()
+        assert clib.gemm_kernel_launches() - launches == 1, "a kernel besides the GEMM was launched"
         assert clib.gemm_last_kernel() == b"umma_bf16_noalloc"
-        torch.cuda.synchronize()
+        assert clib.gemm_synchronize() == 0
         if call == 1:
             # the second call (set-up done) leaves device memory untouched
             assert torch.cuda.mem_get_info()[0] == free_before
-        got = _bits_to_f64(out)
-        assert np.all(np.abs(got - want) <= tol), f"call {call}: max err {np.max(np.abs(got - want))}"
+        got = _bits_to_f64(out).reshape(M, N)
+        if full:
+            res = compare.check("bf16_rm", got, C_ref, S, K)
+            assert res["ok"], (call, res)
+        else:
+            res_r, res_c = check_bands("bf16_rm", got, A, B, M, N, K)
+            assert res_r["ok"] and res_c["ok"], (call, res_r, res_c)
+        # against the regular entry point, within the same bf16 tolerance
+        tol = compare.tol_half(regular, K, "bf16")
+        err = np.abs(got - regular)
+        assert np.all(err <= tol), f"call {call}: max err vs gemm_bf16_rm {err.max()}"
+
+
+def test_noalloc_timeout_is_reported(lib):
+    """A call whose pipeline waits run out (the "umma_stall" test hook: a
+    producer that issues no loads) leaves its code in the static status word;
+    gemm_synchronize reports it once, and the next call is correct."""
+    clib = g.load()
+    M, N, K = 256, 256, 128
+    A, B = synthetic.problem_inputs("bf16_rm", M, N, K, 3)
+    dA = torch.from_numpy(A.view(np.int16)).cuda()
+    dB = torch.from_numpy(B.view(np.int16)).cuda()
+    out = torch.full((M * N,), -1, dtype=torch.int16, device="cuda")
+    clib.gemm_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert clib.gemm_force_kernel(b"umma_stall") == 0
+    try:
+        st = clib.gemm_bf16_rm_noalloc(dA.data_ptr(), dB.data_ptr(), out.data_ptr(), M, N, K)
+    finally:
+        clib.gemm_force_kernel(None)
+    assert st == 0 and clib.gemm_last_kernel() == b"umma_stall"
+    assert clib.gemm_synchronize() == 5  # GEMM_ERR_TIMEOUT
+    assert clib.gemm_synchronize() == 0  # reported once
+    st = clib.gemm_bf16_rm_noalloc(dA.data_ptr(), dB.data_ptr(), out.data_ptr(), M, N, K)
+    assert st == 0 and clib.gemm_synchronize() == 0
+    C_ref, S = oracle.gemm("bf16_rm", A, B, M, N, K)
+    res = compare.check("bf16_rm", _bits_to_f64(out).reshape(M, N), C_ref, S, K)
+    assert res["ok"], res
 
 
 def test_noalloc_rejects_what_the_tensor_core_kernel_cannot_run(lib):
