@@ -49,6 +49,26 @@ from dense_matrix_multiply_gb300 import metrics  # noqa: E402
 
 METRIC = "GEMM TFLOP/s (2·M·N·K/t) and % of FP32-SIMT or BF16/FP16 tensor peak"
 DEFAULT_WORKLOAD = "sgemm_f32_rm_4096"
+# The other workloads measured in the default run ("paths"): every other
+# configuration of the five (the FP16 and BF16 tensor-core problems and the
+# whole ragged/edge sweep on both the FP32 and the BF16 path, the K = 4100 tail
+# beside its K = 4096 control), then the fused, general-form and FP8 workloads.
+DEFAULT_PATHS = ["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144", "ffn_bf16_rm_1024x12288x4096",
+                 "sgemm_f32_rm_256",
+                 "edge_f32_rm_1000x1000x1000", "edge_bf16_rm_1000x1000x1000",
+                 "edge_bf16_rm_1x12288x4096", "edge_f32_rm_1x12288x4096", "edge_bf16_rm_32x12288x4096",
+                 "edge_f32_rm_64x64x64", "edge_bf16_rm_64x64x64",
+                 "edge_bf16_rm_8192x4096x4100", "edge_bf16_rm_8192x4096x4096",
+                 "edge_f32_rm_8192x4096x4100", "edge_f32_rm_8192x4096x4096",
+                 "ffn_gate_up_bf16_silu_mul_1024x12288x4096",
+                 "gemm_ex_bf16_rm_NT_8192x8192x8192", "gemm_ex_f16_rm_NN_batch32_1024x1024x1024",
+                 "gemm_ex_f32_rm_NT_4096x4096x4096", "fp8_rowscale_e4m3_4096x1536x4096"]
+# Problems the oracle is also timed on with one host thread (the small
+# configurations): whole problems up to ONE_THREAD_FULL_FMAS multiply-adds,
+# else a bounded sample of rows.
+ONE_THREAD_WORKLOADS = ["sgemm_f32_rm_256", "edge_f32_rm_1000x1000x1000", "edge_bf16_rm_1000x1000x1000",
+                        "edge_f32_rm_64x64x64", "edge_bf16_rm_64x64x64"]
+ONE_THREAD_FULL_FMAS = 1 << 26
 SMS_NOMINAL = 152
 FP32_LANES_PER_SM = 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
@@ -859,6 +879,74 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     return res
 
 
+def add_k4096_controls(paths):
+    """Beside each K = 4100 workload measured with its K = 4096 control (same M,
+    N and path), the control's time and throughput and the slowdown of the odd K:
+    throughput at K = 4096 over throughput at K = 4100 (> 1: the tail costs more
+    than its extra 0.1 % of FLOPs)."""
+    by_name = {p["workload"]: p for p in paths}
+    for p in paths:
+        name = p["workload"]
+        if not name.endswith("x4100"):
+            continue
+        ctrl = by_name.get(name[:-len("4100")] + "4096")
+        if ctrl is None:
+            continue
+        p["k4096_control"] = {"workload": ctrl["workload"], "ms_per_step": ctrl["ms_per_step"],
+                              "tflops": ctrl["tflops"], "kernel": ctrl["kernel"],
+                              "slowdown_vs_k4096": ctrl["tflops"] / p["tflops"]}
+
+
+def compact_paths(paths):
+    """One short record per path: kernel, microseconds per call, TFLOP/s, the
+    roofline fraction and its bound, DRAM traffic over the algorithmic bytes
+    (when captured), cuBLAS's TFLOP/s on the same inputs, and the K = 4096
+    control's slowdown for the K = 4100 rows."""
+    out = {}
+    for p in paths:
+        rf = p.get("roofline") or {}
+        rec = {"kernel": p["kernel"], "us": round(1e3 * p["ms_per_step"], 2), "tflops": round(p["tflops"], 2),
+               "frac": round(rf.get("frac", 0.0), 3), "bound": rf.get("bound")}
+        if rf.get("traffic") and rf.get("algorithmic_bytes"):
+            rec["traffic_x"] = round(rf["traffic"] / rf["algorithmic_bytes"], 2)
+        cb = p.get("cublas") or {}
+        if cb.get("tflops"):
+            rec["cublas_tflops"] = round(cb["tflops"], 2)
+        if "k4096_control" in p:
+            rec["slowdown_vs_k4096"] = round(p["k4096_control"]["slowdown_vs_k4096"], 3)
+        out[p["workload"]] = rec
+    return out
+
+
+def cpu_one_thread(names, budget_s: float):
+    """The oracle on one host thread for the small configurations: the whole
+    problem when it holds at most ONE_THREAD_FULL_FMAS multiply-adds, else rows
+    spread over M for about budget_s seconds.  TFLOP/s on the 2*M*N*K convention."""
+    import oracle
+    threads = oracle.num_threads()
+    out = {}
+    oracle.set_num_threads(1)
+    try:
+        for name in names:
+            cfg, (variant, M, N, K, da, sa, db, sb) = all_workloads()[name]
+            A, B, extra = host_inputs(variant, cfg, M, N, K, da, sa, db, sb)
+            if M * N * K <= ONE_THREAD_FULL_FMAS:
+                sel = np.arange(M, dtype=np.int64)
+            else:
+                t0 = time.perf_counter()
+                oracle_rows(variant, A, B, M, N, K, np.zeros(1, dtype=np.int64), extra)
+                per_row = max(time.perf_counter() - t0, 1e-6)
+                sel = sample_rows(M, max(1, int(budget_s / per_row)))
+            t0 = time.perf_counter()
+            fl, _ = oracle_rows(variant, A, B, M, N, K, sel, extra)
+            dt = time.perf_counter() - t0
+            out[name] = {"tflops": fl / dt / 1e12, "seconds": dt, "cores": 1,
+                         "sample": "whole problem" if sel.size == M else f"{sel.size} of {M} rows"}
+    finally:
+        oracle.set_num_threads(threads)
+    return out
+
+
 def bench_line(res, workload, steps, warmup, world, ms_total, e2e_ms, paths):
     """The JSON line of our arm from rank 0's measurement `res`, the slowest
     rank's timed-region length `ms_total` and per-step end-to-end times `e2e_ms`
@@ -900,7 +988,9 @@ def bench_line(res, workload, steps, warmup, world, ms_total, e2e_ms, paths):
     if res.get("cublas"):
         line["cublas"] = res["cublas"]
     if paths:
-        line["paths"] = paths
+        # the full records first, then a compact summary as the line's last key
+        line["paths_detail"] = paths
+        line["paths"] = compact_paths(paths)
     return line
 
 
@@ -955,10 +1045,17 @@ def run_ours(args):
                                             "roofline", "clocks", "kernels", "cublas", "l2", "gpu_launches",
                                             "per_call")
                           if k in r})
+        add_k4096_controls(paths)
+
+    one_thread = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        one_thread = cpu_one_thread(ONE_THREAD_WORKLOADS, args.one_thread_seconds)
 
     if rank == 0:
-        print(json.dumps(bench_line(res, args.workload, args.steps, args.warmup, world, ms_total, e2e_ms, paths)),
-              flush=True)
+        line = bench_line(res, args.workload, args.steps, args.warmup, world, ms_total, e2e_ms, paths)
+        if one_thread:
+            line["cpu_baseline"]["one_thread"] = one_thread
+        print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -1012,22 +1109,14 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
-    p.add_argument("--paths", nargs="*", default=["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144",
-                                                   "ffn_bf16_rm_1024x12288x4096", "edge_bf16_rm_1x12288x4096",
-                                                   "edge_f32_rm_1x12288x4096", "edge_bf16_rm_32x12288x4096",
-                                                   "edge_bf16_rm_8192x4096x4100",
-                                                   "edge_f32_rm_8192x4096x4100", "sgemm_f32_rm_256",
-                                                   "ffn_gate_up_bf16_silu_mul_1024x12288x4096",
-                                                   "gemm_ex_bf16_rm_NT_8192x8192x8192",
-                                                   "gemm_ex_f16_rm_NN_batch32_1024x1024x1024",
-                                                   "gemm_ex_f32_rm_NT_4096x4096x4096",
-                                                   "fp8_rowscale_e4m3_4096x1536x4096"])
+    p.add_argument("--paths", nargs="*", default=DEFAULT_PATHS)
     p.add_argument("--path-steps", type=int, default=50)
     p.add_argument("--no-paths", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--ref-seconds", type=float, default=60.0)
+    p.add_argument("--one-thread-seconds", type=float, default=2.0)
     args = p.parse_args(argv)
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps

@@ -77,6 +77,8 @@ def _load():
             lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
             lib.oracle_decode_bf16.restype = ctypes.c_double
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
@@ -299,3 +301,8 @@ def decode(dtype: str, bits) -> np.ndarray:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's later calls (its results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))

@@ -405,3 +405,14 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Number of OpenMP threads the oracle's later calls use (n >= 1); for timing the
+ * oracle on one core.  The results do not depend on it (see the loop order above). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -7,6 +7,7 @@ import json
 import pytest
 
 import bench
+import synthetic
 
 FLOPS = 2 * 4096 ** 3
 
@@ -76,9 +77,44 @@ def test_half_precision_workloads_name_their_dtype_and_layout():
     res.update(variant="f16_cm", workload="hgemm_f16_cm_8192")
     for key in ("e2e", "e2e_serial", "cpu_baseline"):
         res.pop(key)
-    line = bench.bench_line(res, "hgemm_f16_cm_8192", 10, 3, 1, 6.0, {}, [{"workload": "x"}])
+    path = {"workload": "x", "kernel": "umma_bf16", "ms_per_step": 0.5, "tflops": 100.0,
+            "roofline": {"frac": 0.5, "bound": "tensor", "traffic": None, "algorithmic_bytes": 10}}
+    line = bench.bench_line(res, "hgemm_f16_cm_8192", 10, 3, 1, 6.0, {}, [path])
     assert line["dtype"] == "f16" and line["config"]["layout"] == "column-major"
-    assert "e2e" not in line and line["paths"] == [{"workload": "x"}]
+    assert "e2e" not in line and line["paths_detail"] == [path]
+    assert line["paths"] == {"x": {"kernel": "umma_bf16", "us": 500.0, "tflops": 100.0, "frac": 0.5,
+                                   "bound": "tensor"}}
+    # the compact summary is the line's last key (the end of the output)
+    assert list(line)[-1] == "paths"
+
+
+def test_k4100_rows_carry_their_k4096_control():
+    def rec(name, ms, tf):
+        return {"workload": name, "kernel": "simt_f32_vec4", "ms_per_step": ms, "tflops": tf,
+                "roofline": {"frac": 0.8, "bound": "alu", "traffic": 300, "algorithmic_bytes": 150},
+                "cublas": {"tflops": 60.0}}
+    paths = [rec("edge_f32_rm_8192x4096x4100", 4.4, 62.5), rec("edge_f32_rm_8192x4096x4096", 4.2, 65.0),
+             rec("edge_bf16_rm_8192x4096x4100", 0.2, 1400.0)]
+    bench.add_k4096_controls(paths)
+    c = paths[0]["k4096_control"]
+    assert c["workload"] == "edge_f32_rm_8192x4096x4096" and c["slowdown_vs_k4096"] == pytest.approx(65.0 / 62.5)
+    assert "k4096_control" not in paths[1] and "k4096_control" not in paths[2]  # no bf16 control measured
+    compact = bench.compact_paths(paths)
+    assert compact["edge_f32_rm_8192x4096x4100"] == {
+        "kernel": "simt_f32_vec4", "us": 4400.0, "tflops": 62.5, "frac": 0.8, "bound": "alu", "traffic_x": 2.0,
+        "cublas_tflops": 60.0, "slowdown_vs_k4096": 1.04}
+
+
+def test_default_paths_cover_every_configuration_shape():
+    """Every workload of the five configurations is the headline or a path."""
+    names = set(bench.DEFAULT_PATHS) | {bench.DEFAULT_WORKLOAD}
+    for wl in synthetic.WORKLOADS:
+        assert wl in names
+    for (M, N, K) in synthetic.EDGE_SHAPES:
+        for v in ("f32_rm", "bf16_rm"):
+            if (M, N, K) == (32, 12288, 4096) and v == "f32_rm":
+                continue  # M = 32 decode: a 16-bit addition of this library's sweep
+            assert f"edge_{v}_{M}x{N}x{K}" in names
 
 
 def test_per_call_spread_statistics():
