@@ -18,7 +18,7 @@ std::atomic<unsigned long long> gemm_gb300::g_launches{0};
 
 namespace {
 
-enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma, UmmaStall };
+enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma, UmmaStall, UmmaStallPair, UmmaStallPeer };
 
 thread_local cudaStream_t t_stream = nullptr;
 thread_local const char *t_last_kernel = "none";
@@ -189,6 +189,13 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     case Family::UmmaStall:
         if (elt == Elt::F32) return GEMM_ERR_INVALID_VALUE;
         return finish(launch_umma_stall_test(p, dev->num_sms, dev->status, s), "umma_stall");
+    case Family::UmmaStallPair:
+    case Family::UmmaStallPeer: {
+        if (elt == Elt::F32 || M <= 128) return GEMM_ERR_INVALID_VALUE;
+        const bool peer = t_force == Family::UmmaStallPeer;
+        return finish(launch_umma_pair_stall_test(p, peer ? 2 : 1, dev->status, s),
+                      peer ? "umma_stall_peer" : "umma_stall_pair");
+    }
     case Family::Auto:
         break;
     }
@@ -517,6 +524,33 @@ GEMM_API gemm_status_t gemm_e4m3_rowscale(const uint8_t *Q, const float *scale, 
     return finish(e, "umma_e4m3_rowscale");
 }
 
+GEMM_API gemm_status_t gemm_e4m3_rowscale_fused(const uint16_t *A, const uint8_t *Wt, uint16_t *C, int M, int N,
+                                                int K) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) { t_last_kernel = "noop"; return GEMM_OK; }
+    if (!C || (K > 0 && (!A || !Wt))) return GEMM_ERR_INVALID_VALUE;
+    const size_t c_bytes = (size_t)M * N * 2;
+    if (overlaps(C, c_bytes, A, (size_t)M * K * 2) || overlaps(C, c_bytes, Wt, (size_t)N * K))
+        return GEMM_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    gemm_status_t st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = t_stream;
+    if (K == 0) {
+        return finish(zero_fill(C, c_bytes, dev->num_sms, s), "zero_fill");
+    }
+    if (!umma_e4m3_fused_supported(A, Wt, C, N, K)) {
+        record_message("gemm_e4m3_rowscale_fused: needs A, Wt, C 16-byte aligned, K % 16 == 0 and N % 8 == 0");
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    const cudaError_t e = launch_umma_e4m3_fused(A, Wt, C, M, N, K, dev->status, s);
+    if (e == cudaErrorNotSupported) {
+        record_message("gemm_e4m3_rowscale_fused: the tensor-core kernel cannot describe these operands");
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    return finish(e, "umma_e4m3_rowscale_fused");
+}
+
 GEMM_API gemm_status_t gemm_set_stream(void *cuda_stream) {
     t_stream = static_cast<cudaStream_t>(cuda_stream);
     return GEMM_OK;
@@ -576,6 +610,8 @@ GEMM_API gemm_status_t gemm_force_kernel(const char *family) {
     else if (!strcmp(family, "gemv_scalar")) t_force = Family::GemvScalar;
     else if (!strcmp(family, "umma")) t_force = Family::Umma;
     else if (!strcmp(family, "umma_stall")) t_force = Family::UmmaStall;
+    else if (!strcmp(family, "umma_stall_pair")) t_force = Family::UmmaStallPair;
+    else if (!strcmp(family, "umma_stall_peer")) t_force = Family::UmmaStallPeer;
     else return GEMM_ERR_INVALID_VALUE;
     return GEMM_OK;
 }

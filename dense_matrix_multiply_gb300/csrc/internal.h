@@ -145,10 +145,30 @@ bool umma_e4m3_supported(const void *Q, const void *Wt, const void *C, int N, in
 cudaError_t launch_umma_e4m3_rowscale(const void *Q, const float *scale, const void *Wt, void *C, int M, int N,
                                       int K, int *status, cudaStream_t s);
 
+// Row amax of a half [M,K] row-major matrix: amax[i] = max_k |a_ik| (see
+// quant_e4m3.cu).  M, K >= 1.
+cudaError_t launch_row_amax_f16(const void *A, float *amax, int M, int K, cudaStream_t s);
+
+// Row-scaled FP8 product with the quantisation fused into the load path: C
+// [M,N] half = diag(amax/448) E4M3(diag(448/amax) A) Wt^T, A [M,K] half, Wt
+// [N,K] E4M3, row-major.  A row amax pass first (its M floats in stream-ordered
+// scratch), then the CTA-pair kernel whose converter warps quantise A's tiles
+// as they load them.  Needs A, Wt, C 16-byte aligned, K % 16 == 0, N % 8 == 0;
+// returns cudaErrorNotSupported, before any launch, otherwise.
+bool umma_e4m3_fused_supported(const void *A, const void *Wt, const void *C, int N, int K);
+cudaError_t launch_umma_e4m3_fused(const void *A, const void *Wt, void *C, int M, int N, int K, int *status,
+                                   cudaStream_t s);
+
 // Test of the bounded pipeline waits: the single-CTA tensor-core kernel with a
 // producer that issues no load, so every CTA takes its timeout path (~2 s) and
 // records a code in *status.  Returns the launch status.
 cudaError_t launch_umma_stall_test(const Problem &p, int num_sms, int *status, cudaStream_t s);
+// The same on the CTA-pair kernel (16-bit, M > 128, A TMA-describable).  mode
+// 1: both producers load nothing; mode 2: the peer CTA loads one stage and
+// gives up (recording a timeout) while the leader has loaded further.  Either way the leader's MMA thread gives up,
+// raises the abort flag of both CTAs, the leader waits until every stage either
+// CTA loaded has landed, and the pair ends with its tensor memory released.
+cudaError_t launch_umma_pair_stall_test(const Problem &p, int mode, int *status, cudaStream_t s);
 
 // Fused FFN gate/up projection Z = SiLU(X W_g) * (X W_u) on the tensor-core
 // CTA pairs: p.A = X [M,K], p.B = W_g [K,N], p.C = Z [M,N], w_u = W_u [K,N],

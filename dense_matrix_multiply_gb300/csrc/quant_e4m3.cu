@@ -86,6 +86,35 @@ quantize_rows_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, floa
     if (lane == 0) scale[row] = amax / 448.0f;
 }
 
+// amax pass alone (the fused product's first step): one warp per row, the
+// same loads and reduction as the first pass above.
+template <bool VEC>
+__global__ void __launch_bounds__(WARPS * 32)
+row_amax_kernel(const __half *__restrict__ A, float *__restrict__ amax_out, int M, int K) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (row >= M) return;
+    const __half *a = A + row * K;
+    float amax = 0.0f;
+    if (VEC) {
+        for (int k = lane * 8; k < K; k += 32 * 8) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a + k));
+            const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(h[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    } else {
+        for (int k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(__half2float(a[k])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) amax_out[row] = amax;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
@@ -104,6 +133,16 @@ cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int 
                                   static_cast<uint8_t *>(Q), scale, M, K);
     return launch_counted(&cfg, quantize_rows_kernel<false>, static_cast<const __half *>(A),
                               static_cast<uint8_t *>(Q), scale, M, K);
+}
+
+cudaError_t launch_row_amax_f16(const void *A, float *amax, int M, int K, cudaStream_t s) {
+    const long long blocks = ((long long)M + WARPS - 1) / WARPS;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(WARPS * 32), 0, s, attr);
+    if (aligned(A, 16) && (K % 8) == 0)
+        return launch_counted(&cfg, row_amax_kernel<true>, static_cast<const __half *>(A), amax, M, K);
+    return launch_counted(&cfg, row_amax_kernel<false>, static_cast<const __half *>(A), amax, M, K);
 }
 
 }  // namespace gemm_gb300

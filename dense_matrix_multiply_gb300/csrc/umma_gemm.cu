@@ -49,6 +49,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -95,6 +96,8 @@ struct BarsT {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t peer_done;        // CTA pairs (leader's copy): the peer's producer has finished
+    long long peer_issued;     // CTA pairs (leader's copy): stages the peer's producer loaded
     uint32_t tmem_base;
     int abort;
 };
@@ -119,6 +122,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+// Counts `bytes` of the current phase's expected transactions as done.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
@@ -233,6 +240,13 @@ __device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
+// Raises the abort flag of this CTA and of its peer in the pair, so that the
+// peer's waits give up at once instead of timing out on their own.
+__device__ __forceinline__ void raise_abort_pair(volatile int *abort_flag, uint32_t rank) {
+    *abort_flag = 1;
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to_rank((const void *)abort_flag, rank ^ 1u)), "r"(1)
+                 : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -344,6 +358,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16 *) {
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half *) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+// Two FP32 values to E4M3FN codes (nearest, ties to even, saturating to
+// +-448), the first in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 __device__ __forceinline__ void store1(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void store1(__half *p, float x) { *p = __float2half_rn(x); }
@@ -666,7 +685,8 @@ struct PairArgs {
     int b_t;                  // B stored [N, K] (K contiguous) instead of [K, N]
     int a_bcast, b_bcast;     // batch stride 0: every b reads matrix 0
     float alpha, beta;
-    const float *row_scale;   // FP8 products: per-row scale of the output
+    const float *row_scale;   // FP8 products: per-row scale of the output (F8Q: the row's amax)
+    const void *a_src;        // F8Q: A [M,K] row-major half, quantised as it is loaded
     int *status;
     // Stream-K tail (sk_tiles > 0): the last sk_tiles tiles are cut into
     // K-block ranges of sk_w spread over clusters sk_first .. G-1, whose FP32
@@ -674,6 +694,7 @@ struct PairArgs {
     // 256-column slab per epilogue warp and CTA, column-major) instead of C.
     float *sk_ws;
     int sk_tiles, sk_w, sk_first;
+    int stall;  // test of the bounded waits: 1 = the producers load nothing, 2 = the peer stops after one stage
 };
 
 // Tile t -> (batch index, row tile, column tile); M-grouped raster inside a batch.
@@ -787,8 +808,20 @@ __device__ __forceinline__ void umma_pair_f8(uint32_t d_tmem, uint64_t a_desc, u
 // elements) and one kind::f8f6f4 MMA consumes K = 32 (32 bytes, as a 16-bit
 // K = 16 step).  The epilogue multiplies row i by row_scale[i] and rounds to
 // T (half).
-template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool DUAL = false, bool F8 = false>
-__global__ void __launch_bounds__(THREADS, 1)
+// F8Q (F8 with the quantisation fused into the load path, example 5-8's second
+// scheme): A is the half matrix itself.  Four more warps per CTA (6-9) read
+// its tile from global memory, 128 rows x 128 k per stage, multiply each value
+// by 448 / amax_i of its row (amax from a pass over the whole rows before the
+// product, row_scale[i] = amax_i), convert to E4M3 (nearest, saturating: the
+// codes gemm_quantize_rows_e4m3 writes) and store the codes into the stage in
+// the swizzled layout TMA would have written; full[s] then counts their eight
+// warp arrivals besides the B bytes.  The epilogue scales row i by
+// amax_i / 448.
+// STALL: the instance the bounded-wait tests launch (args.stall); the
+// production instances carry no test code on the producer's path.
+template <typename T, uint32_t AB_FORMAT, int PSTAGES, bool DUAL = false, bool F8 = false, bool F8Q = false,
+          bool STALL = false>
+__global__ void __launch_bounds__(F8Q ? THREADS + 128 : THREADS, 1)
 umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
                  const PairArgs args)
@@ -796,6 +829,10 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     using namespace pairk;
     using PBars = BarsT<PSTAGES>;
     static_assert(sizeof(PBars) <= 256, "barrier block");
+    static_assert(!F8Q || (F8 && !DUAL), "fused quantisation is an FP8 product");
+    // bytes the leader's full[s] expects per stage: both CTAs' A and B tiles, or
+    // (F8Q) only their B tiles -- the A codes are written by threads
+    constexpr uint32_t STAGE_TX = F8Q ? 2u * P_B_STAGE : P_STAGE_TX;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -819,9 +856,10 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PSTAGES; ++s) {
-            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->full[s], F8Q ? 1 + 8 : 1);  // F8Q: + 4 converter warps of each CTA
             mbar_init(&bars->empty[s], 1);
         }
+        mbar_init(&bars->peer_done, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->acc_full[b], 1);
             mbar_init(&bars->acc_empty[b], 256);
@@ -849,12 +887,26 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
+        // Every load of either CTA completes on the LEADER's full[s], which the
+        // leader arms with both halves' bytes; both producers wait for the MMAs
+        // to free a stage (empty[s], committed to both CTAs).  At the end the
+        // peer tells the leader how many stages it loaded (peer_issued, then an
+        // arrival on peer_done), and the leader waits until every stage either
+        // CTA loaded has landed -- counting, on a path that gave up early, the
+        // half of a stage that one side never loaded as done and arming a stage
+        // that only the peer loaded -- before the pair passes its final cluster
+        // barrier: no load is left in flight into either CTA's shared memory.
         int stage = 0;
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
+        // stall (STALL instances, a test of the bounded waits): 1 -- neither
+        // producer loads anything; 2 -- the peer loads only its first stage and
+        // then gives up, as on a failed wait, while the leader goes on.
+        const long long stop_after = STALL && args.stall == 2 && !leader ? 1 : (STALL && args.stall == 1 ? 0 : -1);
         for (int u = 0; ok; ++u) {
             int t, kb0, kb1, sk;
+            if (STALL && stop_after == 0) break;
             if (!pair_unit(u, cluster, nclusters, num_tiles, args, num_kb, t, kb0, kb1, sk)) break;
             int bt, tm, tn;
             coords(t, bt, tm, tn);
@@ -862,13 +914,16 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int row0 = tm * PBM + (int)rank * 128;
             const int col0 = tn * bn + (int)rank * (bn >> 1);
             for (int kb = kb0; kb < kb1; ++kb) {
+                if (STALL && issued == stop_after) { ok = false; break; }
                 if (!mbar_wait_cluster(&bars->empty[stage], phase ^ 1u, abort_flag, true)) { ok = false; break; }
                 const uint32_t full_leader = map_to_rank(&bars->full[stage], 0);
-                if (leader) mbar_arrive_expect_tx(&bars->full[stage], P_STAGE_TX);
+                if (leader) mbar_arrive_expect_tx(&bars->full[stage], STAGE_TX);
                 uint8_t *a_dst = a_tiles + stage * P_A_STAGE;
                 uint8_t *b_dst = b_tiles + stage * P_B_STAGE;
                 const int k0 = kb * KB;
-                if (!args.a_t) {
+                if (F8Q) {
+                    // A comes from the converter warps
+                } else if (!args.a_t) {
                     tma_load_3d_pair(a_dst, &tmA, full_leader, k0, row0, za);
                 } else {
                     tma_load_3d_pair(a_dst, &tmA, full_leader, row0, k0, za);
@@ -890,23 +945,39 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         if (!ok) {
             atomicOr(status, ST_PRODUCER);
-            *abort_flag = 1;
+            raise_abort_pair(abort_flag, rank);
         }
-        if (leader) {
-            // Every stage this pair armed has landed (both halves) before exit.
-            for (long long i = (issued > PSTAGES ? issued - PSTAGES : 0); i < issued; ++i) {
+        if (!leader) {
+            asm volatile("st.shared::cluster.b64 [%0], %1;" ::"r"(map_to_rank(&bars->peer_issued, 0)), "l"(issued)
+                         : "memory");
+            mbar_arrive_cluster(map_to_rank(&bars->peer_done, 0));  // release: the count is visible first
+        } else {
+            long long ip = issued;
+            if (mbar_wait_cluster(&bars->peer_done, 0, abort_flag, false)) {
+                ip = *reinterpret_cast<volatile long long *>(&bars->peer_issued);
+            } else {
+                atomicOr(status, ST_DRAIN);
+            }
+            // Uses of a stage complete in order, and neither side runs more than
+            // PSTAGES uses ahead of the MMAs, so only the last PSTAGES can be open.
+            // The two counts differ only after one side gave up (and recorded
+            // it in the status word): the MMAs may then have read a stage that
+            // is completed below without the other half, which is why such a
+            // call's C is undefined.
+            const long long hi = issued > ip ? issued : ip;
+            for (long long i = (hi > PSTAGES ? hi - PSTAGES : 0); i < hi; ++i) {
                 const int s = (int)(i % PSTAGES);
                 const uint32_t par = (uint32_t)((i / PSTAGES) & 1);
+                if (i >= issued) {
+                    mbar_arrive_expect_tx(&bars->full[s], STAGE_TX / 2);  // only the peer's half was loaded
+                } else if (i >= ip) {
+                    mbar_complete_tx(&bars->full[s], STAGE_TX / 2);       // the peer's half never will be
+                }
                 if (!mbar_wait_cluster(&bars->full[s], par, abort_flag, false)) {
                     atomicOr(status, ST_DRAIN);
                     break;
                 }
             }
-        } else if (!ok) {
-            // The peer cannot observe the leader's barriers: give loads already
-            // issued into its own shared memory time to land.
-            const unsigned long long t0 = globaltimer();
-            while (globaltimer() - t0 < 100000ull) { }
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer (leader)
@@ -954,10 +1025,73 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         if (!ok) {
             atomicOr(status, ST_MMA);
-            *abort_flag = 1;
+            raise_abort_pair(abort_flag, rank);
         }
         umma_commit_pair(&bars->drain);
         if (!mbar_wait_cluster(&bars->drain, 0, abort_flag, false)) atomicOr(status, ST_DRAIN);
+    } else if (F8Q && warp >= 6) {
+        // ------------------------------------------------------------ A converters (F8Q, both CTAs)
+        // Warp w (0-3) makes rows 32w .. 32w + 31 of this CTA's 128 rows of the
+        // A tile: per pass two rows, lanes 0-15 and 16-31, each lane 8
+        // consecutive k of its row (one 16-byte load, 8 codes).
+        const int cw = warp - 6;
+        const __half *Ah = static_cast<const __half *>(args.a_src);
+        const uint32_t full0 = map_to_rank(&bars->full[0], 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = 0; ok; ++u) {
+            int t, kb0, kb1, sk;
+            if (!pair_unit(u, cluster, nclusters, num_tiles, args, num_kb, t, kb0, kb1, sk)) break;
+            int bt, tm, tn;
+            coords(t, bt, tm, tn);
+            const int row_w = tm * PBM + (int)rank * 128 + cw * 32;  // this warp's first row
+            // lane l: 448 / amax of row row_w + l (0 for a row of zeros or past M:
+            // its codes are 0, as the separate quantiser writes them)
+            const float amax = row_w + lane < M ? args.row_scale[row_w + lane] : 0.0f;
+            const float inv_l = amax > 0.0f ? 448.0f / amax : 0.0f;
+            const int j = lane & 15;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->empty[stage], phase ^ 1u, abort_flag, true))) {
+                    ok = false;
+                    break;
+                }
+                const int gk = kb * KB + 8 * j;
+                uint4 v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int gr = row_w + 2 * i + (lane >> 4);
+                    v[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (gr < M && gk < K)  // K % 16 == 0: the 8 values are all in or all out
+                        v[i] = __ldg(reinterpret_cast<const uint4 *>(Ah + (size_t)gr * K + gk));
+                }
+                uint8_t *a_dst = a_tiles + stage * P_A_STAGE;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = 2 * i + (lane >> 4);  // row within the warp's 32
+                    const float inv = __shfl_sync(0xffffffffu, inv_l, r);
+                    const __half2 *h = reinterpret_cast<const __half2 *>(&v[i]);
+                    uint32_t w[2];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const float2 f0 = __half22float2(h[2 * q]);
+                        const float2 f1 = __half22float2(h[2 * q + 1]);
+                        w[q] = (uint32_t)e4m3x2(f0.x * inv, f0.y * inv) | ((uint32_t)e4m3x2(f1.x * inv, f1.y * inv) << 16);
+                    }
+                    const int rr = cw * 32 + r;  // row within the CTA's 128
+                    const uint32_t dst = smem_u32(a_dst + rr * 128 + ((((j >> 1) ^ (rr & 7))) << 4) + ((j & 1) << 3));
+                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(dst), "r"(w[0]), "r"(w[1]) : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the codes, to the MMAs
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(full0 + (uint32_t)(stage * sizeof(uint64_t)));
+                if (++stage == PSTAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok && lane == 0) {
+            atomicOr(status, ST_PRODUCER);
+            raise_abort_pair(abort_flag, rank);
+        }
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
@@ -974,7 +1108,11 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             coords(t, bt, tm, tn);
             const int buf = it & 1;
             const uint32_t acc_par = (uint32_t)((it >> 1) & 1);
-            if (!mbar_wait_cluster(&bars->acc_full[buf], acc_par, abort_flag, true)) { ok = false; break; }
+            // every lane waits; the warp leaves together if any lane gave up
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->acc_full[buf], acc_par, abort_flag, true))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             __syncwarp();
             const int n0 = tn * bn;
@@ -1036,7 +1174,8 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
             } else {
                 const int row = box_row0 + lane;
-                const float scale_v = F8 ? (row < M ? args.row_scale[row] : 0.0f) : alpha;
+                const float scale_v =
+                    F8 ? (row < M ? (F8Q ? args.row_scale[row] / 448.0f : args.row_scale[row]) : 0.0f) : alpha;
                 // This thread's row of C in batch bt, read only when beta != 0.
                 const T *c_old = (use_beta && row < M)
                                      ? static_cast<const T *>(args.C) + (long long)bt * args.stride_c +
@@ -1099,9 +1238,9 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_arrive_cluster(map_to_rank(&bars->acc_empty[buf], 0));
         }
         if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        if (!ok) {
+        if (!ok && lane == 0) {
             atomicOr(status, ST_EPILOGUE);
-            *abort_flag = 1;
+            raise_abort_pair(abort_flag, rank);
         }
     }
 
@@ -1585,19 +1724,19 @@ bool make_map3(CUtensorMap *map, const void *base, CUtensorMapDataType dt, long 
 
 // Largest number of co-resident two-CTA clusters of the pair kernel, per device
 // (0: the pair kernel cannot be launched).
-template <typename T, uint32_t F, bool DUAL = false, bool F8 = false>
+template <typename T, uint32_t F, bool DUAL = false, bool F8 = false, bool F8Q = false, bool STALL = false>
 int pair_clusters_max(int dev) {
     static std::atomic<int> cached[64];
     static std::once_flag once[64];
     std::call_once(once[dev & 63], [&] {
-        auto kern = umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>;
+        auto kern = umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8, F8Q, STALL>;
         const int smem = pairk::smem_bytes(pairk::P_STAGES);
         int n = 0;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2, 1, 1);
-            cfg.blockDim = dim3(THREADS, 1, 1);
+            cfg.blockDim = dim3(F8Q ? THREADS + 128 : THREADS, 1, 1);
             cfg.dynamicSmemBytes = smem;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1614,12 +1753,12 @@ int pair_clusters_max(int dev) {
     return cached[dev & 63].load();
 }
 
-template <typename T, uint32_t F, bool DUAL, bool F8 = false>
+template <typename T, uint32_t F, bool DUAL, bool F8 = false, bool F8Q = false, bool STALL = false>
 cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                             const CUtensorMap &tb2, const PairArgs &args, int clusters, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(F8Q ? THREADS + 128 : THREADS, 1, 1);
     cfg.dynamicSmemBytes = pairk::smem_bytes(pairk::P_STAGES);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -1630,7 +1769,8 @@ cudaError_t launch_pair_cfg(const CUtensorMap &ta, const CUtensorMap &tb, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl ? 2 : 1;
-    return launch_counted(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8>, ta, tb, tc, tb2, args);
+    return launch_counted(&cfg, umma_pair_kernel<T, F, pairk::P_STAGES, DUAL, F8, F8Q, STALL>, ta, tb, tc, tb2,
+                          args);
 }
 
 // Whether T tiles of KB K-blocks on G clusters take a stream-K tail: the last
@@ -1690,7 +1830,7 @@ cudaError_t launch_pair_planned(const CUtensorMap &ta, const CUtensorMap &tb, co
 // launch, when a tensor map cannot describe an operand.
 template <typename T, uint32_t F>
 cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status, cudaStream_t s,
-                              bool allow_sk = true) {
+                              bool allow_sk = true, int stall = 0) {
     const CUtensorMapDataType dt = F == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const long long ba = p.sa == 0 ? 1 : p.batch, bb = p.sb == 0 ? 1 : p.batch;
     CUtensorMap ta, tb, tc;
@@ -1734,6 +1874,8 @@ cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status,
     args.alpha = p.alpha;
     args.beta = p.beta;
     args.status = status;
+    args.stall = stall;
+    if (stall) return launch_pair_cfg<T, F, false, false, false, true>(ta, tb, tc, tb, args, clusters, s);
     return launch_pair_planned<T, F>(ta, tb, tc, tb, args, clusters, tiles, allow_sk, s);
 }
 
@@ -1799,6 +1941,45 @@ cudaError_t launch_pair_e4m3(const void *Q, const float *scale, const void *Wt, 
     args.row_scale = scale;
     args.status = status;
     return launch_pair_planned<__half, 0, false, true>(ta, tb, tc, tb, args, clusters, tiles, true, s);
+}
+
+// C [M,N] half = diag(amax / 448) E4M3(diag(448 / amax) A) Wt^T on CTA pairs,
+// the quantisation of A [M,K] (half) done by the kernel's converter warps as
+// each tile is loaded; amax [M] from launch_row_amax_f16.  Same tile plan as
+// launch_pair_e4m3 without the stream-K tail.
+cudaError_t launch_pair_e4m3_fused(const void *A, const float *amax, const void *Wt, void *C, int M, int N, int K,
+                                   int clusters_max, int *status, cudaStream_t s) {
+    CUtensorMap tb, tc;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!make_map3(&tb, Wt, u8, K, N, 1, K, 0, 128, 128, 1) ||
+        !make_map3(&tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, N, M, 1, N, 0, 64, 32))
+        return cudaErrorNotSupported;
+    const long long tiles_m = (M + pairk::PBM - 1) / pairk::PBM;
+    int bn = 256;
+    long long best = -1;
+    for (int cand = 256; cand >= 128; cand -= 64) {
+        const long long t = tiles_m * ((N + cand - 1) / cand);
+        const long long waves = (t + clusters_max - 1) / clusters_max;
+        const long long cost = waves * (cand > 224 ? cand : 224);
+        if (best < 0 || cost < best) { best = cost; bn = cand; }
+    }
+    const long long tiles = tiles_m * ((N + bn - 1) / bn);
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
+    PairArgs args = {};
+    args.C = C;
+    args.ldc = N;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.batch = 1;
+    args.bn = bn;
+    args.b_t = 1;
+    args.alpha = 1.0f;
+    args.row_scale = amax;
+    args.a_src = A;
+    args.status = status;
+    return launch_pair_cfg<__half, 0, false, true, true>(tb, tb, tc, tb, args, clusters, s);
 }
 
 // The tight problem of the plain entry points as a general one; lda: row
@@ -2033,6 +2214,44 @@ cudaError_t launch_umma_e4m3_rowscale(const void *Q, const float *scale, const v
     const int cmax = pair_clusters_max<__half, 0, false, true>(dev);
     if (cmax <= 0) return cudaErrorNotSupported;
     return launch_pair_e4m3(Q, scale, Wt, C, M, N, K, cmax, status, s);
+}
+
+cudaError_t launch_umma_pair_stall_test(const Problem &p, int mode, int *status, cudaStream_t s) {
+    if (mode != 1 && mode != 2) return cudaErrorInvalidValue;
+    if (!umma_supported(p) || !a_tma_ok(p) || p.M <= BM) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // (the test instance: its shared-memory attribute is set by this query)
+    const int cmax = p.elt == Elt::BF16 ? pair_clusters_max<__nv_bfloat16, 1, false, false, false, true>(dev)
+                                        : pair_clusters_max<__half, 0, false, false, false, true>(dev);
+    if (cmax <= 0) return cudaErrorNotSupported;
+    const ProblemEx q = plain_ex(p);
+    return p.elt == Elt::BF16 ? launch_pair_typed<__nv_bfloat16, 1>(q, cmax, status, s, false, mode)
+                              : launch_pair_typed<__half, 0>(q, cmax, status, s, false, mode);
+}
+
+bool umma_e4m3_fused_supported(const void *A, const void *Wt, const void *C, int N, int K) {
+    return aligned(A, 16) && umma_e4m3_supported(A, Wt, C, N, K);
+}
+
+cudaError_t launch_umma_e4m3_fused(const void *A, const void *Wt, void *C, int M, int N, int K, int *status,
+                                   cudaStream_t s) {
+    if (!umma_e4m3_fused_supported(A, Wt, C, N, K)) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int cmax = pair_clusters_max<__half, 0, false, true, true>(dev);
+    if (cmax <= 0) return cudaErrorNotSupported;
+    // the rows' amax, in stream-ordered scratch for the duration of the call
+    void *amax = nullptr;
+    e = cudaMallocAsync(&amax, (size_t)M * sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    e = launch_row_amax_f16(A, static_cast<float *>(amax), M, K, s);
+    if (e == cudaSuccess)
+        e = launch_pair_e4m3_fused(A, static_cast<const float *>(amax), Wt, C, M, N, K, cmax, status, s);
+    const cudaError_t f = cudaFreeAsync(amax, s);
+    return e != cudaSuccess ? e : f;
 }
 
 cudaError_t launch_umma_stall_test(const Problem &p, int num_sms, int *status, cudaStream_t s) {

@@ -235,6 +235,28 @@ GEMM_API gemm_status_t gemm_quantize_rows_e4m3(const uint16_t *A, uint8_t *Q, fl
 GEMM_API gemm_status_t gemm_e4m3_rowscale(const uint8_t *Q, const float *scale, const uint8_t *Wt, uint16_t *C,
                                           int M, int N, int K);
 
+/* Row-scaled FP8 projection with the quantisation fused into the product's
+ * load path ("Chapter 5 Operators and Runtime", section 5.4.4, example 5-8, the
+ * second scheme: the row scales from a first pass over the whole input, then
+ * every column block of the product reads the half input and quantises it
+ * locally):
+ *     amax_i  = max_k |a_ik|
+ *     C[i,j]  = (amax_i / 448) * sum_k E4M3(a_ik * (448 / amax_i)) * W[k,j]
+ * -- the codes and the row scale of gemm_quantize_rows_e4m3 (the same FP32
+ * steps), but never written to memory: the product's loader quantises each
+ * tile of A as it stages it.  A [M,K] row-major IEEE half; the weights W [K,N]
+ * given transposed, Wt [N,K] row-major E4M3FN codes; C [M,N] row-major half.
+ * Results equal gemm_quantize_rows_e4m3 followed by gemm_e4m3_rowscale up to
+ * the summation order of the FP32 accumulation.  The rows' amax (4 bytes per
+ * row) are kept in the device's default stream-ordered pool for the duration
+ * of the call (cudaMallocAsync / cudaFreeAsync on the caller's stream).  Needs
+ * A, Wt, C 16-byte aligned, K % 16 == 0 and N % 8 == 0
+ * (GEMM_ERR_INVALID_VALUE otherwise, with a message in gemm_last_error).
+ * K = 0 gives C = 0.  GEMM_ERR_ALIAS if C overlaps A or Wt.  NaN or infinite
+ * inputs are outside the contract. */
+GEMM_API gemm_status_t gemm_e4m3_rowscale_fused(const uint16_t *A, const uint8_t *Wt, uint16_t *C,
+                                                int M, int N, int K);
+
 /* Stream for the calling host thread's subsequent calls: a cudaStream_t passed
  * as void*.  NULL selects the legacy default stream.  The stream stays owned by
  * the caller and must outlive the calls issued on it. */
@@ -275,7 +297,11 @@ GEMM_API const char *gemm_last_error(void);
  * "umma_stall" tests the tensor-core kernel's bounded waits: a 16-bit call whose
  * A, B and C suit the TMA kernel launches it with a producer that issues no
  * loads, every CTA gives up after about two seconds, C is left unwritten and
- * the next gemm_synchronize returns GEMM_ERR_TIMEOUT.  gemm_bf16_rm_noalloc
+ * the next gemm_synchronize returns GEMM_ERR_TIMEOUT.  "umma_stall_pair" does the
+ * same on the CTA-pair kernel (16-bit, M > 128, A 16-byte aligned with K a
+ * multiple of 8), and "umma_stall_peer" makes the pair's second CTA give up
+ * after loading one stage while the first has loaded further, so that the pair
+ * ends with loads of only one CTA outstanding.  gemm_bf16_rm_noalloc
  * honours "umma_stall" (recording in its static status word) and ignores the
  * other families. */
 GEMM_API gemm_status_t gemm_force_kernel(const char *family);

@@ -133,6 +133,8 @@ MID_CASES = [
     ("bf16_rm", 16, 4096, 12288, None, "umma_bf16"),         # long K, 32 strips on clusters
     ("bf16_rm", 3, 1032, 2000, None, "umma_bf16"),           # 8-row X box, 3 rows used; ragged K
     ("f16_cm", 1000, 24, 3000, None, "umma_f16"),            # row-major M = 24 through the swap
+    ("bf16_rm", 2600, 4104, 520, None, "umma_bf16"),         # CTA pairs over 2.5 waves, ragged M and N
+    ("bf16_rm", 1000, 12296, 264, None, "umma_bf16"),        # ragged M and N, 3 waves
 ]
 
 
