@@ -62,7 +62,9 @@ DEFAULT_PATHS = ["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144", "ffn_bf16_r
                  "edge_f32_rm_8192x4096x4100", "edge_f32_rm_8192x4096x4096",
                  "ffn_gate_up_bf16_silu_mul_1024x12288x4096",
                  "gemm_ex_bf16_rm_NT_8192x8192x8192", "gemm_ex_f16_rm_NN_batch32_1024x1024x1024",
-                 "gemm_ex_f32_rm_NT_4096x4096x4096", "fp8_rowscale_e4m3_4096x1536x4096"]
+                 "gemm_ex_f32_rm_NT_4096x4096x4096", "fp8_rowscale_e4m3_4096x1536x4096",
+                 "fp8_rowscale_fused_e4m3_4096x1536x4096", "fp8_rowscale_e4m3_8192x8192x8192",
+                 "fp8_rowscale_fused_e4m3_8192x8192x8192"]
 # Problems the oracle is also timed on with one host thread (the small
 # configurations): whole problems up to ONE_THREAD_FULL_FMAS multiply-adds,
 # else a bounded sample of rows.
@@ -116,6 +118,14 @@ def all_workloads():
     # row-wise to E4M3, times E4M3 weights [4096,1536], half output
     out["fp8_rowscale_e4m3_4096x1536x4096"] = (5, ("e4m3_rowscale", 4096, 1536, 4096, "normal", 1.0,
                                                     "uniform", 1.0))
+    # the same step with the quantisation fused into the product's load path
+    # (example 5-8's second scheme), and both schemes on a large square problem
+    out["fp8_rowscale_fused_e4m3_4096x1536x4096"] = (5, ("e4m3_fused", 4096, 1536, 4096, "normal", 1.0,
+                                                          "uniform", 1.0))
+    out["fp8_rowscale_e4m3_8192x8192x8192"] = (5, ("e4m3_rowscale", 8192, 8192, 8192, "normal", 1.0,
+                                                    "uniform", 1.0))
+    out["fp8_rowscale_fused_e4m3_8192x8192x8192"] = (5, ("e4m3_fused", 8192, 8192, 8192, "normal", 1.0,
+                                                          "uniform", 1.0))
     # the general form (gemm_ex): a linear layer's X W^T with W stored [N, K],
     # a strided batch, and FP32 with a transposed B on the SIMT kernel
     for dtype, ops, batch, (M, N, K) in (("bf16", "NT", 1, (8192, 8192, 8192)),
@@ -273,6 +283,9 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
     elif variant == "e4m3_rowscale":  # the product kernel: Q, W codes, the row scales, half C
         flops = metrics.gemm_flops(M, N, K)
         algo_bytes = M * K + K * N + 4 * M + 2 * M * N
+    elif variant == "e4m3_fused":  # the whole fused step: half A once, W codes, half C
+        flops = metrics.gemm_flops(M, N, K)
+        algo_bytes = 2 * M * K + K * N + 2 * M * N
     elif variant.startswith("ex:"):  # batch independent products, beta = 0 (C not read)
         batch = ex_parse(variant)[4]
         flops = batch * metrics.gemm_flops(M, N, K)
@@ -292,7 +305,7 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
     if kind == "umma":
         # below the ridge point (FLOPs per byte at which the measured tensor and
         # HBM peaks meet) the tensor-core kernel is bound by HBM: skinny M
-        tpeak = float(peaks["bf16_tflops"]) * (2.0 if variant == "e4m3_rowscale" else 1.0)
+        tpeak = float(peaks["bf16_tflops"]) * (2.0 if variant in ("e4m3_rowscale", "e4m3_fused") else 1.0)
         if flops / algo_bytes < tpeak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9):
             achieved = algo_bytes / seconds_per_launch / 1e9
             peak = float(peaks["hbm_gbs"])
@@ -300,7 +313,7 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
                     "traffic": traffic, "algorithmic_bytes": algo_bytes, "algorithmic_flops": flops,
                     "peak_source": peaks_src}
     achieved = flops / seconds_per_launch / 1e12
-    if kind == "umma" and variant == "e4m3_rowscale":
+    if kind == "umma" and variant in ("e4m3_rowscale", "e4m3_fused"):
         # dense FP8 rate = 2 x the dense BF16 rate (4.5 vs 2.25 PFLOP/s nominal)
         peak = 2.0 * float(peaks["bf16_tflops"])
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -417,7 +430,7 @@ def host_inputs(variant, cfg, M, N, K, da, sa, db, sb):
         A = synthetic.matrix("bf16", M, K, synthetic.seed_for(cfg, 1), da, sa)
         B = synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 2), db, sb)
         return A, B, (synthetic.matrix("bf16", K, N, synthetic.seed_for(cfg, 3), db, sb),)
-    if variant == "e4m3_rowscale":
+    if variant in ("e4m3_rowscale", "e4m3_fused"):
         A = synthetic.matrix("f16", M, K, synthetic.seed_for(cfg, 1), da, sa)
         return A, synthetic.e4m3_codes(N, K, synthetic.seed_for(cfg, 2)), ()
     if variant.startswith("ex:"):
@@ -437,7 +450,7 @@ def oracle_rows(variant, A, B, M, N, K, rows, extra=()):
     if variant == "bf16_silu_mul":
         oracle.silu_mul(A, B, extra[0], M, N, K, rows=rows)
         return 4.0 * len(rows) * N * K, None
-    if variant == "e4m3_rowscale":  # quantise the rows, then their products
+    if variant in ("e4m3_rowscale", "e4m3_fused"):  # quantise the rows, then their products
         a = np.ascontiguousarray(A.reshape(M, K)[rows])
         Q, S = oracle.quantize_rows_e4m3(a, len(rows), K)
         oracle.gemm_e4m3_rowscale(Q, S, B, len(rows), N, K)
@@ -716,6 +729,20 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
 
         def call():
             return quantize() or product()
+    elif variant == "e4m3_fused":
+        # one step: the row amax pass and the product that quantises A as it loads it
+        A, B, _ = host_inputs(variant, cfg, M, N, K, da, sa, db, sb)
+        dA = torch.from_numpy(A.view(np.int16)).cuda()
+        dB = torch.from_numpy(B).cuda()
+        dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+        fused_fn = g.load().gemm_e4m3_rowscale_fused
+        plain_sets = [(dA.data_ptr(), dB.data_ptr(), dC.data_ptr())]
+        plain_i = [0]
+
+        def call():
+            pa_, pb_, pc_ = plain_sets[plain_i[0] % len(plain_sets)]
+            plain_i[0] += 1
+            return fused_fn(pa_, pb_, pc_, M, N, K)
     elif variant.startswith("ex:"):
         # tight strides: A stored [M,K] or [K,M], B [K,N] or [N,K], batch matrices back to back
         dtype, layout, op_a, op_b, batch = ex_parse(variant)
@@ -759,10 +786,10 @@ def measure_workload(name, steps, warmup, peaks, peaks_src, sms, stream, sampler
     # timed back to back.
     rotated = 1
     keep = []
-    if footprint <= L2_BYTES and (variant in ENTRY or variant == "e4m3_rowscale"):
+    if footprint <= L2_BYTES and (variant in ENTRY or variant in ("e4m3_rowscale", "e4m3_fused")):
         rotated = int(min(512, -(-3 * int(L2_BYTES) // max(1, footprint))))
         for _ in range(rotated - 1):
-            if variant in ENTRY:
+            if variant in ENTRY or variant == "e4m3_fused":
                 a2, b2, c2 = dA.clone(), dB.clone(), torch.empty_like(dC)
                 keep += [a2, b2, c2]
                 plain_sets.append((a2.data_ptr(), b2.data_ptr(), c2.data_ptr()))

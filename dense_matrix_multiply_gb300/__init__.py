@@ -42,6 +42,7 @@ SIGNATURES = {
                  _I], _I),
     "gemm_quantize_rows_e4m3": ([_VP, _VP, _VP, _I, _I], _I),
     "gemm_e4m3_rowscale": ([_VP, _VP, _VP, _VP, _I, _I, _I], _I),
+    "gemm_e4m3_rowscale_fused": ([_VP, _VP, _VP, _I, _I, _I], _I),
     "gemm_set_stream": ([_VP], _I),
     "gemm_get_stream": ([], _VP),
     "gemm_synchronize": ([], _I),
@@ -162,6 +163,17 @@ def gemm_e4m3_rowscale(Q, scale, Wt, C, M: int, N: int, K: int) -> None:
     st = lib.gemm_e4m3_rowscale(_addr(Q), _addr(scale), _addr(Wt), _addr(C), int(M), int(N), int(K))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_e4m3_rowscale", lib.gemm_last_error().decode())
+
+
+def gemm_e4m3_rowscale_fused(A, Wt, C, M: int, N: int, K: int) -> None:
+    """C[M,N] (half) = diag(amax/448) E4M3(diag(448/amax) A) W, the row-wise
+    quantisation of the half A [M,K] fused into the product's load path; the
+    E4M3 weights given as Wt [N,K]."""
+    lib = load()
+    _bind_torch_stream(A, Wt, C)
+    st = lib.gemm_e4m3_rowscale_fused(_addr(A), _addr(Wt), _addr(C), int(M), int(N), int(K))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_e4m3_rowscale_fused", lib.gemm_last_error().decode())
 
 
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}

@@ -142,3 +142,69 @@ def test_rowscale_k_zero_and_rejections():
     with pytest.raises(g.GemmError, match="INVALID"):
         g.gemm_e4m3_rowscale(Q, s, Q, dC, M, N, 24)     # K % 16 != 0
     assert "K % 16" in g.gemm_last_error()
+
+
+# ---------------------------------------------------------- quantisation fused into the product
+def run_fused(A, W, M, N, K):
+    dA, dW = dev_u16(A), dev_u8(W)
+    dC = torch.full((M * N,), 0x7E00, dtype=torch.int16, device="cuda")
+    g.gemm_e4m3_rowscale_fused(dA, dW, dC, M, N, K)
+    name = g.gemm_last_kernel()
+    g.gemm_synchronize()
+    return dC.cpu().numpy().view(np.float16).astype(np.float64).reshape(M, N), name
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (300, 200, 272), (512, 1536, 4096), (1, 8, 16),
+                                   (130, 264, 4112), (1024, 392, 640), (600, 1000, 1008)])
+def test_fused_quantisation_product(M, N, K):
+    """The fused scheme against the oracle (quantise the rows, then the row-scaled
+    product), and bit for bit against the separate scheme on the same tiles:
+    the converter warps must write the quantiser's very codes."""
+    A = half_rows(M, K, 4, spread=False)
+    if M > 6:
+        A[3] = 0                               # a row of zeros: codes 0, scale 0
+        A[5, :] = 0
+        A[5, K - 1] = synthetic.f32_to_f16_bits(np.array([-3.0], dtype=np.float32))[0]
+    W = synthetic.e4m3_codes(N, K, synthetic.seed_for(CFG, 70))
+    C, name = run_fused(A, W, M, N, K)
+    assert name == "umma_e4m3_rowscale_fused"
+    Q, S = oracle.quantize_rows_e4m3(A, M, K)
+    C_ref, Sab = oracle.gemm_e4m3_rowscale(Q, S, W, M, N, K)
+    res = compare.check_e4m3(C, C_ref, Sab)
+    assert res["ok"], res
+    # the separate scheme (no stream-K tail below K = 48 blocks of 128): same bits
+    Qg, Sg, _ = quantize_gpu(A, M, K)
+    C_sep, _ = run_rowscale(Qg, Sg, W, M, N, K)
+    assert np.array_equal(C.view(np.uint64), C_sep.view(np.uint64))
+
+
+def test_fused_quantisation_pages_workload_sampled_rows():
+    """Example 5-8's shapes (A [4096,4096] half, W [4096,1536] E4M3): the fused
+    product equals the separate one bit for bit and the oracle on sampled rows."""
+    M, K, N = 4096, 4096, 1536
+    A = half_rows(M, K, 3, spread=False)
+    W = synthetic.e4m3_codes(N, K, synthetic.seed_for(CFG, 60))
+    C, _ = run_fused(A, W, M, N, K)
+    Qg, Sg, _ = quantize_gpu(A, M, K)
+    C_sep, _ = run_rowscale(Qg, Sg, W, M, N, K)
+    assert np.array_equal(C.view(np.uint64), C_sep.view(np.uint64))
+    rows = np.concatenate([np.random.default_rng(1).integers(0, M, 48), [0, 255, 256, M - 1]])
+    Q, S = oracle.quantize_rows_e4m3(A[rows], rows.size, K)
+    C_ref, Sab = oracle.gemm_e4m3_rowscale(Q, S, W, rows.size, N, K)
+    res = compare.check_e4m3(C[rows], C_ref, Sab)
+    assert res["ok"], res
+
+
+def test_fused_quantisation_k_zero_and_rejections():
+    M, N = 64, 64
+    dC = torch.full((M * N,), 0x3C00, dtype=torch.int16, device="cuda")
+    a = torch.zeros(M * 32 + 8, dtype=torch.int16, device="cuda")
+    w = torch.zeros(N * 32, dtype=torch.uint8, device="cuda")
+    g.gemm_e4m3_rowscale_fused(a, w, dC, M, N, 0)
+    g.gemm_synchronize()
+    assert not dC.any()
+    with pytest.raises(g.GemmError, match="INVALID"):
+        g.gemm_e4m3_rowscale_fused(a, w, dC, M, N, 24)    # K % 16 != 0
+    with pytest.raises(g.GemmError, match="INVALID"):
+        g.gemm_e4m3_rowscale_fused(a[1:], w, dC, M, N, 32)  # A not 16-byte aligned
+    assert "aligned" in g.gemm_last_error()
