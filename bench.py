@@ -111,6 +111,13 @@ def all_workloads():
     for (M, N, K) in synthetic.EDGE_SHAPES:
         for v in ("f32_rm", "bf16_rm"):
             out[f"edge_{v}_{M}x{N}x{K}"] = (synthetic.EDGE_CONFIG_ID, (v, M, N, K, "uniform", 1.0, "uniform", 1.0))
+    # kernels of the dispatch table that no configuration above reaches, for
+    # their profiles: the single-CTA tensor-core kernel (M = 128) and the
+    # scalar-FFMA SIMT kernel (FP32 rows not 16-byte aligned: K = 4095)
+    out["single_cta_bf16_rm_128x12288x4096"] = (synthetic.EDGE_CONFIG_ID, ("bf16_rm", 128, 12288, 4096, "uniform",
+                                                                         1.0, "uniform", 1.0))
+    out["unaligned_f32_rm_4096x4096x4095"] = (synthetic.EDGE_CONFIG_ID, ("f32_rm", 4096, 4096, 4095, "uniform", 1.0,
+                                                                       "uniform", 1.0))
     # the FFN gate/up projection with its SiLU * U epilogue fused (two GEMMs)
     out["ffn_gate_up_bf16_silu_mul_1024x12288x4096"] = (3, ("bf16_silu_mul", 1024, 12288, 4096, "normal", 1.0,
                                                              "normal", 1.0 / 64.0))

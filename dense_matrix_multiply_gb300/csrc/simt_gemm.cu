@@ -683,6 +683,102 @@ cudaError_t launch_ffma2_split(const float *A, const float *B, float *C, int M, 
                               (int)base);
 }
 
+// ------------------------------------------------------------ small problems
+// A plain FP32 problem whose 128 x 64 tiles would occupy at most a quarter of
+// the SMs (SGEMM 256^3 is 8 such tiles on 152 SMs) runs on 32 x 32 tiles
+// instead: sixteen times the CTAs, 64 threads each, 4 x 4 outputs per thread,
+// K step 16.  Measured on GB300 (back to back, operands from DRAM), small
+// kernel against the 128 x 64 one: 256^3 9.3 vs 13.6 us, 512^3 22.7 vs 26.6,
+// 300 x 520 x 272 12.8 vs 15.3, 64^3 3.2 vs 4.7; with more tiles the large
+// kernel wins (1000^3: 128 tiles, 50.5 vs 83.9 us).  The k-major A
+// tile and the B tile are double-buffered in shared memory, the next K step
+// loaded into registers (16-byte loads) while the current one is multiplied;
+// one barrier per step.  Per k a thread makes one 16-byte shared load of A
+// (its four rows) and one of B (its four columns) and 16 FFMAs, every output
+// summed over k in ascending order with one rounding per step, as in the
+// other SIMT kernels.
+#ifndef SIMT_SMALL
+#define SIMT_SMALL 1
+#endif
+constexpr int S_BM = 32, S_BN = 32, S_BK = 16, S_THREADS = 64;
+
+__global__ void __launch_bounds__(S_THREADS, 16)
+simt_small_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ C, int M, int N,
+                  int K)
+{
+    pdl_wait();  // several CTAs per SM: dependents launch as the CTAs exit
+    __shared__ __align__(16) float As[2][S_BK][S_BM];
+    __shared__ __align__(16) float Bs[2][S_BK][S_BN];
+    const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
+    const int tiles_n = (N + S_BN - 1) / S_BN;
+    const int m0 = (int)(blockIdx.x / tiles_n) * S_BM, n0 = (int)(blockIdx.x % tiles_n) * S_BN;
+    float4 ra[2], rb[2];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + i * S_THREADS;
+            const int row = idx >> 2, kq = (idx & 3) * 4;  // A: 32 rows x 4 quads of k
+            const int gm = m0 + row, gk = k0 + kq;
+            ra[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (gm < M && gk < K) ra[i] = __ldg(reinterpret_cast<const float4 *>(A + (size_t)gm * K + gk));
+            const int kr = idx >> 3, nq = (idx & 7) * 4;   // B: 16 k-rows x 8 quads of n
+            const int gk2 = k0 + kr, gn = n0 + nq;
+            rb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (gk2 < K && gn < N) rb[i] = __ldg(reinterpret_cast<const float4 *>(B + (size_t)gk2 * N + gn));
+        }
+    };
+    auto store = [&](int b) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + i * S_THREADS;
+            const int row = idx >> 2, kq = (idx & 3) * 4;
+            As[b][kq + 0][row] = ra[i].x;
+            As[b][kq + 1][row] = ra[i].y;
+            As[b][kq + 2][row] = ra[i].z;
+            As[b][kq + 3][row] = ra[i].w;
+            *reinterpret_cast<float4 *>(&Bs[b][idx >> 3][(idx & 7) * 4]) = rb[i];
+        }
+    };
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const int ktiles = (K + S_BK - 1) / S_BK;
+    load(0);
+    store(0);
+    __syncthreads();
+    for (int t = 0; t < ktiles; ++t) {
+        const int b = t & 1;
+        if (t + 1 < ktiles) load((t + 1) * S_BK);
+#pragma unroll
+        for (int kk = 0; kk < S_BK; ++kk) {
+            const float4 a = *reinterpret_cast<const float4 *>(&As[b][kk][ty * 4]);
+            const float4 bb = *reinterpret_cast<const float4 *>(&Bs[b][kk][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        if (t + 1 < ktiles) store(b ^ 1);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gm = m0 + ty * 4 + i, gn = n0 + tx * 4;
+        if (gm >= M) continue;
+        float *dst = C + (size_t)gm * N + gn;
+        if (gn + 3 < N) {
+            *reinterpret_cast<float4 *>(dst) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gn + j < N) dst[j] = acc[i][j];
+        }
+    }
+}
+
 // Tile configuration of the SIMT kernel: K step and CTAs per SM.
 #ifndef SIMT_BK
 #define SIMT_BK 8
@@ -704,6 +800,12 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
             float *fC = static_cast<float *>(p.C);
             // three packed-FMA CTAs are resident per SM
             const long long ftiles = (long long)((p.M + G_BM - 1) / G_BM) * ((p.N + G_BN - 1) / G_BN);
+            if (SIMT_SMALL && 4 * ftiles <= num_sms) {
+                const long long stiles = (long long)((p.M + S_BM - 1) / S_BM) * ((p.N + S_BN - 1) / S_BN);
+                cudaLaunchAttribute attr[1];
+                const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)stiles), dim3(S_THREADS), 0, s, attr);
+                return launch_counted(&cfg, simt_small_kernel, fA, fB, fC, p.M, p.N, p.K);
+            }
             const long long tail = ffma2_tail_tiles(ftiles, p.K, 3LL * num_sms);
             if (tail > 0) return launch_ffma2_split(fA, fB, fC, p.M, p.N, p.K, ftiles, tail, s);
             return launch_ffma2<false, false, false>(fA, fB, fC, p.M, p.N, p.K, SimtEx{}, 1, s);
