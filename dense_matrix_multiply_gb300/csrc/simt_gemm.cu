@@ -337,9 +337,11 @@ struct F2Shared {
 // alpha and beta), TA: A stored [K, M] -- its tile is already k-major and goes
 // to shared memory by cp.async; TB: B stored [N, K] -- its tile passes through
 // registers to be transposed into the swizzled layout.
-// MODE 0: every tile of the problem.  A plain problem whose last round of
-// resident CTAs would be part full runs as two grids: MODE 1 the whole tiles
-// before tile_base, MODE 2 the rest on clusters of two CTAs, the first taking
+// MODE 0: every tile of the problem.  MODE 3: every tile as a cluster of two
+// half-K CTAs (a problem too small for one round of resident CTAs).  A plain
+// problem whose last round of resident CTAs would be part full runs as two
+// grids: MODE 1 the whole tiles before tile_base, MODE 2 the rest on clusters
+// of two CTAs, the first taking
 // the first half of the K blocks and the second the rest; the halves' FP32
 // sums are exchanged through distributed shared memory and added.
 template <bool EX, bool TA, bool TB, int MODE = 0>
@@ -354,7 +356,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     // this grid frees.  The tail reads only A and B (complete once every MODE 1
     // CTA has passed its wait) and waits for MODE 1 before it exits, so that
     // the next kernel on the stream sees both grids' tiles of C.
-    if constexpr (MODE != 2) pdl_wait();
+    if constexpr (MODE != 2) pdl_wait();  // MODE 3, a grid of its own, waits too
     if constexpr (MODE == 1) pdl_launch_dependents();
     extern __shared__ __align__(16) uint8_t f2_smem[];
     F2Shared &sm = *reinterpret_cast<F2Shared *>(f2_smem);
@@ -377,7 +379,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     const int tiles_m = (M + G_BM - 1) / G_BM, tiles_n = (N + G_BN - 1) / G_BN;
     int tm, tn;
     {
-        const int pid = MODE == 2 ? tile_base + (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+        const int pid = MODE >= 2 ? tile_base + (int)(blockIdx.x >> 1) : (int)blockIdx.x;
         const int per_group = GROUP_M * tiles_n;
         const int group = pid / per_group;
         const int first_m = group * GROUP_M;
@@ -389,9 +391,9 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     const int m0 = tm * G_BM, n0 = tn * G_BN;
     const int ktiles = (K + G_BK - 1) / G_BK;
     // K blocks [kt0, kt0 + kcount) of the tile: all of them, or one half (MODE 2)
-    const int khalf = MODE == 2 ? (int)(blockIdx.x & 1) : 0;
+    const int khalf = MODE >= 2 ? (int)(blockIdx.x & 1) : 0;
     const int kt0 = khalf ? ktiles / 2 : 0;
-    const int kcount = MODE == 2 ? (khalf ? ktiles - ktiles / 2 : ktiles / 2) : ktiles;
+    const int kcount = MODE >= 2 ? (khalf ? ktiles - ktiles / 2 : ktiles / 2) : ktiles;
 
     auto cp16 = [&](float *dst, const float *src, bool in) {
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
@@ -545,7 +547,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 
     // row i: a_off + 32 (i >> 2) + (i & 3); column pair j: b_off + 16 (j >> 1) + 2 (j & 1).
-    if constexpr (MODE == 2) {
+    if constexpr (MODE >= 2) {
         // Rows a_off + 32 q + {0..3} are stored by the CTA of rank q.  Each CTA
         // puts the rows its partner stores into its own shared memory (row
         // wm 32 + lm 4 + i of a 64-row buffer, stride 68 floats so that the
@@ -594,7 +596,7 @@ simt_ffma2_kernel(const float *__restrict__ A, const float *__restrict__ B, floa
             }
         }
         cluster.sync();  // the partner's reads of this CTA's shared memory are done
-        pdl_wait();      // MODE 1 complete before this grid counts as complete
+        if constexpr (MODE == 2) pdl_wait();  // MODE 1 complete before this grid counts as complete
         return;
     }
     // The general form scales by alpha and, when beta != 0, adds beta * old C.
@@ -699,6 +701,9 @@ cudaError_t launch_ffma2_split(const float *A, const float *B, float *C, int M, 
 // other SIMT kernels.
 #ifndef SIMT_SMALL
 #define SIMT_SMALL 1
+#endif
+#ifndef SIMT_SPLIT_ALL
+#define SIMT_SPLIT_ALL 1
 #endif
 constexpr int S_BM = 32, S_BN = 32, S_BK = 16, S_THREADS = 64;
 
@@ -805,6 +810,22 @@ cudaError_t launch_typed(const Problem &p, int num_sms, cudaStream_t s) {
                 cudaLaunchAttribute attr[1];
                 const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)stiles), dim3(S_THREADS), 0, s, attr);
                 return launch_counted(&cfg, simt_small_kernel, fA, fB, fC, p.M, p.N, p.K);
+            }
+            // fewer tiles than one round of resident CTAs, at most half a round:
+            // every tile as two half-K CTAs (1000^3: 128 tiles, 256 CTAs; on
+            // GB300 48.4 against 50.3 us, 1024 x 1024 x 4096 174.5 against 191.2)
+            if (SIMT_SPLIT_ALL && g_simt_split_tail && g_pdl && 2 * ftiles <= 3LL * num_sms &&
+                (p.K + G_BK - 1) / G_BK >= 32) {
+                cudaLaunchAttribute attr[2];
+                cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(2 * ftiles)), dim3(THREADS),
+                                                    (int)sizeof(F2Shared), s, attr);
+                attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+                attr[cfg.numAttrs].val.clusterDim.x = 2;
+                attr[cfg.numAttrs].val.clusterDim.y = 1;
+                attr[cfg.numAttrs].val.clusterDim.z = 1;
+                cfg.numAttrs += 1;
+                return launch_counted(&cfg, simt_ffma2_kernel<false, false, false, 3>, fA, fB, fC, p.M, p.N, p.K,
+                                      SimtEx{}, 0);
             }
             const long long tail = ffma2_tail_tiles(ftiles, p.K, 3LL * num_sms);
             if (tail > 0) return launch_ffma2_split(fA, fB, fC, p.M, p.N, p.K, ftiles, tail, s);

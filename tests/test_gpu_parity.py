@@ -96,6 +96,8 @@ MID_CASES = [
     ("f32_rm", 300, 520, 272, None, "simt_f32_vec4"),
     ("f32_rm", 129, 68, 1000, None, "simt_f32_vec4"),
     ("f32_rm", 257, 131, 77, None, "simt_f32_scalar"),
+    ("f32_rm", 1030, 700, 600, None, "simt_f32_vec4"),        # 99 tiles: every tile as two half-K CTAs
+    ("f32_rm", 512, 520, 264, None, "simt_f32_vec4"),         # 36 tiles: the small-tile kernel
     ("f32_rm", 200, 300, 96, "simt_scalar", "simt_f32_scalar"),
     ("f32_rm", 5, 300, 999, None, "gemv_f32_vec"),
     ("f32_rm", 3, 301, 257, None, "gemv_f32_scalar"),
