@@ -4,7 +4,8 @@ When the 256 x 256 tiles leave the last wave nearly empty (at most a quarter
 of the clusters) and K is long (at least 48 K-blocks), the K iterations of the
 remainder tiles are spread over the clusters and each such tile is the sum, in
 K order, of two to five FP32 partials.  The shapes below make 80 or 81 tiles,
-4 to 7 tiles past a full wave of the 74-76 CTA pairs of a GB300.  Checked: whole rows
+4 to 7 tiles past a full wave of the 74-76 CTA pairs of a GB300; two more make
+192 tiles, 40 past two waves, which run as whole tiles.  Checked: whole rows
 from every quarter of both CTA halves of every 256-row band (so every tile,
 stream-K or not, is hit), and bit-identical results on a second run."""
 
@@ -42,6 +43,8 @@ CASES = [
     ("bf16_rm", 2048, 2560, 3072),  # 8 x 10 tiles
     ("bf16_rm", 2304, 2296, 3080),  # 9 x 9 tiles, ragged N and K
     ("f16_cm", 2560, 2048, 3072),   # C^T = B^T A^T: 8 x 10 tiles
+    ("bf16_rm", 1024, 12288, 2048), # 4 x 48 tiles: 40 in the last wave
+    ("bf16_rm", 1000, 12040, 1032), # 4 x 48 tiles, ragged M, N and K
 ]
 
 
