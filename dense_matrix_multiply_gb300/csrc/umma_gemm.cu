@@ -1855,6 +1855,10 @@ cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status,
         const long long cost = waves * (cand > 224 ? cand : 224);
         if (best < 0 || cost < best) { best = cost; bn = cand; }
     }
+    // Under one wave even at 128 columns: the narrowest tiles, the most SMs
+    // busy (measured back to back: bf16 1024^3 9.9 vs 10.2 us with 192-wide
+    // tiles, 2048 x 1024 x 512 7.8 vs 8.2, 1000 x 1536 x 1000 10.0 vs 10.7).
+    if (!sk_ok && tiles_mb * ((p.N + 127) / 128) <= clusters_max) bn = 128;
     const long long tiles = tiles_mb * ((p.N + bn - 1) / bn);
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     const int clusters = (int)(tiles < clusters_max ? tiles : clusters_max);
