@@ -10,10 +10,12 @@
 // ones an FP32 evaluation of these steps gives.  A row of zeros gives q = 0 and
 // scale 0.
 //
-// Bound: HBM (read 2 bytes, write 1 byte per element).  One warp per row: a
-// first pass of 16-byte loads finds amax (warp shuffle reduction), a second
-// pass re-reads the row -- from L1/L2, the row was just read -- and writes 8
-// codes per 8-byte store.  Rows that are not 16-byte aligned use scalar loads.
+// Bound: HBM (read 2 bytes, write 1 byte per element).  One warp per row.  A
+// row of at most 4096 elements (16-byte aligned, K % 8 == 0) is read once into
+// registers -- all of its 16-byte loads in flight together -- its amax found by
+// a warp shuffle reduction, and its codes written from the registers, 8 per
+// 8-byte store.  Longer rows take two passes (amax, then a re-read from L1/L2
+// and the codes); rows that are not 16-byte aligned use scalar loads.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -26,6 +28,53 @@ constexpr int WARPS = 8;
 
 __device__ __forceinline__ uint16_t cvt2(float lo, float hi) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Rows held in registers: NV 16-byte chunks per lane (K <= NV * 256).
+template <int NV>
+__global__ void __launch_bounds__(WARPS * 32)
+quantize_rows_reg_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, float *__restrict__ scale, int M,
+                         int K) {
+    pdl_wait();  // dependents launch as this grid's CTAs exit (several CTAs per SM: no early trigger)
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (row >= M) return;
+    const __half *a = A + row * K;
+    uint8_t *q = Q + row * K;
+    uint4 v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int k = (i * 32 + lane) * 8;
+        v[i] = k < K ? __ldg(reinterpret_cast<const uint4 *>(a + k)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&v[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(h[j]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float inv = amax == 0.0f ? 0.0f : 448.0f / amax;  // a row of zeros: codes 0
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int k = (i * 32 + lane) * 8;
+        if (k >= K) break;
+        const __half2 *h = reinterpret_cast<const __half2 *>(&v[i]);
+        uint32_t w[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float2 f0 = __half22float2(h[2 * j]);
+            const float2 f1 = __half22float2(h[2 * j + 1]);
+            w[j] = (uint32_t)cvt2(f0.x * inv, f0.y * inv) | ((uint32_t)cvt2(f1.x * inv, f1.y * inv) << 16);
+        }
+        *reinterpret_cast<uint2 *>(q + k) = make_uint2(w[0], w[1]);
+    }
+    if (lane == 0) scale[row] = amax / 448.0f;
 }
 
 template <bool VEC>
@@ -41,6 +90,7 @@ quantize_rows_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, floa
 
     float amax = 0.0f;
     if (VEC) {
+#pragma unroll 4
         for (int k = lane * 8; k < K; k += 32 * 8) {
             const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a + k));
             const __half2 *h = reinterpret_cast<const __half2 *>(&u);
@@ -67,6 +117,7 @@ quantize_rows_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, floa
     }
     const float inv = 448.0f / amax;
     if (VEC) {
+#pragma unroll 4
         for (int k = lane * 8; k < K; k += 32 * 8) {
             const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a + k));
             const __half2 *h = reinterpret_cast<const __half2 *>(&u);
@@ -98,6 +149,7 @@ row_amax_kernel(const __half *__restrict__ A, float *__restrict__ amax_out, int 
     const __half *a = A + row * K;
     float amax = 0.0f;
     if (VEC) {
+#pragma unroll 4
         for (int k = lane * 8; k < K; k += 32 * 8) {
             const uint4 u = __ldg(reinterpret_cast<const uint4 *>(a + k));
             const __half2 *h = reinterpret_cast<const __half2 *>(&u);
@@ -128,9 +180,13 @@ cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int 
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(WARPS * 32), 0, s, attr);
-    if (quantize_rows_vec_ok(A, Q, K))
-        return launch_counted(&cfg, quantize_rows_kernel<true>, static_cast<const __half *>(A),
-                                  static_cast<uint8_t *>(Q), scale, M, K);
+    if (quantize_rows_vec_ok(A, Q, K)) {
+        const __half *a = static_cast<const __half *>(A);
+        uint8_t *q = static_cast<uint8_t *>(Q);
+        if (K <= 1024) return launch_counted(&cfg, quantize_rows_reg_kernel<4>, a, q, scale, M, K);
+        if (K <= 4096) return launch_counted(&cfg, quantize_rows_reg_kernel<16>, a, q, scale, M, K);
+        return launch_counted(&cfg, quantize_rows_kernel<true>, a, q, scale, M, K);
+    }
     return launch_counted(&cfg, quantize_rows_kernel<false>, static_cast<const __half *>(A),
                               static_cast<uint8_t *>(Q), scale, M, K);
 }
