@@ -18,7 +18,7 @@ std::atomic<unsigned long long> gemm_gb300::g_launches{0};
 
 namespace {
 
-enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma, UmmaStall, UmmaStallPair, UmmaStallPeer };
+enum class Family { Auto, Simt, SimtScalar, Gemv, GemvScalar, Umma, UmmaSkinnyWide, UmmaStall, UmmaStallPair, UmmaStallPeer };
 
 thread_local cudaStream_t t_stream = nullptr;
 thread_local const char *t_last_kernel = "none";
@@ -186,6 +186,10 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     case Family::Umma:
         if (!umma_supported(p)) return GEMM_ERR_INVALID_VALUE;
         return finish(launch_umma(p, dev->num_sms, dev->status, s), kernel_name("umma", elt));
+    case Family::UmmaSkinnyWide:
+        if (!skinny_wide_supported(p)) return GEMM_ERR_INVALID_VALUE;
+        return finish(launch_skinny_wide(p, dev->num_sms, dev->status, s),
+                      elt == Elt::BF16 ? "umma_skinny_wide_bf16" : "umma_skinny_wide_f16");
     case Family::UmmaStall:
         if (elt == Elt::F32) return GEMM_ERR_INVALID_VALUE;
         return finish(launch_umma_stall_test(p, dev->num_sms, dev->status, s), "umma_stall");
@@ -201,23 +205,15 @@ gemm_status_t run(const void *A, const void *B, void *C, int M, int N, int K, El
     }
 
     // Skinny M: the streaming GEMV for FP32 and for 16-bit problems the
-    // tensor-core kernels cannot take; other 16-bit problems with 2 <= M <= 8
-    // run on the tensor cores (the skinny kernel, weights as the MMA's rows),
-    // which stream B faster once more than one row of A multiplies it.  For
-    // M = 1 the skinny kernel is taken when its 128-column strips, times the K
-    // split it can use, occupy at least 80 % of the SMs, or when N <= 2048;
-    // otherwise the GEMV, whose many small CTAs fill the GPU.  Measured back to
-    // back (bf16, W from DRAM), skinny against GEMV: N = 4096, K = 12288 20.4
-    // vs 23.7 us; N = 18944, K = 3584 22.8 vs 26.4; N = 4096, K = 4096 9.1 vs
-    // 10.5; N = 1024, K = 4096 5.9 vs 8.3; N = 12288, K = 4096 (96 strips on
-    // 152 SMs) 20.0 vs 19.3.
-    bool m1_tensor = false;
-    if (M == 1 && elt != Elt::F32 && umma_supported(p) && (K % 8) == 0 && aligned16(A)) {
-        const long long strips = (N + 127) / 128, kb = (K + 127) / 128;
-        long long cs = 1;
-        while (cs < 8 && strips * (cs + 1) <= dev->num_sms && cs + 1 <= kb) ++cs;
-        m1_tensor = strips <= dev->num_sms && (strips <= 16 || strips * cs * 5 >= 4LL * dev->num_sms);
-    }
+    // tensor-core kernels cannot take; other 16-bit problems with M <= 8 run on
+    // the tensor cores (the skinny kernels, weights as the MMA's rows), which
+    // stream B faster -- for M = 1 too whenever the X rows suit TMA and the
+    // 256-column strips fit on the SMs at once.  Measured back to back (bf16, W
+    // from DRAM), skinny against GEMV, M = 1: N = 12288, K = 4096 17.7 vs
+    // 18.8 us; N = 4096, K = 12288 19.1 vs 22.2; N = 1024, K = 4096 5.5 vs 7.3;
+    // N = 28672, K = 4096 38.1 vs 48.6.
+    const bool m1_tensor = M == 1 && elt != Elt::F32 && umma_supported(p) && (K % 8) == 0 && aligned16(A) &&
+                           (N + 255) / 256 <= dev->num_sms;
     if (M <= kGemvMaxM && (elt == Elt::F32 || (M == 1 && !m1_tensor) || !umma_supported(p)))
         return gemv_vec_ok ? finish(launch_gemv(p, true, dev->num_sms, s), kernel_name("gemv", elt))
                            : finish(launch_gemv(p, false, dev->num_sms, s), kernel_name("gemv_scalar", elt));
@@ -609,6 +605,7 @@ GEMM_API gemm_status_t gemm_force_kernel(const char *family) {
     else if (!strcmp(family, "gemv")) t_force = Family::Gemv;
     else if (!strcmp(family, "gemv_scalar")) t_force = Family::GemvScalar;
     else if (!strcmp(family, "umma")) t_force = Family::Umma;
+    else if (!strcmp(family, "umma_skinny_wide")) t_force = Family::UmmaSkinnyWide;
     else if (!strcmp(family, "umma_stall")) t_force = Family::UmmaStall;
     else if (!strcmp(family, "umma_stall_pair")) t_force = Family::UmmaStallPair;
     else if (!strcmp(family, "umma_stall_peer")) t_force = Family::UmmaStallPeer;

@@ -16,10 +16,14 @@ namespace gemm_gb300 {
 // Programmatic dependent launch.  Every kernel is launched with programmatic
 // stream serialisation allowed: it may start while the previous kernel on the
 // stream drains.  After a prologue that touches only its shared memory, tensor
-// memory and parameters it waits for the previous grid to complete and its
-// writes to become visible (pdl_wait) before its first global-memory access.
+// memory and parameters -- the skinny kernels add L2 prefetch hints for their
+// first weight tiles, which read nothing and change no value a later load
+// returns -- it waits for the previous grid to complete and its writes to
+// become visible (pdl_wait) before its first global-memory access.
 // The tensor-core kernels (one CTA per SM) also let their own dependents launch
-// at once (pdl_launch_dependents); kernels with several CTAs per SM leave that
+// at once (pdl_launch_dependents) -- the skinny ones once every CTA has issued
+// its last load, so that the dependent's CTAs prefetch their first weights
+// into L2 while this grid drains; kernels with several CTAs per SM leave that
 // to their CTAs' exit, so that a small grid's successor is not placed, and
 // packed onto the same SMs, while the grid still runs (FP32 1000^3: 86 against
 // 49 us).  The one exception is the first grid of an FP32 problem split in two,
@@ -123,6 +127,13 @@ cudaError_t launch_gemv(const Problem &p, bool vec, int num_sms, cudaStream_t s)
 // stream-ordered scratch (cudaMallocAsync); without it they use cp.async.
 cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t s, bool may_allocate = true);
 bool umma_supported(const Problem &p);
+
+// Skinny 16-bit GEMM (1 <= M <= 64) on 256-column strips of B, K split over a
+// cluster of up to 8 CTAs (see skinny_wide.cu).  Needs A and B 16-byte
+// aligned, C 8-byte aligned, K % 8 == 0 and N % 8 == 0 (cudaErrorNotSupported
+// otherwise, before any launch).  status: device word for timeout codes.
+bool skinny_wide_supported(const Problem &p);
+cudaError_t launch_skinny_wide(const Problem &p, int num_sms, int *status, cudaStream_t s);
 
 // The general form on the tensor-core CTA pairs (16-bit only).  Needs A, B, C
 // 16-byte aligned, every leading dimension (and, for batch > 1, every nonzero

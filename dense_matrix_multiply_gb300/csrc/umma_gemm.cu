@@ -162,6 +162,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+// Asks for the tile at (x, y) of a 2-D tensor map to be brought into L2 (a
+// hint: no shared memory, no barrier, no effect on what later loads return).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -1418,7 +1426,19 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
-    pdl_launch_dependents();
+    if (warp == 0 && lane == 0 && g_pdl) {
+        // While the previous kernel on the stream finishes, the strip's first
+        // ring-full of W is requested into L2, so that the weight stream does
+        // not start from cold DRAM latency after this grid's wait.  A prefetch
+        // is only a hint -- it changes no value that a later load returns --
+        // so it is correct whatever that kernel writes; X is left alone, since
+        // it is usually that kernel's output.
+        const int n_left = N - n0;
+        const int wboxes = n_left >= 128 ? 2 : (n_left + 63) / 64;
+        const int pf = min(kb1 - kb0, stages);
+        for (int kb = kb0; kb < kb0 + pf; ++kb)
+            for (int j = 0; j < wboxes; ++j) tma_prefetch_l2_2d(&tmW, n0 + 64 * j, kb * SKB);
+    }
     pdl_wait();  // the previous kernel's writes are visible from here on
 
     if (warp == 0 && lane == 0) {
@@ -1444,6 +1464,15 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             ++issued;
             if (++stage == stages) { stage = 0; phase ^= 1u; }
         }
+        // The dependent grid may launch once every CTA has issued its last load:
+        // its CTAs then take the idle SMs and prefetch their first W stages
+        // while this grid's last stages drain, rather than competing with its
+        // full-rate stream (N = 12288, K = 4096, back to back, W from DRAM,
+        // M = 1 / 8 / 32 / 64: 17.7 / 17.9 / 18.9 / 21.3 us, against 18.7 /
+        // 19.0 / 20.0 / 22.5 with the launch released at the start and no
+        // prefetch, and 20.0 / 20.1 / 20.3 / 22.4 with the prefetch but the
+        // launch released at the start).
+        pdl_launch_dependents();
         // Let every load this thread issued land before the stages are reused.
         for (long long i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
             const int s = (int)(i % stages);
@@ -2091,6 +2120,13 @@ cudaError_t launch_umma(const Problem &p, int num_sms, int *status, cudaStream_t
             return p.elt == Elt::BF16 ? launch_skinny_typed<__nv_bfloat16, 1>(p, cs, num_sms, status, s)
                                       : launch_skinny_typed<__half, 0>(p, cs, num_sms, status, s);
         }
+        // More 128-column strips than SMs: 256-column strips (skinny_wide.cu),
+        // one CTA each while they fit on the SMs at once.  N = 28672, K = 4096,
+        // back to back, W from DRAM: M = 1 / 8 / 32 / 64 at 37.9 / 38.6 / 39.6 /
+        // 41.0 us, against 48.9 (the GEMV) / 57.4 / 38.7 / 39.7 for the
+        // single-CTA 128 x 256 tiles.
+        if ((p.N + 255) / 256 <= num_sms && skinny_wide_supported(p))
+            return launch_skinny_wide(p, num_sms, status, s);
     }
     // 256-row tiles on CTA pairs once M fills more than one 128-row tile.
     if (p.M > BM) {

@@ -290,8 +290,9 @@ GEMM_API unsigned long long gemm_kernel_launches(void);
 GEMM_API const char *gemm_last_error(void);
 
 /* Test and benchmark hook: forces the calling thread's later calls onto one
- * kernel family -- "simt", "simt_scalar", "gemv", "gemv_scalar", "umma" -- or
- * back to automatic dispatch with NULL or "".  A forced family that cannot run
+ * kernel family -- "simt", "simt_scalar", "gemv", "gemv_scalar", "umma",
+ * "umma_skinny_wide" (16-bit, M <= 64: the skinny tensor-core kernel on
+ * 256-column strips of B) -- or back to automatic dispatch with NULL or "".  A forced family that cannot run
  * a given problem makes that call return GEMM_ERR_INVALID_VALUE; an unknown
  * name is rejected here with GEMM_ERR_INVALID_VALUE.
  * "umma_stall" tests the tensor-core kernel's bounded waits: a 16-bit call whose

@@ -69,7 +69,7 @@ def test_status_strings(built):
 
 
 def test_force_kernel_names(built):
-    for fam in ("simt", "simt_scalar", "gemv", "gemv_scalar", "umma", "umma_stall", "umma_stall_pair", "umma_stall_peer", None, ""):
+    for fam in ("simt", "simt_scalar", "gemv", "gemv_scalar", "umma", "umma_skinny_wide", "umma_stall", "umma_stall_pair", "umma_stall_peer", None, ""):
         g.gemm_force_kernel(fam)
     with pytest.raises(g.GemmError):
         g.gemm_force_kernel("cpu")

@@ -73,8 +73,10 @@ def test_A_beyond_2_31_elements(dtype, M, N, K, expect):
     del dA, dB, dC
 
 
-def test_decode_weights_beyond_2_31_elements():
-    """M = 1 with W [65536, 32800] bf16 (2.15e9 elements): the GEMV path."""
+@pytest.mark.parametrize("force,expect", [(None, "umma_bf16"), ("gemv", "gemv_bf16")])
+def test_decode_weights_beyond_2_31_elements(force, expect):
+    """M = 1 with W [65536, 32800] bf16 (2.15e9 elements): the 256-column skinny
+    tensor-core kernel (129 strips) and the GEMV."""
     M, N, K = 1, 32800, 65536
     assert K * N > 2 ** 31
     x = synthetic.matrix("bf16", 1, K, synthetic.seed_for(CFG, 3))
@@ -82,8 +84,12 @@ def test_decode_weights_beyond_2_31_elements():
     dW = tiled_rows(wblk, K, N, "bf16")
     dx = torch.from_numpy(x.view(np.int16)).cuda()
     dc = torch.empty(N, dtype=torch.int16, device="cuda")
-    g.gemm_bf16_rm(dx, dW, dc, M, N, K)
-    assert g.gemm_last_kernel().startswith("gemv_bf16")
+    g.gemm_force_kernel(force)
+    try:
+        g.gemm_bf16_rm(dx, dW, dc, M, N, K)
+        assert g.gemm_last_kernel().startswith(expect)
+    finally:
+        g.gemm_force_kernel(None)
     g.gemm_synchronize()
     c = widen("bf16", dc)
     cols = np.array([0, 1, 1023, 16384, N - 2, N - 1])

@@ -123,7 +123,9 @@ MID_CASES = [
     ("f16_cm", 1000, 8, 1000, None, "umma_f16"),
     ("bf16_rm", 1, 1024, 512, "umma", "umma_bf16"),          # skinny M = 1: 8 strips x 4 ranks
     ("bf16_rm", 1, 4096, 1024, None, "umma_bf16"),           # M = 1, 32 strips x 4: the skinny kernel
-    ("bf16_rm", 1, 12288, 512, None, "gemv_bf16_vec"),       # M = 1, 96 strips alone: the GEMV
+    ("bf16_rm", 1, 12288, 512, None, "umma_bf16"),           # M = 1, 96 strips: the skinny kernel
+    ("bf16_rm", 1, 12288, 512, "gemv", "gemv_bf16_vec"),     # the same on the GEMV
+    ("bf16_rm", 1, 20480, 520, None, "umma_bf16"),           # 160 strips > SMs: 80 strips of 256 columns
     ("f16_cm", 2048, 1, 768, None, "umma_f16"),              # row-major M = 1 through the swap
     ("bf16_rm", 2, 264, 128, None, "umma_bf16"),             # 3 strips (the last one 8 columns)
     ("bf16_rm", 64, 2048, 4096, None, "umma_bf16"),          # 16 strips on clusters, M = 64
