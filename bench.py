@@ -52,11 +52,13 @@ DEFAULT_WORKLOAD = "sgemm_f32_rm_4096"
 # The other workloads measured in the default run ("paths"): every other
 # configuration of the five (the FP16 and BF16 tensor-core problems and the
 # whole ragged/edge sweep on both the FP32 and the BF16 path, the K = 4100 tail
-# beside its K = 4096 control), then the fused, general-form and FP8 workloads.
+# beside its K = 4096 control), a decode batch with more 128-column weight
+# strips than SMs, then the fused, general-form and FP8 workloads.
 DEFAULT_PATHS = ["hgemm_f16_cm_8192", "hgemm_f16_cm_3072x5120x6144", "ffn_bf16_rm_1024x12288x4096",
                  "sgemm_f32_rm_256",
                  "edge_f32_rm_1000x1000x1000", "edge_bf16_rm_1000x1000x1000",
                  "edge_bf16_rm_1x12288x4096", "edge_f32_rm_1x12288x4096", "edge_bf16_rm_32x12288x4096",
+                 "decode_bf16_rm_8x28672x4096",
                  "edge_f32_rm_64x64x64", "edge_bf16_rm_64x64x64",
                  "edge_bf16_rm_8192x4096x4100", "edge_bf16_rm_8192x4096x4096",
                  "edge_f32_rm_8192x4096x4100", "edge_f32_rm_8192x4096x4096",
@@ -81,20 +83,39 @@ L2_BYTES = 129e6
 # the kernels the call launches, the fix-up of a stream-K call excepted) from one
 # ncu capture, keyed by workload; valid only while the kernel's source is the one
 # captured (sha256 prefix of the .cu file's code, comments and blank lines
-# removed), else reported as null.
+# removed: the family's file, or "file" where the kernel lives elsewhere), else
+# reported as null.
 TRAFFIC = {
-    # both grids of the call: the whole rounds (304.2 + 51.4 MB) and the half-K last round (46.2 + 1.2 MB)
-    "sgemm_f32_rm_4096": {"bytes": 304213248 + 51446528 + 46163712 + 1196544, "source": "eced23f8e828"},
-    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 331792384 + 56420608, "source": "eced23f8e828"},
-    "hgemm_f16_cm_8192": {"bytes": 1046693632 + 125557248, "source": "7fc1ab5c13f8"},
-    # the CTA-pair kernel of a stream-K call (its fix-up kernel adds 12.6 MB of reads)
-    "hgemm_f16_cm_3072x5120x6144": {"bytes": 183561472 + 22897408, "source": "7fc1ab5c13f8"},
-    "ffn_bf16_rm_1024x12288x4096": {"bytes": 110036736 + 11962624, "source": "7fc1ab5c13f8"},
-    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 211854336 + 18776064, "source": "7fc1ab5c13f8"},
-    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1065488896 + 124942848, "source": "7fc1ab5c13f8"},
-    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120640 + 0, "source": "7fc1ab5c13f8"},
-    "edge_bf16_rm_1x12288x4096": {"bytes": 100693760 + 3052544, "source": "a821897d27f4"},
-    "edge_bf16_rm_32x12288x4096": {"bytes": 100961024 + 3403776, "source": "7fc1ab5c13f8"},
+    "decode_bf16_rm_8x28672x4096": {"bytes": 238177024, "source": "58dc7414ad7d", "file": "skinny_wide.cu"},
+    "edge_bf16_rm_1000x1000x1000": {"bytes": 4047104, "source": "66c8e97e68f1"},
+    "edge_bf16_rm_1x12288x4096": {"bytes": 103623680, "source": "66c8e97e68f1"},
+    "edge_bf16_rm_32x12288x4096": {"bytes": 103879680, "source": "66c8e97e68f1"},
+    "edge_bf16_rm_64x64x64": {"bytes": 55296, "source": "66c8e97e68f1"},
+    "edge_bf16_rm_8192x4096x4096": {"bytes": 205569280, "source": "66c8e97e68f1"},
+    # the A rows staged into aligned rows (pad_rows_kernel), then the CTA pairs
+    "edge_bf16_rm_8192x4096x4100": {"bytes": 87306752 + 201608192, "source": "66c8e97e68f1"},
+    "edge_f32_rm_1000x1000x1000": {"bytes": 8025856, "source": "308e43d5575f"},
+    "edge_f32_rm_1x12288x4096": {"bytes": 204522240, "source": "a821897d27f4"},
+    "edge_f32_rm_64x64x64": {"bytes": 51968, "source": "308e43d5575f"},
+    "edge_f32_rm_8192x4096x4096": {"bytes": 788443136, "source": "308e43d5575f"},
+    "edge_f32_rm_8192x4096x4100": {"bytes": 790477056, "source": "308e43d5575f"},
+    "ffn_bf16_rm_1024x12288x4096": {"bytes": 121902592, "source": "66c8e97e68f1"},
+    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 230424832, "source": "66c8e97e68f1"},  # the fix-up kernel adds 4.2 MB
+    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120640, "source": "66c8e97e68f1"},  # the quantiser moves 33.6 MB
+    "fp8_rowscale_e4m3_8192x8192x8192": {"bytes": 458721792, "source": "66c8e97e68f1"},  # the quantiser moves 279.1 MB
+    "fp8_rowscale_fused_e4m3_4096x1536x4096": {"bytes": 33560064 + 39922688, "source": "66c8e97e68f1"},  # the row amax pass, then the product
+    "fp8_rowscale_fused_e4m3_8192x8192x8192": {"bytes": 137384704 + 744140544, "source": "66c8e97e68f1"},  # the row amax pass, then the product
+    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1204170496, "source": "66c8e97e68f1"},
+    "gemm_ex_f16_rm_NN_batch32_1024x1024x1024": {"bytes": 173609216, "source": "66c8e97e68f1"},
+    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 386299392, "source": "308e43d5575f"},
+    "gemv_bf16_rm_1x12288x4100": {"bytes": 103612672, "source": "a821897d27f4"},
+    "hgemm_f16_cm_3072x5120x6144": {"bytes": 204261888, "source": "66c8e97e68f1"},  # the fix-up kernel adds 12.6 MB
+    "hgemm_f16_cm_8192": {"bytes": 1188005888, "source": "66c8e97e68f1"},
+    "sgemm_f32_rm_256": {"bytes": 543488, "source": "308e43d5575f"},
+    # both grids of the call: the whole rounds and the half-K last round
+    "sgemm_f32_rm_4096": {"bytes": 351713024 + 46196480, "source": "308e43d5575f"},
+    "single_cta_bf16_rm_128x12288x4096": {"bytes": 104824064, "source": "66c8e97e68f1"},
+    "unaligned_f32_rm_4096x4096x4095": {"bytes": 384833280, "source": "308e43d5575f"},
 }
 
 KERNEL_SOURCE = {
@@ -118,6 +139,13 @@ def all_workloads():
                                                                          1.0, "uniform", 1.0))
     out["unaligned_f32_rm_4096x4096x4095"] = (synthetic.EDGE_CONFIG_ID, ("f32_rm", 4096, 4096, 4095, "uniform", 1.0,
                                                                        "uniform", 1.0))
+    # a decode batch whose 128-column strips outnumber the SMs (the 256-column
+    # skinny kernel), and the GEMV's bf16 instance (A rows of 8200 bytes, which
+    # TMA cannot describe, keep M = 1 off the tensor cores)
+    out["decode_bf16_rm_8x28672x4096"] = (synthetic.EDGE_CONFIG_ID, ("bf16_rm", 8, 28672, 4096, "uniform", 1.0,
+                                                                   "uniform", 1.0))
+    out["gemv_bf16_rm_1x12288x4100"] = (synthetic.EDGE_CONFIG_ID, ("bf16_rm", 1, 12288, 4100, "uniform", 1.0,
+                                                                 "uniform", 1.0))
     # the FFN gate/up projection with its SiLU * U epilogue fused (two GEMMs)
     out["ffn_gate_up_bf16_silu_mul_1024x12288x4096"] = (3, ("bf16_silu_mul", 1024, 12288, 4096, "normal", 1.0,
                                                              "normal", 1.0 / 64.0))
@@ -188,11 +216,16 @@ def code_text(src: str) -> str:
     return "\n".join(line.strip() for line in "".join(out).splitlines() if line.strip())
 
 
-def source_hash(kind: str) -> str:
+def file_hash(name: str) -> str:
     """sha256 prefix of a kernel file's code (comments and blank lines removed)."""
-    path = os.path.join(ROOT, "dense_matrix_multiply_gb300", "csrc", KERNEL_SOURCE[kind])
+    path = os.path.join(ROOT, "dense_matrix_multiply_gb300", "csrc", name)
     with open(path, encoding="utf-8") as f:
         return hashlib.sha256(code_text(f.read()).encode()).hexdigest()[:12]
+
+
+def source_hash(kind: str) -> str:
+    """Code hash of the file that holds a kernel family."""
+    return file_hash(KERNEL_SOURCE[kind])
 
 
 # ------------------------------------------------------------------ clocks
@@ -302,7 +335,9 @@ def roofline_for(kind: str, variant: str, M, N, K, seconds_per_launch: float, pe
         algo_bytes = metrics.min_bytes(M, N, K, es)
     tr = TRAFFIC.get(workload)
     traffic = None
-    if tr and tr.get("source") == source_hash(kind if kind in KERNEL_SOURCE else "simt"):
+    src_file = tr.get("file") if tr else None
+    if tr and tr.get("source") == (file_hash(src_file) if src_file else
+                                   source_hash(kind if kind in KERNEL_SOURCE else "simt")):
         traffic = tr["bytes"]
     if kind == "gemv":
         achieved = algo_bytes / seconds_per_launch / 1e9
