@@ -89,7 +89,9 @@ def check_chain(dtype, M, dims, x, ws, outs):
 
 CHAINS = [
     ("bf16", 8, [1024, 4096, 2048, 12288, 1024], "skinny kernel (strips alone and on clusters)"),
-    ("bf16", 1, [4096, 4096, 12288, 1024], "GEMV"),
+    ("bf16", 1, [4096, 4096, 12288, 1024], "skinny kernel at M = 1"),
+    ("bf16", 8, [1024, 20480, 4096, 20480, 512], "256-column skinny kernel (160 strips) between 128-column ones"),
+    ("bf16", 1, [4100, 4096, 1024], "GEMV (X rows of 8200 bytes), then the skinny kernel"),
     ("bf16", 2048, [3072, 2560, 3072, 2560], "CTA pairs, stream-K tail on the 2560-wide stages"),
     ("bf16", 512, [1024, 2048, 520, 1024], "CTA pairs, ragged N then ragged K"),
     ("f32", 256, [512, 1024, 256, 768], "packed-FMA SIMT kernel"),
@@ -113,7 +115,7 @@ def test_chain_captured_in_a_cuda_graph():
     stream-K tail becomes graph memory nodes; the SGEMM's split last round a
     programmatic edge to a cluster launch) and replayed twice: the results equal
     the eager ones bit for bit."""
-    cases = [CHAINS[0], CHAINS[2], CHAINS[4], CHAINS[6]]
+    cases = [CHAINS[0], CHAINS[2], CHAINS[4], CHAINS[6], CHAINS[8]]
     eager, staged = [], []
     for case in cases:
         dtype, M, dims, _ = case
