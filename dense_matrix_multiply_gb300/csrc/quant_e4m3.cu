@@ -14,8 +14,10 @@
 // row of at most 4096 elements (16-byte aligned, K % 8 == 0) is read once into
 // registers -- all of its 16-byte loads in flight together -- its amax found by
 // a warp shuffle reduction, and its codes written from the registers, 8 per
-// 8-byte store.  Longer rows take two passes (amax, then a re-read from L1/L2
-// and the codes); rows that are not 16-byte aligned use scalar loads.  Four
+// 8-byte store; a row of up to 8192 elements is held the same way by two warps,
+// which combine their amax through shared memory.  Longer rows take two passes
+// (amax, then a re-read from L1/L2 and the codes); rows that are not 16-byte
+// aligned use scalar loads.  Four
 // warps per CTA: a row held in registers takes 143 per thread, so CTAs of eight
 // warps ran one per SM and CTAs of four run three (12 rows in flight per SM):
 // A [4096, 4096] in 9.9 us against 11.5 us with eight warps and 10.4 us for
@@ -35,22 +37,30 @@ __device__ __forceinline__ uint16_t cvt2(float lo, float hi) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Rows held in registers: NV 16-byte chunks per lane (K <= NV * 256).
-template <int NV>
+// Rows held in registers: NV 16-byte chunks per lane, WPR warps per row (warp
+// part p holds elements [p NV 256, (p + 1) NV 256) of its row; K <= WPR NV 256).
+// With two warps per row their amax values meet in shared memory; the largest
+// magnitude does not depend on the order it is found in, so the codes are the
+// one-warp kernel's.
+template <int NV, int WPR>
 __global__ void __launch_bounds__(WARPS * 32)
 quantize_rows_reg_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, float *__restrict__ scale, int M,
                          int K) {
+    static_assert(WARPS % WPR == 0, "whole rows per CTA");
     pdl_wait();  // dependents launch as this grid's CTAs exit (several CTAs per SM: no early trigger)
-    const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
-    if (row >= M) return;
-    const __half *a = A + row * K;
-    uint8_t *q = Q + row * K;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long row = (long long)blockIdx.x * (WARPS / WPR) + warp / WPR;
+    const int part = warp % WPR;
+    const bool valid = row < M;
+    if (WPR == 1 && !valid) return;
+    const __half *a = A + (valid ? row : 0) * K;
+    uint8_t *q = Q + (valid ? row : 0) * K;
+    const int kbase = part * NV * 256;
     uint4 v[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-        const int k = (i * 32 + lane) * 8;
-        v[i] = k < K ? __ldg(reinterpret_cast<const uint4 *>(a + k)) : make_uint4(0u, 0u, 0u, 0u);
+        const int k = kbase + (i * 32 + lane) * 8;
+        v[i] = valid && k < K ? __ldg(reinterpret_cast<const uint4 *>(a + k)) : make_uint4(0u, 0u, 0u, 0u);
     }
     float amax = 0.0f;
 #pragma unroll
@@ -64,10 +74,18 @@ quantize_rows_reg_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, 
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if constexpr (WPR > 1) {
+        __shared__ float part_amax[WARPS];
+        if (lane == 0) part_amax[warp] = amax;
+        __syncthreads();
+#pragma unroll
+        for (int p = 0; p < WPR; ++p) amax = fmaxf(amax, part_amax[warp - part + p]);
+        if (!valid) return;
+    }
     const float inv = amax == 0.0f ? 0.0f : 448.0f / amax;  // a row of zeros: codes 0
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-        const int k = (i * 32 + lane) * 8;
+        const int k = kbase + (i * 32 + lane) * 8;
         if (k >= K) break;
         const __half2 *h = reinterpret_cast<const __half2 *>(&v[i]);
         uint32_t w[2];
@@ -79,7 +97,7 @@ quantize_rows_reg_kernel(const __half *__restrict__ A, uint8_t *__restrict__ Q, 
         }
         *reinterpret_cast<uint2 *>(q + k) = make_uint2(w[0], w[1]);
     }
-    if (lane == 0) scale[row] = amax / 448.0f;
+    if (lane == 0 && part == 0) scale[row] = amax / 448.0f;
 }
 
 template <bool VEC>
@@ -188,8 +206,16 @@ cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int 
     if (quantize_rows_vec_ok(A, Q, K)) {
         const __half *a = static_cast<const __half *>(A);
         uint8_t *q = static_cast<uint8_t *>(Q);
-        if (K <= 1024) return launch_counted(&cfg, quantize_rows_reg_kernel<4>, a, q, scale, M, K);
-        if (K <= 4096) return launch_counted(&cfg, quantize_rows_reg_kernel<16>, a, q, scale, M, K);
+        if (K <= 1024) return launch_counted(&cfg, quantize_rows_reg_kernel<4, 1>, a, q, scale, M, K);
+        if (K <= 4096) return launch_counted(&cfg, quantize_rows_reg_kernel<16, 1>, a, q, scale, M, K);
+        if (K <= 8192) {
+            // two warps per row: half as many rows per CTA
+            const long long blocks2 = ((long long)M + WARPS / 2 - 1) / (WARPS / 2);
+            if (blocks2 > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+            cudaLaunchAttribute attr2[1];
+            const cudaLaunchConfig_t cfg2 = pdl_config(dim3((unsigned)blocks2), dim3(WARPS * 32), 0, s, attr2);
+            return launch_counted(&cfg2, quantize_rows_reg_kernel<16, 2>, a, q, scale, M, K);
+        }
         return launch_counted(&cfg, quantize_rows_kernel<true>, a, q, scale, M, K);
     }
     return launch_counted(&cfg, quantize_rows_kernel<false>, static_cast<const __half *>(A),

@@ -60,7 +60,10 @@ def quantize_gpu(A, M, K, a_off=0, q_off=0):
     (64, 4096, 0, 0, "quantize_e4m3_vec"), (37, 304, 0, 0, "quantize_e4m3_vec"),
     (37, 300, 0, 0, "quantize_e4m3_scalar"), (5, 4096, 1, 0, "quantize_e4m3_scalar"),
     (9, 64, 0, 3, "quantize_e4m3_scalar"), (1, 8, 0, 0, "quantize_e4m3_vec"), (300, 1000, 0, 0, "quantize_e4m3_vec"),
-    (12, 8200, 0, 0, "quantize_e4m3_vec"), (20, 2056, 0, 0, "quantize_e4m3_vec")])  # K > 4096: two passes over A; else rows held in registers
+    (12, 8200, 0, 0, "quantize_e4m3_vec"), (20, 2056, 0, 0, "quantize_e4m3_vec"),
+    (7, 5000, 0, 0, "quantize_e4m3_vec"), (33, 8192, 0, 0, "quantize_e4m3_vec")])
+# K > 8192: two passes over A; K > 4096: a row held by two warps (M = 7: a CTA
+# with one row past M); else a row held by one warp
 def test_quantize_rows_bit_exact(M, K, a_off, q_off, expect):
     A = half_rows(M, K, 1)
     if M > 6:

@@ -45,6 +45,7 @@ SHAPES = [
     (300, 520, 264, "same kernel"),
     (256, 512, 100, "same kernel"),
     (32, 4096, 4096, "skinny kernel"),
+    (8, 20480, 1024, "256-column skinny kernel (strips past the SM count)"),
     (1024, 2048, 1028, "stages A into aligned rows (K % 8 = 4)"),
     (1024, 12288, 4096, "same kernel (the FFN projection)"),
     (3072, 5120, 6144, "adds a stream-K tail and its fix-up kernel"),
