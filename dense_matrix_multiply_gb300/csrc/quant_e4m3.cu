@@ -10,19 +10,19 @@
 // ones an FP32 evaluation of these steps gives.  A row of zeros gives q = 0 and
 // scale 0.
 //
-// Bound: HBM (read 2 bytes, write 1 byte per element).  One warp per row.  A
-// row of at most 4096 elements (16-byte aligned, K % 8 == 0) is read once into
-// registers -- all of its 16-byte loads in flight together -- its amax found by
-// a warp shuffle reduction, and its codes written from the registers, 8 per
-// 8-byte store; a row of up to 8192 elements is held the same way by two warps,
-// which combine their amax through shared memory.  Longer rows take two passes
-// (amax, then a re-read from L1/L2 and the codes); rows that are not 16-byte
-// aligned use scalar loads.  Four
-// warps per CTA: a row held in registers takes 143 per thread, so CTAs of eight
-// warps ran one per SM and CTAs of four run three (12 rows in flight per SM):
-// A [4096, 4096] in 9.9 us against 11.5 us with eight warps and 10.4 us for
-// the two-pass kernel, [16384, 4096] in 30.7 against 35.3 and 34.2 us (back to
-// back, A read from DRAM).
+// Bound: HBM (read 2 bytes, write 1 byte per element).  A row (16-byte aligned,
+// K % 8 == 0) is read once into registers -- all of its 16-byte loads in flight
+// together -- its amax found by warp shuffles and, where several warps hold the
+// row, through shared memory, and its codes written from the registers, 8 per
+// 8-byte store: one warp per row up to 1024 elements, four warps (1024
+// elements each, 54 registers per thread) up to 4096, two warps (4096 each, 143
+// registers) up to 8192.  Longer rows take two passes (amax, then a re-read from
+// L1/L2 and the codes); rows that are not 16-byte aligned use scalar loads.
+// CTAs of four warps.  Measured back to back with A read from DRAM, A [4096,
+// 4096]: 9.0 us with four warps per row, 9.3 with two, 10.0 with one (143
+// registers: three CTAs per SM), 11.5 with one warp per row in CTAs of eight
+// warps (one CTA per SM), 10.4 for the two-pass kernel; [16384, 4096] 29.4 us;
+// [8192, 8192] 30.9 us against 52.3 for the two-pass kernel.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -206,16 +206,17 @@ cudaError_t launch_quantize_rows_e4m3(const void *A, void *Q, float *scale, int 
     if (quantize_rows_vec_ok(A, Q, K)) {
         const __half *a = static_cast<const __half *>(A);
         uint8_t *q = static_cast<uint8_t *>(Q);
-        if (K <= 1024) return launch_counted(&cfg, quantize_rows_reg_kernel<4, 1>, a, q, scale, M, K);
-        if (K <= 4096) return launch_counted(&cfg, quantize_rows_reg_kernel<16, 1>, a, q, scale, M, K);
-        if (K <= 8192) {
-            // two warps per row: half as many rows per CTA
-            const long long blocks2 = ((long long)M + WARPS / 2 - 1) / (WARPS / 2);
+        // WPR warps per row: WARPS / WPR rows per CTA
+        auto launch_reg = [&](auto kern, int wpr) {
+            const long long blocks2 = ((long long)M + WARPS / wpr - 1) / (WARPS / wpr);
             if (blocks2 > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
             cudaLaunchAttribute attr2[1];
             const cudaLaunchConfig_t cfg2 = pdl_config(dim3((unsigned)blocks2), dim3(WARPS * 32), 0, s, attr2);
-            return launch_counted(&cfg2, quantize_rows_reg_kernel<16, 2>, a, q, scale, M, K);
-        }
+            return launch_counted(&cfg2, kern, a, q, scale, M, K);
+        };
+        if (K <= 1024) return launch_reg(quantize_rows_reg_kernel<4, 1>, 1);
+        if (K <= 4096) return launch_reg(quantize_rows_reg_kernel<4, 4>, 4);
+        if (K <= 8192) return launch_reg(quantize_rows_reg_kernel<16, 2>, 2);
         return launch_counted(&cfg, quantize_rows_kernel<true>, a, q, scale, M, K);
     }
     return launch_counted(&cfg, quantize_rows_kernel<false>, static_cast<const __half *>(A),
