@@ -1816,6 +1816,19 @@ bool sk_worth(long long tiles, int clusters, long long num_kb) {
     return rem > 0 && rem * 4 <= clusters && num_kb >= 48;
 }
 
+// Whether a problem of T tiles (256 wide) of KB K-blocks runs as stream-K over
+// all of its tiles, four clusters per tile: the tiles would occupy at most a
+// quarter of the G co-resident clusters and K is long (KB >= 64), so that the
+// spread pays for the partials and the fix-up kernel.  Measured back to back on
+// GB300, bf16, against whole tiles: 512 x 512 x 8192 and 256 x 1024 x 8192
+// 21.4 against 40.5 us, 768 x 768 x 4096 18.8 against 22.9, 1024 x 1024 x 4096
+// 22.4 against 23.1; where it is not taken it lost: 1024 x 2048 x 6144 (32
+// tiles) 34.7 against 32.4, 1000 x 1000 x 3072 (48 K-blocks) 20.8 against
+// 19.3, 1000^3 (16 K-blocks) 18.3 against 11.4.
+bool sk_small(long long tiles, int clusters_max, long long num_kb) {
+    return g_pair_sk && g_pdl && tiles > 0 && tiles * 4 <= clusters_max && num_kb >= 64;
+}
+
 // Launch with a stream-K tail when sk_worth: the last rem tiles' K iterations
 // are spread over the G_sk = min(G, 4 rem) highest clusters,
 // W = ceil(rem * KB / G_sk) each, instead of leaving G - rem clusters idle for
@@ -1826,8 +1839,33 @@ bool sk_worth(long long tiles, int clusters, long long num_kb) {
 template <typename T, uint32_t F, bool DUAL = false, bool F8 = false>
 cudaError_t launch_pair_planned(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                                 const CUtensorMap &tb2, PairArgs args, int clusters, long long tiles, bool allow_sk,
-                                cudaStream_t s) {
+                                cudaStream_t s, int small_clusters = 0) {
     const long long num_kb = (args.K + (F8 ? 128 : BK) - 1) / (F8 ? 128 : BK);
+    if (allow_sk && small_clusters > 0) {
+        // every tile's K iterations in equal shares over 4 clusters per tile;
+        // the fix-up kernel adds the partials
+        const long long g_sk = std::min<long long>(small_clusters, 4 * tiles);
+        const long long w = (tiles * num_kb + g_sk - 1) / g_sk;
+        const size_t ws_bytes = (size_t)g_sk * 2 * 8 * 256 * 32 * sizeof(float);
+        void *buf = nullptr;
+        if (cudaMallocAsync(&buf, ws_bytes, s) == cudaSuccess) {
+            args.sk_ws = static_cast<float *>(buf);
+            args.sk_tiles = (int)tiles;
+            args.sk_w = (int)w;
+            args.sk_first = 0;
+            cudaError_t e = launch_pair_cfg<T, F, DUAL, F8>(ta, tb, tc, tb2, args, (int)g_sk, s);
+            if (e == cudaSuccess) {
+                cudaLaunchAttribute fa[1];
+                const cudaLaunchConfig_t fc =
+                    pdl_config(dim3((unsigned)(2 * tiles), (unsigned)(args.bn / 8), 1), dim3(128), 0, s, fa);
+                e = launch_counted(&fc, pair_sk_fixup_kernel<T, DUAL, F8>, static_cast<const PairArgs>(args),
+                                   (int)num_kb);
+            }
+            const cudaError_t f = cudaFreeAsync(buf, s);
+            return e != cudaSuccess ? e : f;
+        }
+        cudaGetLastError();
+    }
     const long long rem = clusters > 0 ? tiles % clusters : 0;
     if (allow_sk && sk_worth(tiles, clusters, num_kb)) {
         const long long g_sk = std::min<long long>(clusters, 4 * rem);
@@ -1876,7 +1914,9 @@ cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status,
     // with the tile's N.
     const long long tiles_mb = (long long)((p.M + pairk::PBM - 1) / pairk::PBM) * p.batch;
     int bn = 256;
-    const bool sk_ok = allow_sk && sk_worth(tiles_mb * ((p.N + 255) / 256), clusters_max, (p.K + BK - 1) / BK);
+    const bool small = allow_sk && sk_small(tiles_mb * ((p.N + 255) / 256), clusters_max, (p.K + BK - 1) / BK);
+    const bool sk_ok = small || (allow_sk && sk_worth(tiles_mb * ((p.N + 255) / 256), clusters_max,
+                                                      (p.K + BK - 1) / BK));
     long long best = -1;
     for (int cand = 256; cand >= 128 && !sk_ok; cand -= 64) {
         const long long t = tiles_mb * ((p.N + cand - 1) / cand);
@@ -1909,7 +1949,7 @@ cudaError_t launch_pair_typed(const ProblemEx &p, int clusters_max, int *status,
     args.status = status;
     args.stall = stall;
     if (stall) return launch_pair_cfg<T, F, false, false, false, true>(ta, tb, tc, tb, args, clusters, s);
-    return launch_pair_planned<T, F>(ta, tb, tc, tb, args, clusters, tiles, allow_sk, s);
+    return launch_pair_planned<T, F>(ta, tb, tc, tb, args, clusters, tiles, allow_sk, s, small ? clusters_max : 0);
 }
 
 // Z = SiLU(X W_g) * (X W_u): p.A = X [M,K], p.B = W_g [K,N], p.C = Z [M,N];

@@ -5,7 +5,9 @@ of the clusters) and K is long (at least 48 K-blocks), the K iterations of the
 remainder tiles are spread over the clusters and each such tile is the sum, in
 K order, of two to five FP32 partials.  The shapes below make 80 or 81 tiles,
 4 to 7 tiles past a full wave of the 74-76 CTA pairs of a GB300; two more make
-192 tiles, 40 past two waves, which run as whole tiles.  Checked: whole rows
+192 tiles, 40 past two waves, which run as whole tiles; four more are under a
+quarter of a wave with at least 64 K-blocks, and every one of their tiles is
+split.  Checked: whole rows
 from every quarter of both CTA halves of every 256-row band (so every tile,
 stream-K or not, is hit), and bit-identical results on a second run."""
 
@@ -45,6 +47,11 @@ CASES = [
     ("f16_cm", 2560, 2048, 3072),   # C^T = B^T A^T: 8 x 10 tiles
     ("bf16_rm", 1024, 12288, 2048), # 4 x 48 tiles: 40 in the last wave
     ("bf16_rm", 1000, 12040, 1032), # 4 x 48 tiles, ragged M, N and K
+    # problems under a quarter of a wave with long K: stream-K over every tile, 4 shares each
+    ("bf16_rm", 768, 768, 4096),    # 9 tiles on 36 clusters, 16 K-blocks per share
+    ("bf16_rm", 520, 776, 4104),    # 12 tiles of 65 K-blocks, ragged M, N and K: shares cross tiles
+    ("f16_cm", 1000, 520, 4104),    # C^T: 12 tiles of 65 K-blocks, shares of 17
+    ("bf16_rm", 256, 256, 4160),    # one tile, four shares
 ]
 
 
