@@ -294,3 +294,34 @@ def test_stream_k_tail_batched_alpha_beta(dtype, op_a, op_b):
                              beta, C0[b * sc:], ldc, 0, 1)
         out = widen(dtype, C1[b * sc: b * sc + M * ldc].reshape(M, ldc)[:, :N])[None]
         check(dtype, out, ref, K, alpha)
+
+@pytest.mark.parametrize("dtype,op_a,op_b", [("bf16", "N", "N"), ("f16", "T", "T")])
+def test_small_long_k_split_batched_alpha_beta(dtype, op_a, op_b):
+    """Two batches of 304 x 264 x 4160 make 8 pair tiles of 65 K-blocks: every
+    tile runs as stream-K over four clusters, and alpha and beta * old C are
+    applied once, after the partials are added.  Both batches and the padding
+    are checked."""
+    M, N, K, batch, alpha, beta = 304, 264, 4160, 2, 0.5, -1.25
+    a_r, a_c = (M, K) if op_a == "N" else (K, M)
+    b_r, b_c = (K, N) if op_b == "N" else (N, K)
+    lda, ldb, ldc = a_c + 8, b_c + 16, N + 8
+    sa, sb, sc = a_r * lda + 64, b_r * ldb + 32, M * ldc + 8
+    s0 = synthetic.seed_for(SEED, 0) + 8000
+    A = padded(dtype, a_r, a_c, lda, sa, batch, s0 + 100)
+    B = padded(dtype, b_r, b_c, ldb, sb, batch, s0 + 200)
+    C0 = padded(dtype, M, N, ldc, sc, batch, s0 + 300)
+    dA, dB, dC = dev(A), dev(B), dev(C0.copy())
+    launches = g.gemm_kernel_launches()
+    g.gemm_ex(dtype, "rm", op_a, op_b, M, N, K, alpha, dA, lda, sa, dB, ldb, sb, beta, dC, ldc, sc, batch)
+    assert g.gemm_last_kernel() == f"umma_ex_{dtype}"
+    assert g.gemm_kernel_launches() - launches == 2  # the pair kernel and the fix-up
+    g.gemm_synchronize()
+    C1 = host(dC, dtype)
+    for b in range(batch):
+        ref = oracle.gemm_ex(dtype, "rm", op_a, op_b, M, N, K, alpha, A[b * sa:], lda, 0, B[b * sb:], ldb, 0,
+                             beta, C0[b * sc:], ldc, 0, 1)
+        out = widen(dtype, C1[b * sc: b * sc + M * ldc].reshape(M, ldc)[:, :N])[None]
+        check(dtype, out, ref, K, alpha)
+        # the padding columns of C are left as they were
+        pad = C1[b * sc: b * sc + M * ldc].reshape(M, ldc)[:, N:]
+        assert np.array_equal(pad, C0[b * sc: b * sc + M * ldc].reshape(M, ldc)[:, N:])
