@@ -86,35 +86,35 @@ L2_BYTES = 129e6
 # removed: the family's file, or "file" where the kernel lives elsewhere), else
 # reported as null.
 TRAFFIC = {
-    "decode_bf16_rm_8x28672x4096": {"bytes": 238600704, "source": "58dc7414ad7d", "file": "skinny_wide.cu"},
-    "edge_bf16_rm_1000x1000x1000": {"bytes": 4046848, "source": "533bb04085d7"},
-    "edge_bf16_rm_1x12288x4096": {"bytes": 103698688, "source": "533bb04085d7"},
-    "edge_bf16_rm_32x12288x4096": {"bytes": 103910912, "source": "533bb04085d7"},
-    "edge_bf16_rm_64x64x64": {"bytes": 55040, "source": "533bb04085d7"},
-    "edge_bf16_rm_8192x4096x4096": {"bytes": 205875200, "source": "533bb04085d7"},
+    "decode_bf16_rm_8x28672x4096": {"bytes": 238219008, "source": "58dc7414ad7d", "file": "skinny_wide.cu"},
+    "edge_bf16_rm_1000x1000x1000": {"bytes": 4047360, "source": "2f4b56551425"},
+    "edge_bf16_rm_1x12288x4096": {"bytes": 103672576, "source": "2f4b56551425"},
+    "edge_bf16_rm_32x12288x4096": {"bytes": 103931136, "source": "2f4b56551425"},
+    "edge_bf16_rm_64x64x64": {"bytes": 55552, "source": "2f4b56551425"},
+    "edge_bf16_rm_8192x4096x4096": {"bytes": 209809152, "source": "2f4b56551425"},
     # the A rows staged into aligned rows (pad_rows_kernel), then the CTA pairs
-    "edge_bf16_rm_8192x4096x4100": {"bytes": 87155968 + 203320064, "source": "533bb04085d7"},
+    "edge_bf16_rm_8192x4096x4100": {"bytes": 87304704 + 206491392, "source": "2f4b56551425"},
     "edge_f32_rm_1000x1000x1000": {"bytes": 8025856, "source": "308e43d5575f"},
     "edge_f32_rm_1x12288x4096": {"bytes": 204522240, "source": "a821897d27f4"},
     "edge_f32_rm_64x64x64": {"bytes": 51968, "source": "308e43d5575f"},
     "edge_f32_rm_8192x4096x4096": {"bytes": 788443136, "source": "308e43d5575f"},
     "edge_f32_rm_8192x4096x4100": {"bytes": 790477056, "source": "308e43d5575f"},
-    "ffn_bf16_rm_1024x12288x4096": {"bytes": 121875712, "source": "533bb04085d7"},
-    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 231035136, "source": "533bb04085d7"},  # the fix-up kernel adds 4.2 MB
-    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23121664, "source": "533bb04085d7"},  # the quantiser moves 33.6 MB
-    "fp8_rowscale_e4m3_8192x8192x8192": {"bytes": 460958080, "source": "533bb04085d7"},  # the quantiser moves 166.2 MB
-    "fp8_rowscale_fused_e4m3_4096x1536x4096": {"bytes": 33560576 + 39923712, "source": "533bb04085d7"},  # the row amax pass, then the product
-    "fp8_rowscale_fused_e4m3_8192x8192x8192": {"bytes": 137389824 + 733416192, "source": "533bb04085d7"},  # the row amax pass, then the product
-    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1214928128, "source": "533bb04085d7"},
-    "gemm_ex_f16_rm_NN_batch32_1024x1024x1024": {"bytes": 173131520, "source": "533bb04085d7"},
+    "ffn_bf16_rm_1024x12288x4096": {"bytes": 121778176, "source": "2f4b56551425"},
+    "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 230824960, "source": "2f4b56551425"},  # the fix-up kernel adds 4.2 MB
+    "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120896, "source": "2f4b56551425"},  # the quantiser moves 33.6 MB
+    "fp8_rowscale_e4m3_8192x8192x8192": {"bytes": 455611264, "source": "2f4b56551425"},  # the quantiser moves 166.2 MB
+    "fp8_rowscale_fused_e4m3_4096x1536x4096": {"bytes": 33559808 + 39924224, "source": "2f4b56551425"},  # the row amax pass, then the product
+    "fp8_rowscale_fused_e4m3_8192x8192x8192": {"bytes": 137113856 + 729919488, "source": "2f4b56551425"},  # the row amax pass, then the product
+    "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1194888448, "source": "2f4b56551425"},
+    "gemm_ex_f16_rm_NN_batch32_1024x1024x1024": {"bytes": 172421632, "source": "2f4b56551425"},
     "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 386299392, "source": "308e43d5575f"},
-    "gemv_bf16_rm_1x12288x4100": {"bytes": 103923456, "source": "a821897d27f4"},
-    "hgemm_f16_cm_3072x5120x6144": {"bytes": 203479552, "source": "533bb04085d7"},  # the fix-up kernel adds 12.6 MB
-    "hgemm_f16_cm_8192": {"bytes": 1267071744, "source": "533bb04085d7"},
+    "gemv_bf16_rm_1x12288x4100": {"bytes": 103579904, "source": "a821897d27f4"},
+    "hgemm_f16_cm_3072x5120x6144": {"bytes": 207828736, "source": "2f4b56551425"},  # the fix-up kernel adds 12.6 MB
+    "hgemm_f16_cm_8192": {"bytes": 1171736320, "source": "2f4b56551425"},
     "sgemm_f32_rm_256": {"bytes": 543488, "source": "308e43d5575f"},
     # both grids of the call: the whole rounds and the half-K last round
     "sgemm_f32_rm_4096": {"bytes": 351713024 + 46196480, "source": "308e43d5575f"},
-    "single_cta_bf16_rm_128x12288x4096": {"bytes": 104856064, "source": "533bb04085d7"},
+    "single_cta_bf16_rm_128x12288x4096": {"bytes": 104717824, "source": "2f4b56551425"},
     "unaligned_f32_rm_4096x4096x4095": {"bytes": 384833280, "source": "308e43d5575f"},
 }
 
