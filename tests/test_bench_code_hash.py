@@ -43,3 +43,16 @@ def test_traffic_figures_and_profiles_name_the_same_captures():
     named = {h for _, h in pairs}
     for workload, t in bench.TRAFFIC.items():
         assert t["source"] in named, workload
+
+
+def test_every_default_workload_has_current_traffic():
+    """The committed traffic figures match the kernel files as they stand, so
+    that the default run reports a traffic figure for every workload it
+    measures (a kernel edit without a new capture would show up as null)."""
+    for workload in [bench.DEFAULT_WORKLOAD] + list(bench.DEFAULT_PATHS):
+        t = bench.TRAFFIC.get(workload)
+        assert t is not None, workload
+        current = {bench.file_hash(f) for f in set(bench.KERNEL_SOURCE.values())}
+        if "file" in t:
+            current = {bench.file_hash(t["file"])}
+        assert t["source"] in current, workload
