@@ -94,11 +94,11 @@ TRAFFIC = {
     "edge_bf16_rm_8192x4096x4096": {"bytes": 209809152, "source": "2f4b56551425"},
     # the A rows staged into aligned rows (pad_rows_kernel), then the CTA pairs
     "edge_bf16_rm_8192x4096x4100": {"bytes": 87304704 + 206491392, "source": "2f4b56551425"},
-    "edge_f32_rm_1000x1000x1000": {"bytes": 8025856, "source": "308e43d5575f"},
+    "edge_f32_rm_1000x1000x1000": {"bytes": 8025856, "source": "61cf656ecb0d"},
     "edge_f32_rm_1x12288x4096": {"bytes": 204522240, "source": "a821897d27f4"},
-    "edge_f32_rm_64x64x64": {"bytes": 51968, "source": "308e43d5575f"},
-    "edge_f32_rm_8192x4096x4096": {"bytes": 788443136, "source": "308e43d5575f"},
-    "edge_f32_rm_8192x4096x4100": {"bytes": 790477056, "source": "308e43d5575f"},
+    "edge_f32_rm_64x64x64": {"bytes": 52480, "source": "61cf656ecb0d"},
+    "edge_f32_rm_8192x4096x4096": {"bytes": 723894528 + 78944000, "source": "61cf656ecb0d"},
+    "edge_f32_rm_8192x4096x4100": {"bytes": 724274432 + 79040768, "source": "61cf656ecb0d"},
     "ffn_bf16_rm_1024x12288x4096": {"bytes": 121778176, "source": "2f4b56551425"},
     "ffn_gate_up_bf16_silu_mul_1024x12288x4096": {"bytes": 230824960, "source": "2f4b56551425"},  # the fix-up kernel adds 4.2 MB
     "fp8_rowscale_e4m3_4096x1536x4096": {"bytes": 23120896, "source": "2f4b56551425"},  # the quantiser moves 33.6 MB
@@ -107,15 +107,15 @@ TRAFFIC = {
     "fp8_rowscale_fused_e4m3_8192x8192x8192": {"bytes": 137113856 + 729919488, "source": "2f4b56551425"},  # the row amax pass, then the product
     "gemm_ex_bf16_rm_NT_8192x8192x8192": {"bytes": 1194888448, "source": "2f4b56551425"},
     "gemm_ex_f16_rm_NN_batch32_1024x1024x1024": {"bytes": 172421632, "source": "2f4b56551425"},
-    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 386299392, "source": "308e43d5575f"},
+    "gemm_ex_f32_rm_NT_4096x4096x4096": {"bytes": 387815680, "source": "61cf656ecb0d"},
     "gemv_bf16_rm_1x12288x4100": {"bytes": 103579904, "source": "a821897d27f4"},
     "hgemm_f16_cm_3072x5120x6144": {"bytes": 207828736, "source": "2f4b56551425"},  # the fix-up kernel adds 12.6 MB
     "hgemm_f16_cm_8192": {"bytes": 1171736320, "source": "2f4b56551425"},
-    "sgemm_f32_rm_256": {"bytes": 543488, "source": "308e43d5575f"},
+    "sgemm_f32_rm_256": {"bytes": 543744, "source": "61cf656ecb0d"},
     # both grids of the call: the whole rounds and the half-K last round
-    "sgemm_f32_rm_4096": {"bytes": 351713024 + 46196480, "source": "308e43d5575f"},
+    "sgemm_f32_rm_4096": {"bytes": 353438976 + 46182912, "source": "61cf656ecb0d"},
     "single_cta_bf16_rm_128x12288x4096": {"bytes": 104717824, "source": "2f4b56551425"},
-    "unaligned_f32_rm_4096x4096x4095": {"bytes": 384833280, "source": "308e43d5575f"},
+    "unaligned_f32_rm_4096x4096x4095": {"bytes": 384094976, "source": "61cf656ecb0d"},
 }
 
 KERNEL_SOURCE = {

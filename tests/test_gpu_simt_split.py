@@ -1,11 +1,11 @@
 """The packed-FMA SGEMM's split last round, against the oracle.
 
 A plain FP32 problem of at least one full round of resident CTAs (three
-128 x 64 tiles per SM) whose last round is at most half full, with at least 32
-K blocks of 16, runs as two grids: the whole rounds, then the remaining tiles
+128 x 64 tiles per SM) whose last round is part full, with at least 32 K
+blocks of 16, runs as two grids: the whole rounds, then the remaining tiles
 as clusters of two CTAs that each sum half of the K blocks and exchange their
-halves through distributed shared memory.  The shapes below leave 12 to 228
-tiles past full rounds on a 152-SM GB300.  Checked: whole rows from each
+halves through distributed shared memory.  The shapes below leave 12 to 405
+tiles past full rounds on a 152-SM GB300 (of 456 slots).  Checked: whole rows from each
 32-row quarter of every 128-row tile (the two CTAs of a cluster store
 alternate quarters), the ragged last tiles in M, N and K, bit-identical
 results on a second run, and back-to-back calls that read each other's C."""
@@ -47,7 +47,7 @@ def split_tail(M, N, K):
     slots = 3 * torch.cuda.get_device_properties(0).multi_processor_count
     tiles = -(-M // 128) * -(-N // 64)
     rem = tiles % slots
-    if tiles < slots or rem == 0 or 2 * rem > slots or -(-K // 16) < 32:
+    if tiles < slots or rem == 0 or -(-K // 16) < 32:
         return 0
     return rem
 
@@ -56,6 +56,8 @@ CASES = [
     (2300, 1660, 1000),   # 18 x 26 tiles: 12 past a round; ragged M, N and K (63 K blocks: 31 + 32)
     (2304, 2432, 2048),   # 18 x 38 tiles: 228 past a round, the largest tail
     (2048, 2560, 512),    # 16 x 40 tiles: 184 past a round, the shortest K (16 + 16 blocks)
+    (2560, 2560, 4096),   # 20 x 40 tiles: 344 past a round, more than half of it
+    (2600, 2600, 1000),   # 21 x 41 tiles: 405 past a round; ragged M, N and K
 ]
 
 
