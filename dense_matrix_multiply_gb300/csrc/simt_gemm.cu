@@ -302,7 +302,7 @@ simt_gemm_kernel(const TIn *__restrict__ A, const TIn *__restrict__ B, TOut *__r
 //     61.1 against 62.5 TFLOP/s at 4096^3).
 //   * A ring of three stages, one barrier per K step.  B is requested two steps
 //     ahead; A is loaded into registers one step before its store, so each load
-//     has a whole compute step to arrive.  160 registers: three CTAs per SM.
+//     has a whole compute step to arrive.  148 registers: three CTAs per SM.
 //   * Grouped rasterisation along M, predicated loads (zero fill) and stores.
 // Every product and sum is the scalar kernel's, in the same order, so the
 // results are bit-identical to it, except in a split last round (below).

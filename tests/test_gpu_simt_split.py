@@ -54,7 +54,7 @@ def split_tail(M, N, K):
 
 CASES = [
     (2300, 1660, 1000),   # 18 x 26 tiles: 12 past a round; ragged M, N and K (63 K blocks: 31 + 32)
-    (2304, 2432, 2048),   # 18 x 38 tiles: 228 past a round, the largest tail
+    (2304, 2432, 2048),   # 18 x 38 tiles: 228 past a round, exactly half of it
     (2048, 2560, 512),    # 16 x 40 tiles: 184 past a round, the shortest K (16 + 16 blocks)
     (2560, 2560, 4096),   # 20 x 40 tiles: 344 past a round, more than half of it
     (2600, 2600, 1000),   # 21 x 41 tiles: 405 past a round; ragged M, N and K
