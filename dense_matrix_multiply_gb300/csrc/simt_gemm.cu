@@ -692,10 +692,12 @@ cudaError_t launch_ffma2_split(const float *A, const float *B, float *C, int M, 
 // A plain FP32 problem whose 128 x 64 tiles would occupy at most a quarter of
 // the SMs (SGEMM 256^3 is 8 such tiles on 152 SMs) runs on 32 x 32 tiles
 // instead: sixteen times the CTAs, 64 threads each, 4 x 4 outputs per thread,
-// K step 16.  Measured on GB300 (back to back, operands from DRAM), small
-// kernel against the 128 x 64 one: 256^3 9.3 vs 13.6 us, 512^3 22.7 vs 26.6,
-// 300 x 520 x 272 12.8 vs 15.3, 64^3 3.2 vs 4.7; with more tiles the large
-// kernel wins (1000^3: 128 tiles, 50.5 vs 83.9 us).  The k-major A
+// K step 16.  Measured on GB300 (back to back over 64 copies of the operands,
+// which at 256^3 -- 49 MB -- stay in L2), small kernel against the 128 x 64
+// one: 256^3 9.3 vs 13.6 us, 512^3 22.7 vs 26.6, 300 x 520 x 272 12.8 vs 15.3,
+// 64^3 3.2 vs 4.7; with more tiles the large kernel wins (1000^3: 128 tiles,
+// 50.5 vs 83.9 us).  With every call's operands from DRAM, 256^3 takes 12.1-12.7
+// us: one K step of lookahead leaves most of a DRAM round trip exposed per step.  The k-major A
 // tile and the B tile are double-buffered in shared memory, the next K step
 // loaded into registers (16-byte loads) while the current one is multiplied;
 // one barrier per step.  Per k a thread makes one 16-byte shared load of A
